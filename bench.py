@@ -1,0 +1,405 @@
+#!/usr/bin/env python3
+"""Benchmark of the FP32 GEMM library on GB300: one JSON line on stdout.
+
+A step is one call of the library on the workload's synthetic inputs, already
+resident in HBM (default workload: M = N = K = 4096, alpha = 1, beta = 0,
+row-major, A and B uniform[-1, 1) from seed 2).  The L2 is flushed between
+timed steps by a 256 MiB memset outside the step's event pair.
+
+Reported, besides the contract keys:
+  roofline      the GEMM kernel against the CUDA-core FP32 peak
+                (SMs x 128 FMA/clk x 2 FLOP x 2070 MHz), "bound": "alu"
+  e2e           the same metric with pinned host buffers: H2D of A, B, the call,
+                D2H of C, every step
+  cpu_baseline  the FP64 oracle timed on this host's cores on a bounded sample
+                of the same problem (whole rows of C)
+  clocks        nvidia-smi samples taken during the timed region
+
+``--impl reference`` times the FP64 oracle instead (the only reference
+implementation this project has), each step a bounded sample of the workload.
+
+Under torchrun (WORLD_SIZE > 1) every rank runs its own copy of the workload
+(weak scaling, no data-path collective); the step time is the max over ranks
+and ``value`` counts the work of all ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from dense_fp32_gemm_sm_gb300 import workloads  # noqa: E402
+
+METRIC = "FP32 GEMM TFLOP/s (2*M*N*K/s) at 4096^3; fraction of GB300 FP32 peak"
+UNIT = "TFLOP/s"
+FMA_PER_CLK_PER_SM = 128  # FP32 lanes per SM
+STATED_SM_MHZ = 2070.0  # maximum SM clock of GB300
+L2_FLUSH_BYTES = 256 << 20
+# Best FP32 kernel of GPU架构下的矩阵乘法深入优化 at 4096^3 ("5. warp tiling + double
+# buffer", V100S-PCIE-32GB): 10642 GFLOPS.  Other hardware: context only.
+PAGES_4096_TFLOPS = 10.642
+SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("fgemm", "reference"), default="fgemm")
+    ap.add_argument("--workload", choices=workloads.WORKLOADS, default="square4096")
+    ap.add_argument("--config", type=int, default=-1,
+                    help="explicit kernel configuration id (default: the library's choice)")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ---- distributed plumbing (one process per GPU, replicas) -----------------------------------
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world):
+    if world > 1 and not torch.distributed.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        torch.distributed.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        torch.distributed.barrier()
+
+
+def aggregate(units: float, seconds: float, world: int, device=None):
+    """Sum of the ranks' units and max of their times (a no-op for one process)."""
+    if world <= 1:
+        return units, seconds
+    t = torch.tensor([units, seconds], dtype=torch.float64, device=device)
+    s = t.clone()
+    torch.distributed.all_reduce(s, op=torch.distributed.ReduceOp.SUM)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(s[0]), float(t[1])
+
+
+# ---- clocks -------------------------------------------------------------------------------
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+
+    def __init__(self, gpu_index: int, enabled: bool = True):
+        self.gpu_index, self.enabled = gpu_index, enabled
+        self.proc, self.path = None, None
+
+    def __enter__(self):
+        if self.enabled:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + SMI_FIELDS,
+                     "--format=csv,noheader,nounits", "-lms", "200"],
+                    stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                time.sleep(0.3)
+            except OSError:
+                self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) == 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        busy = [v for v in sm if mx and v > 0.5 * max(mx)] or sm
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(busy) if busy else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ---- the library arm ----------------------------------------------------------------------
+
+def stated_peak_tflops(device) -> tuple:
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    return sms * FMA_PER_CLK_PER_SM * 2 * STATED_SM_MHZ * 1e6 / 1e12, sms
+
+
+def _launch(fg, w, cfg, dA, dB, dC, dbias, stream):
+    """One step: the library call of the workload (the bench's unit of work)."""
+    nb = max(1, w.batch)
+    sA = w.M * w.K if w.batch else 0
+    sB = w.N * w.K if w.batch else 0
+    sC = w.M * w.N if w.batch else 0
+    if cfg >= 0:
+        fg.gemm_explicit(cfg, w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, sA, dB, w.ldb, sB,
+                         w.beta, dC, w.ldc, sC, nb, dbias, w.relu, stream=stream)
+    elif w.batch:
+        fg.sgemm_strided_batched(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, sA, dB, w.ldb, sB,
+                                 w.beta, dC, w.ldc, sC, w.batch, stream=stream)
+    elif w.bias is not None or w.relu:
+        fg.sgemm_bias_relu(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, dB, w.ldb, w.beta, dC,
+                           w.ldc, dbias, w.relu, stream=stream)
+    else:
+        fg.sgemm(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, dB, w.ldb, w.beta, dC, w.ldc,
+                 stream=stream)
+
+
+def cpu_baseline(w, seconds: float):
+    """FP64 oracle on whole rows of C (all columns), sized to take about `seconds`."""
+    import oracle
+    threads = oracle.default_threads()
+    A = w.A.numpy().reshape(-1) if not w.batch else w.A[0].numpy().reshape(-1)
+    B = w.B.numpy().reshape(-1) if not w.batch else w.B[0].numpy().reshape(-1)
+    C0 = None if w.C0 is None else w.C0.numpy().reshape(-1)
+
+    def timed(rows):
+        t0 = time.perf_counter()
+        oracle.gemm(w.ta, w.tb, w.M, w.N, w.K, w.alpha, A, w.lda, B, w.ldb, w.beta, C0, w.ldc,
+                    bias=w.bias, relu=w.relu, rows=rows, threads=threads, want_mag=False)
+        return time.perf_counter() - t0
+
+    probe = min(w.M, max(threads, 8))
+    t_probe = timed(list(range(probe)))
+    n = int(min(w.M, max(probe, seconds / max(t_probe, 1e-9) * probe)))
+    n = max(threads, (n // threads) * threads) if n >= threads else n
+    t = timed(list(range(n)))
+    flops = 2.0 * n * w.N * w.K
+    return {"value": flops / t / 1e12, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": "%d of %d rows of C (all %d columns)%s, FP64 oracle, %.1f s" % (
+                n, w.M, w.N, " of problem 0 of %d" % w.batch if w.batch else "", t)}
+
+
+def run_fgemm(args, rank, world, local_rank):
+    import dense_fp32_gemm_sm_gb300 as fg
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device; the library has no CPU path")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    fg.library()
+    w = workloads.make(args.workload)
+    stream = torch.cuda.Stream(dev)
+    sh = stream.cuda_stream
+
+    dA, dB = w.A.to(dev), w.B.to(dev)
+    dbias = w.bias.to(dev) if w.bias is not None else None
+    c_shape = (max(1, w.batch), w.M, w.N) if w.batch else (w.M, w.N)
+    dC = torch.zeros(c_shape, device=dev)
+    dC0 = w.C0.to(dev) if w.C0 is not None else None
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    torch.cuda.synchronize()
+
+    def step():
+        if dC0 is not None:  # beta != 0: restore C so every step computes the same thing
+            dC.copy_(dC0)
+        _launch(fg, w, args.config, dA, dB, dC, dbias, sh)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    n_batch_launches = (max(1, w.batch) + 65534) // 65535
+    sampler = ClockSampler(local_rank, enabled=not args.no_clocks)
+    barrier(world)
+    torch.cuda.synchronize()
+    with sampler, torch.cuda.stream(stream):
+        wall0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()  # evict A, B, C from L2 (outside the event pair)
+            if dC0 is not None:
+                dC.copy_(dC0)
+            starts[i].record(stream)
+            _launch(fg, w, args.config, dA, dB, dC, dbias, sh)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier(world)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    local_s = sum(step_ms) / 1e3
+    total_flops, max_s = aggregate(w.flops * args.steps, local_s, world,
+                                   dev if world > 1 else None)
+    value = total_flops / max_s / 1e12
+    kernel_ms = statistics.mean(step_ms)
+    peak, sms = stated_peak_tflops(dev)
+    achieved = w.flops / (kernel_ms / 1e3) / 1e12
+
+    # End to end: pinned host inputs -> device, the call, result -> pinned host.
+    hA, hB = w.A.pin_memory(), w.B.pin_memory()
+    hC = torch.empty(c_shape, dtype=torch.float32).pin_memory()
+    hC0 = w.C0.pin_memory() if w.C0 is not None else None
+    h2d = hA.numel() * 4 + hB.numel() * 4 + (hC0.numel() * 4 if hC0 is not None else 0)
+    d2h = hC.numel() * 4
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        for it in range(args.e2e_steps + 2):
+            if it == 2:
+                e_start.record(stream)
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            if hC0 is not None:
+                dC.copy_(hC0, non_blocking=True)
+            _launch(fg, w, args.config, dA, dB, dC, dbias, sh)
+            hC.copy_(dC, non_blocking=True)
+        e_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_s = e_start.elapsed_time(e_end) / 1e3 / args.e2e_steps
+    e2e_flops, e2e_max = aggregate(w.flops, e2e_s, world, dev if world > 1 else None)
+
+    chosen = args.config
+    if chosen < 0:
+        aligned = True
+        chosen = fg.select_config(w.ta, w.tb, w.M, w.N, w.K, max(1, w.batch), aligned, sms)
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_s * 1e3 /
+                                                                          args.steps, 5),
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": (round(value / PAGES_4096_TFLOPS, 3)
+                        if args.workload == "square4096" else None),
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": describe(w), "kernel_config": fg.config_name(chosen),
+                   "l2": "flushed between steps (256 MiB memset outside the timed event pair)",
+                   "parallelism": "replicas" if world > 1 else "single GPU"},
+        "gpu_launches": args.steps * n_batch_launches,
+        "roofline": {"bound": "alu", "achieved": round(achieved, 4), "peak": round(peak, 3),
+                     "unit": UNIT, "frac": round(achieved / peak, 4), "traffic": None,
+                     "peak_source": "derived: %d SMs x %d FP32 FMA/clk x 2 FLOP x %.0f MHz" % (
+                         sms, FMA_PER_CLK_PER_SM, STATED_SM_MHZ)},
+        "e2e": {"value": round(e2e_flops / e2e_max / 1e12, 4), "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "wall_s_timed_region": round(wall, 3),
+    }
+    clk = sampler.summary()
+    if clk is not None:
+        line["clocks"] = clk
+        if clk.get("sm_mhz"):
+            line["roofline"]["frac_at_measured_clock"] = round(
+                achieved / (peak * clk["sm_mhz"] / STATED_SM_MHZ), 4)
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    return line
+
+
+def describe(w):
+    s = "%s: M=%d N=%d K=%d alpha=%g beta=%g op(A)=%s op(B)=%s" % (
+        w.name, w.M, w.N, w.K, w.alpha, w.beta, "T" if w.ta else "N", "T" if w.tb else "N")
+    if w.batch:
+        s += " batch=%d" % w.batch
+    if w.bias is not None:
+        s += " +bias"
+    if w.relu:
+        s += " +ReLU"
+    return s + ", seed %d" % w.seed
+
+
+# ---- the reference arm: the FP64 oracle on host cores ------------------------------------
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    w = workloads.make(args.workload)
+    threads = oracle.default_threads()
+    A = (w.A[0] if w.batch else w.A).numpy().reshape(-1)
+    B = (w.B[0] if w.batch else w.B).numpy().reshape(-1)
+    C0 = None if w.C0 is None else w.C0.numpy().reshape(-1)
+    # each step: whole rows of C, sized so the whole run stays within a few minutes
+    budget_s = 120.0
+    per_step = budget_s / max(1, args.steps + args.warmup)
+    t0 = time.perf_counter()
+    oracle.gemm(w.ta, w.tb, w.M, w.N, w.K, w.alpha, A, w.lda, B, w.ldb, w.beta, C0, w.ldc,
+                bias=w.bias, relu=w.relu, rows=list(range(min(w.M, threads))), threads=threads,
+                want_mag=False)
+    t_row = (time.perf_counter() - t0) / min(w.M, threads)
+    rows = int(max(1, min(w.M, per_step / max(t_row, 1e-9))))
+    rows = min(w.M, max(threads, rows - rows % threads))
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        oracle.gemm(w.ta, w.tb, w.M, w.N, w.K, w.alpha, A, w.lda, B, w.ldb, w.beta, C0, w.ldc,
+                    bias=w.bias, relu=w.relu, rows=list(range(rows)), threads=threads,
+                    want_mag=False)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    flops = 2.0 * rows * w.N * w.K
+    value = flops * len(times) / sum(times) / 1e12
+    sample = "%d of %d rows of C (all %d columns) per step, FP64 oracle" % (rows, w.M, w.N)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sum(times) / len(times) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": describe(w), "sample": sample},
+        "cpu_baseline": {"value": round(value, 6), "unit": UNIT, "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 6), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    rank, world, local_rank = dist_env()
+    if args.gpus != world and world > 1:
+        print("bench.py: --gpus %d but WORLD_SIZE %d" % (args.gpus, world), file=sys.stderr)
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        dist_init(world)
+        line = run_fgemm(args, rank, world, local_rank)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1 and torch.distributed.is_initialized():
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,25 @@
+"""fgemm: single-GPU FP32 GEMM for NVIDIA GB300 (sm_103a), hand-written CUDA kernels.
+
+The product is the C-ABI shared library ``libfgemm.so`` (declared in
+``include/fgemm.h``).  This package is its thin Python binding: the functions
+below marshal arguments and call the library; all work runs in its kernels.
+"""
+
+from ._binding import (  # noqa: F401
+    ERR_INVALID_VALUE,
+    ERR_LAUNCH,
+    ERR_NOT_SUPPORTED,
+    OK,
+    OP_N,
+    OP_T,
+    FgemmError,
+    config_name,
+    gemm_explicit,
+    library,
+    num_configs,
+    select_config,
+    sgemm,
+    sgemm_bias_relu,
+    sgemm_strided_batched,
+    status_string,
+)

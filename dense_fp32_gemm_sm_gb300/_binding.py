@@ -1,0 +1,158 @@
+"""ctypes binding of the C ABI declared in ``include/fgemm.h``.
+
+Argument marshalling only: every call goes straight to ``libfgemm.so`` and the
+work runs in its CUDA kernels.  Matrices may be given as CUDA float32 torch
+tensors (their ``data_ptr()`` is passed) or as raw device addresses (ints).
+When no stream is given and a tensor is passed, torch's current stream on that
+tensor's device is used; otherwise the legacy default stream (0).
+
+There is no CPU fallback: if the library cannot be built or loaded, every call
+raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import _build
+
+OP_N, OP_T = 0, 1
+OK, ERR_INVALID_VALUE, ERR_LAUNCH, ERR_NOT_SUPPORTED = 0, 1, 2, 3
+
+_lock = threading.Lock()
+_lib = None
+
+_c_int, _c_float, _c_ll, _c_vp = ctypes.c_int, ctypes.c_float, ctypes.c_longlong, ctypes.c_void_p
+
+
+class FgemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s" % (where, status_string(status)))
+
+
+def library() -> ctypes.CDLL:
+    """Load (building first if the sources are newer) ``libfgemm.so``."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build()
+            lib = ctypes.CDLL(path)
+            sig = {
+                "fgemm_sgemm": [_c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_vp, _c_int,
+                                _c_vp, _c_int, _c_float, _c_vp, _c_int, _c_vp],
+                "fgemm_sgemm_bias_relu": [_c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_vp,
+                                          _c_int, _c_vp, _c_int, _c_float, _c_vp, _c_int, _c_vp,
+                                          _c_int, _c_vp],
+                "fgemm_sgemm_strided_batched": [_c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                                _c_vp, _c_int, _c_ll, _c_vp, _c_int, _c_ll,
+                                                _c_float, _c_vp, _c_int, _c_ll, _c_int, _c_vp],
+                "fgemm_gemm_explicit": [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                        _c_vp, _c_int, _c_ll, _c_vp, _c_int, _c_ll, _c_float,
+                                        _c_vp, _c_int, _c_ll, _c_int, _c_vp, _c_int, _c_vp],
+                "fgemm_select_config": [_c_int] * 8,
+                "fgemm_num_configs": [],
+                "fgemm_config_name": [_c_int],
+                "fgemm_status_string": [_c_int],
+            }
+            for name, argtypes in sig.items():
+                fn = getattr(lib, name)
+                fn.argtypes = argtypes
+                fn.restype = _c_int
+            lib.fgemm_config_name.restype = ctypes.c_char_p
+            lib.fgemm_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x or None
+    if hasattr(x, "data_ptr"):
+        if x.numel() and (not x.is_cuda or x.dtype.itemsize != 4 or not x.is_floating_point()):
+            raise TypeError("fgemm takes CUDA float32 tensors (got %s on %s)" % (x.dtype, x.device))
+        return x.data_ptr() or None
+    raise TypeError("expected a CUDA tensor or a device address, got %r" % type(x))
+
+
+def _stream(stream, *tensors):
+    if stream is None:
+        for t in tensors:
+            if hasattr(t, "is_cuda") and t.is_cuda:
+                import torch
+                return torch.cuda.current_stream(t.device).cuda_stream
+        return None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream  # a torch.cuda.Stream
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise FgemmError(status, where)
+
+
+def status_string(status: int) -> str:
+    return library().fgemm_status_string(int(status)).decode()
+
+
+def num_configs() -> int:
+    return library().fgemm_num_configs()
+
+
+def config_name(config: int):
+    name = library().fgemm_config_name(int(config))
+    return name.decode() if name else None
+
+
+def select_config(transa, transb, M, N, K, batch, aligned, num_sms) -> int:
+    return library().fgemm_select_config(int(transa), int(transb), M, N, K, batch,
+                                         1 if aligned else 0, num_sms)
+
+
+def sgemm(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None,
+          check=True) -> int:
+    """``fgemm_sgemm``: C = alpha*op(A)*op(B) + beta*C (row-major, see include/fgemm.h)."""
+    st = library().fgemm_sgemm(int(transa), int(transb), M, N, K, alpha, _ptr(A), lda, _ptr(B),
+                               ldb, beta, _ptr(C), ldc, _stream(stream, C, A, B))
+    if check:
+        _check(st, "fgemm_sgemm")
+    return st
+
+
+def sgemm_bias_relu(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias,
+                    apply_relu, stream=None, check=True) -> int:
+    """``fgemm_sgemm_bias_relu``: C = relu?(alpha*op(A)*op(B) + beta*C + bias[col])."""
+    st = library().fgemm_sgemm_bias_relu(int(transa), int(transb), M, N, K, alpha, _ptr(A), lda,
+                                         _ptr(B), ldb, beta, _ptr(C), ldc, _ptr(bias),
+                                         1 if apply_relu else 0, _stream(stream, C, A, B))
+    if check:
+        _check(st, "fgemm_sgemm_bias_relu")
+    return st
+
+
+def sgemm_strided_batched(transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta,
+                          C, ldc, strideC, batch, stream=None, check=True) -> int:
+    """``fgemm_sgemm_strided_batched``: the plain GEMM on batch offsets b*stride."""
+    st = library().fgemm_sgemm_strided_batched(
+        int(transa), int(transb), M, N, K, alpha, _ptr(A), lda, strideA, _ptr(B), ldb, strideB,
+        beta, _ptr(C), ldc, strideC, batch, _stream(stream, C, A, B))
+    if check:
+        _check(st, "fgemm_sgemm_strided_batched")
+    return st
+
+
+def gemm_explicit(config, transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta,
+                  C, ldc, strideC, batch, bias=None, apply_relu=False, stream=None,
+                  check=True) -> int:
+    """``fgemm_gemm_explicit``: every option, with an explicit kernel configuration."""
+    st = library().fgemm_gemm_explicit(
+        int(config), int(transa), int(transb), M, N, K, alpha, _ptr(A), lda, strideA, _ptr(B), ldb,
+        strideB, beta, _ptr(C), ldc, strideC, batch, _ptr(bias), 1 if apply_relu else 0,
+        _stream(stream, C, A, B))
+    if check:
+        _check(st, "fgemm_gemm_explicit")
+    return st

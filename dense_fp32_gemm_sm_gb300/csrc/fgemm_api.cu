@@ -1,0 +1,281 @@
+// fgemm_api.cu -- the C ABI: argument validation, kernel selection, dispatch.
+//
+// Validation and selection are plain host integer code and run before any CUDA
+// call, so an invalid call never touches the device (and can be tested on a
+// machine without a GPU).  The launcher pattern (build grid/block, launch on the
+// caller's stream, then check the launch) is the host side of every listing in
+// GPU架构下的矩阵乘法深入优化 ("CUDA_CHECK(cudaPeekAtLastError())"), turned into
+// status codes because a library must not abort its caller.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdint>
+
+#include "fgemm_internal.h"
+#include "simt_gemm.cuh"
+
+namespace fgemm {
+
+const ConfigInfo kConfigs[NUM_CONFIGS] = {
+    {"simt_128x128x16_t8x8_s4", 128, 128, true},
+    {"simt_128x64x16_t8x8_s4", 128, 64, true},
+    {"simt_64x64x16_t4x4_s4", 64, 64, true},
+    {"simt_64x64x16_t4x4_s4_scalar", 64, 64, false},
+};
+
+namespace {
+
+struct Problem {
+    int ta, tb, M, N, K;
+    float alpha, beta;
+    const float *A;
+    long long lda, sA;
+    const float *B;
+    long long ldb, sB;
+    float *C;
+    long long ldc, sC;
+    int batch;
+    const float *bias;
+    int relu;
+    cudaStream_t stream;
+};
+
+long long floor_div(long long a, long long b)
+{
+    long long q = a / b;
+    if ((a % b != 0) && ((a < 0) != (b < 0))) --q;
+    return q;
+}
+
+// True when two different problems of the batch would write the same element
+// of C: (b - b') * sC == di * ldc + dj with |di| < M, |dj| < N for some b != b'.
+bool c_batches_overlap(long long M, long long N, long long ldc, long long sC, long long batch)
+{
+    if (batch <= 1) return false;
+    if (sC >= (M - 1) * ldc + N) return false;  // consecutive problems are disjoint ranges
+    const long long reach = (M - 1) * ldc + N;  // |offset| of any two elements of one problem < reach
+    for (long long d = 1; d < batch; ++d) {
+        const long long x = d * sC;
+        if (x >= reach) break;  // every later problem starts beyond this one's last element
+        const long long q = floor_div(x, ldc);
+        for (long long di = q; di <= q + 1; ++di) {
+            const long long dj = x - di * ldc;
+            if (di > -M && di < M && dj > -N && dj < N) return true;
+        }
+    }
+    return false;
+}
+
+// Returns FGEMM_OK when the problem is valid.  Sets *noop when nothing has to run.
+fgemm_status validate(const Problem &p, bool *noop)
+{
+    *noop = false;
+    if (p.ta != 0 && p.ta != 1) return FGEMM_ERR_INVALID_VALUE;
+    if (p.tb != 0 && p.tb != 1) return FGEMM_ERR_INVALID_VALUE;
+    if (p.M < 0 || p.N < 0 || p.K < 0 || p.batch < 0) return FGEMM_ERR_INVALID_VALUE;
+    const long long a_cols = p.ta ? p.M : p.K;  // stored row length of A
+    const long long b_cols = p.tb ? p.K : p.N;
+    if (p.lda < (a_cols > 1 ? a_cols : 1)) return FGEMM_ERR_INVALID_VALUE;
+    if (p.ldb < (b_cols > 1 ? b_cols : 1)) return FGEMM_ERR_INVALID_VALUE;
+    if (p.ldc < (p.N > 1 ? p.N : 1)) return FGEMM_ERR_INVALID_VALUE;
+    if (p.sA < 0 || p.sB < 0 || p.sC < 0) return FGEMM_ERR_INVALID_VALUE;
+    if (p.M == 0 || p.N == 0 || p.batch == 0) {
+        *noop = true;
+        return FGEMM_OK;
+    }
+    const bool products = p.K > 0 && p.alpha != 0.0f;
+    if (products && (p.A == nullptr || p.B == nullptr)) return FGEMM_ERR_INVALID_VALUE;
+    if (p.C == nullptr) return FGEMM_ERR_INVALID_VALUE;
+    if (c_batches_overlap(p.M, p.N, p.ldc, p.sC, p.batch)) return FGEMM_ERR_INVALID_VALUE;
+    return FGEMM_OK;
+}
+
+bool aligned16(const void *ptr, long long ld, long long stride, int batch)
+{
+    if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0) return false;
+    if (ld % 4 != 0) return false;
+    if (batch > 1 && stride % 4 != 0) return false;
+    return true;
+}
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+int select_config(int ta, int tb, long long M, long long N, long long K, long long batch, bool aligned,
+                  int num_sms)
+{
+    (void)ta;
+    (void)tb;
+    (void)K;
+    if (!aligned) return CFG_64x64_SCALAR;
+    if (num_sms < 1) num_sms = 1;
+    const long long b = batch > 0 ? batch : 1;
+    if (ceil_div(M, 128) * ceil_div(N, 128) * b >= num_sms) return CFG_128x128;
+    if (ceil_div(M, 128) * ceil_div(N, 64) * b >= num_sms) return CFG_128x64;
+    return CFG_64x64;
+}
+
+int device_sm_count(int *out)
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    const int slot = dev & 63;
+    int v = cache[slot].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return -1;
+        cache[slot].store(v, std::memory_order_relaxed);
+    }
+    *out = v;
+    return 0;
+}
+
+fgemm_status run(int config, const Problem &p)
+{
+    bool noop = false;
+    fgemm_status st = validate(p, &noop);
+    if (st != FGEMM_OK || noop) return st;
+    if (config >= NUM_CONFIGS) return FGEMM_ERR_INVALID_VALUE;
+
+    const bool products = p.K > 0 && p.alpha != 0.0f;
+    const bool aligned = !products || (aligned16(p.A, p.lda, p.sA, p.batch) &&
+                                       aligned16(p.B, p.ldb, p.sB, p.batch));
+    if (config < 0) {
+        int sms = 0;
+        if (device_sm_count(&sms) != 0) {
+            (void)cudaGetLastError();
+            return FGEMM_ERR_LAUNCH;
+        }
+        config = select_config(p.ta, p.tb, p.M, p.N, p.K, p.batch, aligned, sms);
+    }
+    if (kConfigs[config].needs_vec && !aligned) return FGEMM_ERR_NOT_SUPPORTED;
+
+    GemmParams g{};
+    g.A = products ? p.A : nullptr;
+    g.B = products ? p.B : nullptr;
+    g.C = p.C;
+    g.bias = p.bias;
+    g.lda = p.lda;
+    g.ldb = p.ldb;
+    g.ldc = p.ldc;
+    g.strideA = p.batch > 1 ? p.sA : 0;
+    g.strideB = p.batch > 1 ? p.sB : 0;
+    g.strideC = p.batch > 1 ? p.sC : 0;
+    g.M = p.M;
+    g.N = p.N;
+    g.K = products ? p.K : 0;
+    g.alpha = p.alpha;
+    g.beta = p.beta;
+    g.relu = p.relu ? 1 : 0;
+    g.c_vec = aligned16(p.C, p.ldc, p.sC, p.batch) ? 1 : 0;
+
+    const LaunchFn *table = p.ta ? (p.tb ? kLaunchTT : kLaunchTN) : (p.tb ? kLaunchNT : kLaunchNN);
+    return table[config](g, p.batch, p.stream);
+}
+
+Problem make_problem(fgemm_op ta, fgemm_op tb, int M, int N, int K, float alpha, const float *A,
+                     int lda, long long sA, const float *B, int ldb, long long sB, float beta,
+                     float *C, int ldc, long long sC, int batch, const float *bias, int relu,
+                     cudaStream_t stream)
+{
+    Problem p;
+    p.ta = (int)ta;
+    p.tb = (int)tb;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.alpha = alpha;
+    p.beta = beta;
+    p.A = A;
+    p.lda = lda;
+    p.sA = sA;
+    p.B = B;
+    p.ldb = ldb;
+    p.sB = sB;
+    p.C = C;
+    p.ldc = ldc;
+    p.sC = sC;
+    p.batch = batch;
+    p.bias = bias;
+    p.relu = relu;
+    p.stream = stream;
+    return p;
+}
+
+}  // namespace
+}  // namespace fgemm
+
+using fgemm::make_problem;
+using fgemm::run;
+
+extern "C" {
+
+fgemm_status fgemm_sgemm(fgemm_op transa, fgemm_op transb, int M, int N, int K, float alpha,
+                         const float *A, int lda, const float *B, int ldb, float beta, float *C,
+                         int ldc, cudaStream_t stream)
+{
+    return run(-1, make_problem(transa, transb, M, N, K, alpha, A, lda, 0, B, ldb, 0, beta, C, ldc,
+                                0, 1, nullptr, 0, stream));
+}
+
+fgemm_status fgemm_sgemm_bias_relu(fgemm_op transa, fgemm_op transb, int M, int N, int K,
+                                   float alpha, const float *A, int lda, const float *B, int ldb,
+                                   float beta, float *C, int ldc, const float *bias,
+                                   int apply_relu, cudaStream_t stream)
+{
+    return run(-1, make_problem(transa, transb, M, N, K, alpha, A, lda, 0, B, ldb, 0, beta, C, ldc,
+                                0, 1, bias, apply_relu, stream));
+}
+
+fgemm_status fgemm_sgemm_strided_batched(fgemm_op transa, fgemm_op transb, int M, int N, int K,
+                                         float alpha, const float *A, int lda, long long strideA,
+                                         const float *B, int ldb, long long strideB, float beta,
+                                         float *C, int ldc, long long strideC, int batch,
+                                         cudaStream_t stream)
+{
+    return run(-1, make_problem(transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, strideB,
+                                beta, C, ldc, strideC, batch, nullptr, 0, stream));
+}
+
+fgemm_status fgemm_gemm_explicit(int config, fgemm_op transa, fgemm_op transb, int M, int N,
+                                 int K, float alpha, const float *A, int lda, long long strideA,
+                                 const float *B, int ldb, long long strideB, float beta, float *C,
+                                 int ldc, long long strideC, int batch, const float *bias,
+                                 int apply_relu, cudaStream_t stream)
+{
+    return run(config < 0 ? -1 : config,
+               make_problem(transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta,
+                            C, ldc, strideC, batch, bias, apply_relu, stream));
+}
+
+const char *fgemm_status_string(fgemm_status status)
+{
+    switch (status) {
+    case FGEMM_OK: return "FGEMM_OK: success";
+    case FGEMM_ERR_INVALID_VALUE: return "FGEMM_ERR_INVALID_VALUE: an argument is out of range";
+    case FGEMM_ERR_LAUNCH: return "FGEMM_ERR_LAUNCH: a CUDA call or kernel launch failed";
+    case FGEMM_ERR_NOT_SUPPORTED:
+        return "FGEMM_ERR_NOT_SUPPORTED: the configuration cannot run this call";
+    }
+    return "unknown fgemm_status";
+}
+
+int fgemm_num_configs(void) { return fgemm::NUM_CONFIGS; }
+
+const char *fgemm_config_name(int config)
+{
+    if (config < 0 || config >= fgemm::NUM_CONFIGS) return nullptr;
+    return fgemm::kConfigs[config].name;
+}
+
+int fgemm_select_config(fgemm_op transa, fgemm_op transb, int M, int N, int K, int batch,
+                        int aligned, int num_sms)
+{
+    if ((transa != FGEMM_OP_N && transa != FGEMM_OP_T) ||
+        (transb != FGEMM_OP_N && transb != FGEMM_OP_T) || M < 0 || N < 0 || K < 0 || batch < 0)
+        return -1;
+    return fgemm::select_config((int)transa, (int)transb, M, N, K, batch, aligned != 0, num_sms);
+}
+
+}  // extern "C"

@@ -1,0 +1,39 @@
+// fgemm_internal.h -- declarations shared by the C-ABI layer and the kernel
+// instantiation units (host code only; no device code here).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "../../include/fgemm.h"
+
+namespace fgemm {
+
+struct GemmParams;
+
+// A launcher runs one configuration over `batch` problems (blockIdx.z) on a stream.
+using LaunchFn = fgemm_status (*)(const GemmParams &p, int batch, cudaStream_t stream);
+
+// Kernel configurations.  Ids are part of the test/bench interface.
+enum ConfigId {
+    CFG_128x128 = 0,        // 128x128x16 CTA tile, 8x8 per thread, 4-stage cp.async ring
+    CFG_128x64 = 1,         // 128x64x16, 8x8 per thread, 4 stages (more CTAs for mid sizes)
+    CFG_64x64 = 2,          // 64x64x16, 4x4 per thread, 4 stages (small problems)
+    CFG_64x64_SCALAR = 3,   // 64x64x16 with element-wise copies: any alignment
+    NUM_CONFIGS = 4,
+};
+
+struct ConfigInfo {
+    const char *name;
+    int bm, bn;
+    bool needs_vec;  // requires 16-byte aligned A/B, lda/ldb and batch strides
+};
+
+extern const ConfigInfo kConfigs[NUM_CONFIGS];
+
+// Launch tables, one per transpose combination (defined in inst_<ta><tb>.cu).
+extern const LaunchFn kLaunchNN[NUM_CONFIGS];
+extern const LaunchFn kLaunchNT[NUM_CONFIGS];
+extern const LaunchFn kLaunchTN[NUM_CONFIGS];
+extern const LaunchFn kLaunchTT[NUM_CONFIGS];
+
+}  // namespace fgemm

@@ -1,0 +1,92 @@
+// simt_launch.cuh -- host launchers for the SIMT kernel configurations.
+#pragma once
+
+#include <atomic>
+#include <climits>
+
+#include "fgemm_internal.h"
+#include "simt_gemm.cuh"
+
+namespace fgemm {
+
+// The tile shapes behind each ConfigId.  The lane arrangement follows the B
+// layout: a warp is 8 x 4 lanes when B is N-contiguous (so each thread stores
+// float4 runs of C) and 4 x 8 lanes when B is K-contiguous (so a warp's scalar
+// stores cover 32-byte runs of a row).
+template <int ID, int TA, int TB>
+struct ConfigOf;
+
+template <int TA, int TB>
+struct ConfigOf<CFG_128x128, TA, TB> {
+    using type = SimtCfg<128, 128, 16, TB ? 32 : 64, TB ? 64 : 32, 8, 8, 4, 1, TA, TB, true>;
+};
+template <int TA, int TB>
+struct ConfigOf<CFG_128x64, TA, TB> {
+    using type = SimtCfg<128, 64, 16, TB ? 32 : 64, TB ? 64 : 32, 8, 8, 4, 2, TA, TB, true>;
+};
+template <int TA, int TB>
+struct ConfigOf<CFG_64x64, TA, TB> {
+    using type = SimtCfg<64, 64, 16, TB ? 16 : 32, TB ? 32 : 16, 4, 4, 4, 2, TA, TB, true>;
+};
+template <int TA, int TB>
+struct ConfigOf<CFG_64x64_SCALAR, TA, TB> {
+    using type = SimtCfg<64, 64, 16, TB ? 16 : 32, TB ? 32 : 16, 4, 4, 4, 2, TA, TB, false>;
+};
+
+// Opt the kernel in to its dynamic shared memory once per device.
+template <class Cfg>
+static cudaError_t prepare_kernel()
+{
+    static std::atomic<unsigned long long> ready{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (ready.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(simt_gemm_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(simt_gemm_kernel<Cfg>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             100);
+    if (e != cudaSuccess) return e;
+    ready.fetch_or(bit, std::memory_order_acq_rel);
+    return cudaSuccess;
+}
+
+template <class Cfg>
+static fgemm_status launch_simt(const GemmParams &p0, int batch, cudaStream_t stream)
+{
+    GemmParams p = p0;
+    p.tiles_m = (p.M + Cfg::BM - 1) / Cfg::BM;
+    p.tiles_n = (p.N + Cfg::BN - 1) / Cfg::BN;
+    const long long tiles = (long long)p.tiles_m * p.tiles_n;
+    if (tiles > INT_MAX) return FGEMM_ERR_NOT_SUPPORTED;
+    if (prepare_kernel<Cfg>() != cudaSuccess) {
+        (void)cudaGetLastError();
+        return FGEMM_ERR_LAUNCH;
+    }
+    const int kMaxZ = 65535;
+    for (int b0 = 0; b0 < batch; b0 += kMaxZ) {
+        const int nb = batch - b0 < kMaxZ ? batch - b0 : kMaxZ;
+        GemmParams q = p;
+        if (b0) {
+            if (q.A) q.A += (long long)b0 * q.strideA;
+            if (q.B) q.B += (long long)b0 * q.strideB;
+            q.C += (long long)b0 * q.strideC;
+        }
+        simt_gemm_kernel<Cfg><<<dim3((unsigned)tiles, 1, (unsigned)nb), Cfg::THREADS,
+                                Cfg::SMEM_BYTES, stream>>>(q);
+        if (cudaGetLastError() != cudaSuccess) return FGEMM_ERR_LAUNCH;
+    }
+    return FGEMM_OK;
+}
+
+#define FGEMM_LAUNCH_TABLE(NAME, TA, TB)                                   \
+    const LaunchFn NAME[NUM_CONFIGS] = {                                   \
+        &launch_simt<ConfigOf<CFG_128x128, TA, TB>::type>,                 \
+        &launch_simt<ConfigOf<CFG_128x64, TA, TB>::type>,                  \
+        &launch_simt<ConfigOf<CFG_64x64, TA, TB>::type>,                   \
+        &launch_simt<ConfigOf<CFG_64x64_SCALAR, TA, TB>::type>,            \
+    };
+
+}  // namespace fgemm

@@ -1,0 +1,137 @@
+/*
+ * fgemm.h -- C ABI of a single-GPU FP32 GEMM library for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (GEMM 优化详解, "GEMM 基础理论 / 数学定义"; 第5章-基础Kernel,
+ * "1.1 什么是矩阵乘法"):
+ *
+ *     C = alpha * op(A) * op(B) + beta * C,   op(A) is M x K, op(B) is K x N, C is M x N,
+ *     C[i][j] = alpha * sum_{k=0}^{K-1} op(A)[i][k] * op(B)[k][j] + beta * C[i][j]
+ *
+ * All matrices are ROW-MAJOR with an explicit leading dimension (the distance,
+ * in elements, between the starts of two consecutive stored rows):
+ *   transa == FGEMM_OP_N: A is stored M x K, element (i,k) at A[i*lda + k], lda >= max(1,K)
+ *   transa == FGEMM_OP_T: A is stored K x M, element (i,k) at A[k*lda + i], lda >= max(1,M)
+ *   transb == FGEMM_OP_N: B is stored K x N, element (k,j) at B[k*ldb + j], ldb >= max(1,N)
+ *   transb == FGEMM_OP_T: B is stored N x K, element (k,j) at B[j*ldb + k], ldb >= max(1,K)
+ *   C is stored M x N, element (i,j) at C[i*ldc + j], ldc >= max(1,N).
+ *
+ * Conventions shared by every entry point:
+ *   - Pointers are DEVICE pointers owned by the caller.  The library allocates
+ *     nothing, frees nothing and keeps no workspace.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default stream)
+ *     and never synchronises.  Results are valid once the stream has run.
+ *   - beta == 0: C is not read before it is written (it may hold NaN).
+ *   - alpha == 0 or K == 0: no products are formed and A, B are not read
+ *     (they may be NULL); the result is beta*C (then bias, ReLU).
+ *   - M == 0, N == 0 or batch == 0: nothing happens and FGEMM_OK is returned.
+ *   - Invalid arguments return FGEMM_ERR_INVALID_VALUE before anything is
+ *     launched; C is left untouched.  A failed launch returns FGEMM_ERR_LAUNCH.
+ *     Nothing aborts or exits the process.
+ *   - Any alignment is accepted.  When a pointer, leading dimension or batch
+ *     stride is not a multiple of 16 bytes the call runs a slower kernel that
+ *     moves single elements instead of 16-byte vectors.
+ *   - Arithmetic is IEEE FP32 fused multiply-add on the CUDA cores, summing k
+ *     in an order that differs from the plain loop; results agree with an FP64
+ *     evaluation to within 1e-5 * (|alpha| sum_k |a_ik||b_kj| + |beta||c_ij| + |bias_j|).
+ *   - Thread safety: calls from several host threads are safe.
+ */
+#ifndef FGEMM_H
+#define FGEMM_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fgemm_status {
+    FGEMM_OK = 0,
+    FGEMM_ERR_INVALID_VALUE = 1, /* an argument breaks the rules above; nothing launched */
+    FGEMM_ERR_LAUNCH = 2,        /* the CUDA launch (or a CUDA query before it) failed */
+    FGEMM_ERR_NOT_SUPPORTED = 3, /* e.g. no sm_103a device, or a config that cannot run the call */
+} fgemm_status;
+
+typedef enum fgemm_op { FGEMM_OP_N = 0, FGEMM_OP_T = 1 } fgemm_op;
+
+/*
+ * Plain GEMM: C = alpha*op(A)*op(B) + beta*C.
+ * Defined by GEMM 优化详解, "数学定义" (C = alpha x A x B + beta x C) with the
+ * 0-based sum of 第5章-基础Kernel, "1.1 什么是矩阵乘法".
+ */
+fgemm_status fgemm_sgemm(fgemm_op transa, fgemm_op transb, int M, int N, int K, float alpha,
+                         const float *A, int lda, const float *B, int ldb, float beta, float *C,
+                         int ldc, cudaStream_t stream);
+
+/*
+ * Fully-connected layer epilogue fused into the GEMM (GEMM 优化详解, "Level 6:
+ * Kernel Fusion", and the layer Y = X x W + b of "为什么 GEMM 重要？"):
+ *     C[i][j] = act( alpha * sum_k op(A)[i][k] op(B)[k][j] + beta * C[i][j] + bias[j] )
+ * bias: device vector of N floats indexed by output column, or NULL for none.
+ * apply_relu: nonzero applies act(x) = max(0, x) (a NaN becomes 0); zero applies none.
+ * All four combinations of bias / ReLU are accepted.
+ */
+fgemm_status fgemm_sgemm_bias_relu(fgemm_op transa, fgemm_op transb, int M, int N, int K,
+                                   float alpha, const float *A, int lda, const float *B, int ldb,
+                                   float beta, float *C, int ldc, const float *bias,
+                                   int apply_relu, cudaStream_t stream);
+
+/*
+ * Strided batch: for b in [0, batch), the plain GEMM on A + b*strideA,
+ * B + b*strideB, C + b*strideC (strides in elements).  Used for batched
+ * attention scores Q x K^T (GEMM 优化详解, "为什么 GEMM 重要？", and the
+ * "考虑 batched GEMM" advice of "矩阵大小选择策略").
+ * strideA, strideB >= 0 (0 reuses one operand for every problem).
+ * strideC >= 0, and no element of C may belong to two problems (checked
+ * exactly, so interleaved layouts such as ldc = batch*N, strideC = N are
+ * accepted); an overlap returns FGEMM_ERR_INVALID_VALUE.
+ */
+fgemm_status fgemm_sgemm_strided_batched(fgemm_op transa, fgemm_op transb, int M, int N, int K,
+                                         float alpha, const float *A, int lda, long long strideA,
+                                         const float *B, int ldb, long long strideB, float beta,
+                                         float *C, int ldc, long long strideC, int batch,
+                                         cudaStream_t stream);
+
+/* Static, human-readable text for a status code (never NULL). */
+const char *fgemm_status_string(fgemm_status status);
+
+/* ----------------------------------------------------------------------------
+ * Kernel configurations (for tests and benchmarks).
+ *
+ * The plain entry points pick a kernel configuration from the shape, the
+ * transposes, 16-byte alignment and the SM count.  The calls below expose that
+ * choice so every configuration can be tested on edge shapes, and timed.
+ * ------------------------------------------------------------------------- */
+
+/* Number of kernel configurations; valid ids are 0 .. fgemm_num_configs()-1. */
+int fgemm_num_configs(void);
+
+/* Static name of a configuration ("simt_128x128x16_s4", ...), or NULL for a bad id. */
+const char *fgemm_config_name(int config);
+
+/*
+ * The configuration the plain entry points would use for this problem on a
+ * GPU with `num_sms` SMs.  `aligned` is nonzero when A, B, their leading
+ * dimensions and batch strides are all multiples of 16 bytes.  Host-only: no
+ * CUDA call is made.  Returns -1 for arguments the entry points would reject.
+ */
+int fgemm_select_config(fgemm_op transa, fgemm_op transb, int M, int N, int K, int batch,
+                        int aligned, int num_sms);
+
+/*
+ * The most general call, with an explicit configuration (config < 0 means
+ * "select as the plain entry points do").  Argument meaning and validation are
+ * those of the calls above (bias may be NULL; batch = 1 with zero strides is a
+ * single GEMM).  A configuration that needs 16-byte alignment returns
+ * FGEMM_ERR_NOT_SUPPORTED for unaligned operands.
+ */
+fgemm_status fgemm_gemm_explicit(int config, fgemm_op transa, fgemm_op transb, int M, int N,
+                                 int K, float alpha, const float *A, int lda, long long strideA,
+                                 const float *B, int ldb, long long strideB, float beta, float *C,
+                                 int ldc, long long strideC, int batch, const float *bias,
+                                 int apply_relu, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FGEMM_H */

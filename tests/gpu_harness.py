@@ -1,0 +1,137 @@
+"""Run one problem through the CUDA library and the FP64 oracle on the same inputs.
+
+Inputs are drawn on the CPU (seeded), stored with padded leading dimensions
+(padding holds NaN so any read of it poisons the result) and optionally shifted
+by a few elements so pointers are not 16-byte aligned.  The library is called
+through its C ABI on device copies; the oracle sees the identical float32 bits.
+
+Acceptance, per output element (fixed by the FP32 accuracy requirement of the
+method; the K in "1e-5 * K * sum|A||B| / K" cancels):
+    integer-valued inputs:  bit-exact (every partial sum is an integer < 2^24)
+    otherwise:              |C - C_ref| <= 1e-5 * mag + FLT_MIN
+with mag = |alpha| sum_k |a_ik||b_kj| + |beta||c_ij| + |bias_j| from the oracle.
+Elements of C outside the M x N region must come back unchanged.
+"""
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+import dense_fp32_gemm_sm_gb300 as fg
+import oracle
+from dense_fp32_gemm_sm_gb300 import workloads
+
+REL_TOL = 1e-5
+FLT_MIN = float(np.finfo(np.float32).tiny)
+SENTINEL = -12345.0
+
+
+@dataclass
+class Case:
+    ta: int = 0
+    tb: int = 0
+    M: int = 64
+    N: int = 64
+    K: int = 64
+    alpha: float = 1.0
+    beta: float = 0.0
+    batch: int = 0  # 0: single GEMM through gemm_explicit with batch=1
+    bias: bool = False
+    relu: bool = False
+    ints: bool = True
+    pad: tuple = (0, 0, 0)  # extra leading-dimension elements for A, B, C
+    offset: tuple = (0, 0, 0)  # element offset of A, B, C from a 16-byte boundary
+    config: int = -1
+    seed: int = 0
+    c_nan: bool = False  # fill the initial C with NaN (only meaningful for beta == 0)
+    a_nan: bool = False  # fill A with NaN (only meaningful for alpha == 0)
+
+
+def _draw(g, shape, ints):
+    if ints:
+        return workloads.small_ints(g, shape).numpy()
+    return workloads.uniform(g, shape).numpy()
+
+
+def _device(flat, offset):
+    """Copy a flat float32 array to the GPU at `offset` elements past a 256-byte boundary."""
+    buf = torch.empty(flat.size + offset + 4, dtype=torch.float32, device="cuda")
+    buf[offset:offset + flat.size].copy_(torch.from_numpy(flat))
+    return buf, buf.data_ptr() + 4 * offset
+
+
+def run(case: Case):
+    """Returns (got, want, mag, untouched_ok) with got/want of shape (batch or 1, M, N)."""
+    g = workloads.generator(case.seed)
+    nb = max(case.batch, 1)
+    M, N, K = case.M, case.N, case.K
+    lda = max(1, (M if case.ta else K) + case.pad[0])
+    ldb = max(1, (K if case.tb else N) + case.pad[1])
+    ldc = max(1, N + case.pad[2])
+    a_rows, b_rows = (K if case.ta else M), (N if case.tb else K)
+    sA, sB, sC = a_rows * lda + 3, b_rows * ldb + 5, M * ldc + 7
+    if case.batch == 0:
+        sA = sB = sC = 0
+
+    def stored(rows, ld, cols, stride, ints):
+        flat = np.full(max(stride * (nb - 1) + rows * ld, 1), np.nan, np.float32)
+        for b in range(nb):
+            blk = _draw(g, (rows, cols), ints)
+            for r in range(rows):
+                flat[b * stride + r * ld: b * stride + r * ld + cols] = blk[r]
+        return flat
+
+    A = stored(a_rows, lda, M if case.ta else K, sA, case.ints)
+    B = stored(b_rows, ldb, K if case.tb else N, sB, case.ints)
+    C0 = stored(M, ldc, N, sC, True)
+    # padding of C holds a sentinel that must survive the call
+    C0[np.isnan(C0)] = SENTINEL
+    if case.c_nan:
+        for b in range(nb):
+            for r in range(M):
+                C0[b * sC + r * ldc: b * sC + r * ldc + N] = np.nan
+    if case.a_nan:
+        A[:] = np.nan
+    bias = _draw(g, (N,), True).astype(np.float32) if case.bias else None
+
+    dA, pA = _device(A, case.offset[0])
+    dB, pB = _device(B, case.offset[1])
+    dC, pC = _device(C0, case.offset[2])
+    dbias, pbias = _device(bias, 0) if bias is not None else (None, None)
+    fg.gemm_explicit(case.config, case.ta, case.tb, M, N, K, case.alpha, pA, lda, sA, pB, ldb, sB,
+                     case.beta, pC, ldc, sC, nb, pbias, case.relu,
+                     stream=torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    Cout = dC[case.offset[2]:case.offset[2] + C0.size].cpu().numpy()
+
+    got = np.zeros((nb, M, N), np.float32)
+    want = np.zeros((nb, M, N), np.float64)
+    mag = np.zeros((nb, M, N), np.float64)
+    untouched = np.ones(C0.size, bool)
+    for b in range(nb):
+        o, m = oracle.gemm(case.ta, case.tb, M, N, K, case.alpha, A[b * sA:], lda, B[b * sB:],
+                           ldb, case.beta, C0[b * sC:] if case.beta != 0 else None, ldc,
+                           bias=bias, relu=case.relu)
+        want[b], mag[b] = o, m
+        for r in range(M):
+            got[b, r] = Cout[b * sC + r * ldc: b * sC + r * ldc + N]
+            untouched[b * sC + r * ldc: b * sC + r * ldc + N] = False
+    same = (Cout == C0) | (np.isnan(Cout) & np.isnan(C0))
+    return got, want, mag, bool(same[untouched].all())
+
+
+def check(case: Case):
+    got, want, mag, untouched_ok = run(case)
+    assert untouched_ok, "the call wrote outside the M x N region of C"
+    assert not np.isnan(got).any(), "NaN in the result"
+    if case.ints:
+        bad = got.astype(np.float64) != want
+        assert not bad.any(), "not bit-exact: %d of %d differ, first at %s: %r vs %r" % (
+            bad.sum(), bad.size, np.argwhere(bad)[0], got[bad][0], want[bad][0])
+    else:
+        err = np.abs(got.astype(np.float64) - want)
+        bound = REL_TOL * mag + FLT_MIN
+        bad = err > bound
+        assert not bad.any(), "outside 1e-5*mag: %d of %d, worst ratio %g" % (
+            bad.sum(), bad.size, (err / bound).max())

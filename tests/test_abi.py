@@ -1,0 +1,123 @@
+"""The C-ABI library without a GPU: it loads, exports every declared symbol,
+validates arguments before touching CUDA, and selects configurations."""
+
+import os
+import re
+
+import pytest
+
+import dense_fp32_gemm_sm_gb300 as fg
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "fgemm.h")
+FAKE = 0x10000  # a non-null address that validation never dereferences
+
+
+def declared_functions():
+    text = open(HEADER, encoding="utf-8").read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(fgemm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_symbol():
+    lib = fg.library()
+    names = declared_functions()
+    assert "fgemm_sgemm" in names and "fgemm_sgemm_strided_batched" in names
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    for s in (fg.OK, fg.ERR_INVALID_VALUE, fg.ERR_LAUNCH, fg.ERR_NOT_SUPPORTED):
+        assert fg.status_string(s).startswith("FGEMM_")
+    assert "unknown" in fg.status_string(99)
+
+
+def test_config_table():
+    n = fg.num_configs()
+    assert n >= 4
+    names = [fg.config_name(i) for i in range(n)]
+    assert all(names) and len(set(names)) == n
+    assert fg.config_name(-1) is None and fg.config_name(n) is None
+
+
+def _sgemm(**kw):
+    args = dict(transa=0, transb=0, M=4, N=4, K=4, alpha=1.0, A=FAKE, lda=4, B=FAKE, ldb=4,
+                beta=0.0, C=FAKE, ldc=4)
+    args.update(kw)
+    return fg.sgemm(**args, check=False)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(transa=2), dict(transb=-1), dict(M=-1), dict(N=-1), dict(K=-1),
+    dict(lda=3), dict(ldb=3), dict(ldc=3),
+    dict(transa=1, M=8, lda=7), dict(transb=1, K=9, lda=9, ldb=8),
+    dict(A=None), dict(B=None), dict(C=None),
+])
+def test_invalid_arguments_rejected_before_launch(kw):
+    assert _sgemm(**kw) == fg.ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("kw", [dict(M=0), dict(N=0), dict(M=0, A=None, B=None, C=None)])
+def test_empty_problems_are_noops(kw):
+    assert _sgemm(**kw) == fg.OK
+
+
+def test_ld_minimum_is_one_for_empty_rows():
+    # K == 0 with lda == 0 is still invalid: ld >= max(1, stored row length).
+    assert _sgemm(K=0, lda=0) == fg.ERR_INVALID_VALUE
+
+
+def _batched(**kw):
+    args = dict(transa=0, transb=0, M=4, N=4, K=4, alpha=1.0, A=FAKE, lda=4, strideA=16, B=FAKE,
+                ldb=4, strideB=16, beta=0.0, C=FAKE, ldc=4, strideC=16, batch=3)
+    args.update(kw)
+    return fg.sgemm_strided_batched(**args, check=False)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(batch=-1), dict(strideA=-4), dict(strideB=-4), dict(strideC=-4),
+    dict(strideC=0), dict(strideC=15), dict(strideC=4, ldc=4),  # overlapping C problems
+    dict(ldc=8, strideC=5),  # problem 1 starts inside row 0 of problem 0
+])
+def test_batched_rejects(kw):
+    assert _batched(**kw) == fg.ERR_INVALID_VALUE
+
+
+def test_batched_empty_is_noop():
+    assert _batched(batch=0) == fg.OK
+    assert _batched(batch=0, strideC=0) == fg.OK
+
+
+def test_explicit_rejects_bad_config():
+    st = fg.gemm_explicit(fg.num_configs(), 0, 0, 4, 4, 4, 1.0, FAKE, 4, 0, FAKE, 4, 0, 0.0, FAKE,
+                          4, 0, 1, check=False)
+    assert st == fg.ERR_INVALID_VALUE
+
+
+def test_explicit_vector_config_refuses_unaligned():
+    # An unaligned A pointer with a 16-byte-vector configuration: refused before launch.
+    st = fg.gemm_explicit(0, 0, 0, 4, 4, 4, 1.0, FAKE + 4, 4, 0, FAKE, 4, 0, 0.0, FAKE, 4, 0, 1,
+                          check=False)
+    assert st == fg.ERR_NOT_SUPPORTED
+    st = fg.gemm_explicit(0, 0, 0, 4, 4, 4, 1.0, FAKE, 5, 0, FAKE, 4, 0, 0.0, FAKE, 4, 0, 1,
+                          check=False)
+    assert st == fg.ERR_NOT_SUPPORTED
+
+
+def test_selector():
+    sel = fg.select_config
+    scalar = [i for i in range(fg.num_configs()) if fg.config_name(i).endswith("_scalar")]
+    assert sel(0, 0, 4096, 4096, 4096, 1, 0, 152) in scalar
+    big = sel(0, 0, 4096, 4096, 4096, 1, 1, 152)
+    assert fg.config_name(big).startswith("simt_128x128")
+    small = sel(0, 0, 256, 256, 256, 1, 1, 152)
+    assert not fg.config_name(small).endswith("_scalar")
+    # a batch of small problems fills the GPU with the large tile
+    assert sel(0, 1, 2048, 2048, 128, 128, 1, 152) == big
+    assert sel(0, 0, -1, 4, 4, 1, 1, 152) == -1
+    for ta in (0, 1):
+        for tb in (0, 1):
+            for n in (1, 7, 64, 255, 1000, 5000):
+                c = sel(ta, tb, n, n, n, 1, 1, 152)
+                assert 0 <= c < fg.num_configs()
