@@ -44,6 +44,7 @@ class Case:
     offset: tuple = (0, 0, 0)  # element offset of A, B, C from a 16-byte boundary
     config: int = -1
     seed: int = 0
+    align_ld: bool = True  # round leading dimensions and batch strides up to 16 bytes
     c_nan: bool = False  # fill the initial C with NaN (only meaningful for beta == 0)
     a_nan: bool = False  # fill A with NaN (only meaningful for alpha == 0)
 
@@ -66,11 +67,12 @@ def run(case: Case):
     g = workloads.generator(case.seed)
     nb = max(case.batch, 1)
     M, N, K = case.M, case.N, case.K
-    lda = max(1, (M if case.ta else K) + case.pad[0])
-    ldb = max(1, (K if case.tb else N) + case.pad[1])
-    ldc = max(1, N + case.pad[2])
+    up = (lambda x: (x + 3) // 4 * 4) if case.align_ld else (lambda x: x)
+    lda = up(max(1, (M if case.ta else K) + case.pad[0]))
+    ldb = up(max(1, (K if case.tb else N) + case.pad[1]))
+    ldc = up(max(1, N + case.pad[2]))
     a_rows, b_rows = (K if case.ta else M), (N if case.tb else K)
-    sA, sB, sC = a_rows * lda + 3, b_rows * ldb + 5, M * ldc + 7
+    sA, sB, sC = up(a_rows * lda + 3), up(b_rows * ldb + 5), up(M * ldc + 7)
     if case.batch == 0:
         sA = sB = sC = 0
 
