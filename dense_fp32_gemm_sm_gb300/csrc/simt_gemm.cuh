@@ -3,33 +3,34 @@
 // One CTA computes a BM x BN tile of C = alpha*op(A)*op(B) + beta*C (then bias,
 // ReLU).  Design, GB300-first:
 //
-//  * Staging (global -> shared): a STAGES-deep ring of shared-memory tiles filled
-//    with cp.async (16-byte vectors, or single elements when the operand is not
-//    16-byte aligned).  Out-of-range rows/columns and the K tail are zero-filled
-//    by the copy itself (src-size < cp-size), so the inner loop has no edge
-//    checks.  Each operand lands in the orientation it has in global memory:
-//    no register-staged transpose.  This replaces the two-buffer, register-staged
-//    ping-pong of GPU架构下的矩阵乘法深入优化, "5. warp tiling + double buffer".
+//  * Staging (global -> shared): a STAGES-deep ring of shared tiles filled with
+//    cp.async, replacing the two-buffer, register-staged ping-pong of
+//    GPU架构下的矩阵乘法深入优化, "5. warp tiling + double buffer".  Both operands
+//    are stored k-major in shared memory: sA[k][m] and sB[k][n].  An operand
+//    whose rows already run along m (A stored K x M) or n (B stored K x N) is
+//    copied with 16-byte vectors; an operand stored with k contiguous is
+//    transposed by the copy itself (4-byte cp.async, one element per lane, a
+//    warp covering 8 k x 4 rows so both the global reads and the shared writes
+//    are conflict-free).  Out-of-range rows/columns and the K tail are
+//    zero-filled by the copy (src-size 0), so the inner loop has no edge checks.
 //
-//  * Shared-memory layouts ("MK" = rows of K for A stored M x K, "KM" = rows of
-//    M for A stored K x M; likewise "KN"/"NK" for B).  K-contiguous tiles get a
-//    4-float row pad, so the 8 (or 4) distinct rows a warp reads in one 16-byte
-//    load fall in distinct bank quads (conflict-free; the padding idea of
-//    GEMM 优化详解, "Level 3 / Bank Conflict" and 第5章-基础Kernel, "Shared + Padding").
+//  * k-major tiles let every thread read its A and B fragments for one k with
+//    16-byte loads along m and n (the transposed-A idea of the same page, and the
+//    row padding of GEMM 优化详解, "Level 3" / 第5章-基础Kernel, "Shared + Padding").
+//    Fragments for k+1 are loaded while k is computed (register double buffer).
 //
 //  * Register blocking (GEMM 优化详解, "Level 5: Register Blocking"): each thread
-//    owns TM x TN accumulators; per k it reads TM values of op(A) and TN values of
-//    op(B) from shared memory with 16-byte loads and issues TM*TN FFMAs.  The
-//    thread's rows/columns are chosen so each 16-byte load is either 4
-//    consecutive k (K-contiguous tiles) or 4 consecutive rows/columns.
+//    owns TM x TN accumulators (8 x 8), held as pairs along n and updated with the
+//    packed FP32 FMA of sm_100+ (fma.rn.f32x2): one instruction does two FMAs, so
+//    the FMA pipe stays busy while the issue slots left over carry the shared
+//    loads.  Each a[i] is duplicated into a register pair once per k.
 //
-//  * Epilogue in registers (GEMM 优化详解, "Level 6: Kernel Fusion" and
-//    "Level 7: Vectorized Loads"): v = alpha*acc (+ beta*C) (+ bias[col]),
-//    ReLU, then float4 stores where the thread owns 4 consecutive columns and
-//    C is 16-byte aligned, scalar stores otherwise.
+//  * Epilogue in registers (GEMM 优化详解, "Level 6: Kernel Fusion" and "Level 7:
+//    Vectorized Loads"): v = alpha*acc (+ beta*C) (+ bias[col]), ReLU, then float4
+//    stores when C is 16-byte aligned, scalar stores otherwise.
 //
 //  * Tiles are visited in groups of GROUP_M tile-rows so that concurrently
-//    resident CTAs share panels of A and B in the 126 MB L2.
+//    resident CTAs share panels of A and B in L2.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -90,6 +91,26 @@ __device__ __forceinline__ int clamp_bytes(long long remaining_elems)
     return remaining_elems >= 4 ? 16 : (remaining_elems > 0 ? int(remaining_elems) * 4 : 0);
 }
 
+// d += a * b on two packed FP32 lanes (fma.rn.f32x2: round-to-nearest, no flush).
+__device__ __forceinline__ void ffma2(unsigned long long &d, unsigned long long a,
+                                      unsigned long long b)
+{
+    asm volatile("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
+}
+
+__device__ __forceinline__ unsigned long long dup_pair(float a)
+{
+    unsigned long long d;
+    asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(a));
+    return d;
+}
+
+__device__ __forceinline__ float pair_lo(unsigned long long v) { return __uint_as_float((unsigned)v); }
+__device__ __forceinline__ float pair_hi(unsigned long long v)
+{
+    return __uint_as_float((unsigned)(v >> 32));
+}
+
 // ---- Configuration -------------------------------------------------------------
 
 template <int BM_, int BN_, int BK_, int WM_, int WN_, int TM_, int TN_, int STAGES_, int MINB_,
@@ -104,58 +125,77 @@ struct SimtCfg {
     static constexpr int THREADS = 32 * WARPS_M * WARPS_N;
     static constexpr int LR = WM / TM;  // lanes along M
     static constexpr int LC = WN / TN;  // lanes along N
-    static constexpr int PAD = 4;       // floats of row padding on K-contiguous tiles
-    // Shared-memory tile shapes (floats): A_ROWS x A_LD and B_ROWS x B_LD per stage.
-    static constexpr int A_ROWS = TA ? BK : BM;
-    static constexpr int A_LD = TA ? BM : BK + PAD;
-    static constexpr int B_ROWS = TB ? BN : BK;
-    static constexpr int B_LD = TB ? BK + PAD : BN;
-    static constexpr int A_STAGE = A_ROWS * A_LD;
-    static constexpr int B_STAGE = B_ROWS * B_LD;
+    static constexpr int A_LD = BM + 4;  // sA[k][m]; +4 floats keeps transposed writes conflict-free
+    static constexpr int B_LD = BN + 4;  // sB[k][n]
+    static constexpr int A_STAGE = BK * A_LD;
+    static constexpr int B_STAGE = BK * B_LD;
     static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
     static constexpr int GROUP_M = 8;
 
     static_assert(LR * LC == 32, "a warp is LR x LC lanes");
     static_assert(BM % WM == 0 && BN % WN == 0, "warp tiles must cover the CTA tile");
-    static_assert(TM % 4 == 0 && TN % 4 == 0 && BK % 4 == 0, "16-byte fragments");
-    static_assert((BM * BK / 4) % THREADS == 0 && (BN * BK / 4) % THREADS == 0,
-                  "vector copies divide evenly over the threads");
+    static_assert(TM % 4 == 0 && TN % 4 == 0, "16-byte fragments");
+    static_assert(BK % 8 == 0, "transposing copies move 8 k per warp row");
+    static_assert(BM % 4 == 0 && BN % 4 == 0, "transposing copies move 4 rows per warp");
     static_assert((BM * BK) % THREADS == 0 && (BN * BK) % THREADS == 0,
                   "element copies divide evenly over the threads");
+    static_assert((BM * BK / 4) % THREADS == 0 && (BN * BK / 4) % THREADS == 0,
+                  "vector copies divide evenly over the threads");
+    static_assert(STAGES >= 2, "at least double buffering");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
 // ---- Tile loaders --------------------------------------------------------------
 
-// Copy the (rows x cols) stored block starting at (r0, c0) of a row-major matrix
-// with leading dimension ld into a shared tile with row stride S_LD.  Rows at or
-// beyond R and columns at or beyond Ccount are zero-filled.
-template <int ROWS, int COLS, int S_LD, int THREADS, bool VEC>
-__device__ __forceinline__ void load_block(uint32_t s_tile, const float *g, long long ld, long long r0,
-                                           long long c0, long long R, long long Ccount, int tid)
+// Stored block whose rows run along k (K x MN storage, MN contiguous): rows
+// [k0, k0+BK) x columns [c0, c0+COLS) -> s[k][c] with row stride S_LD.
+template <int BK, int COLS, int S_LD, int THREADS, bool VEC>
+__device__ __forceinline__ void load_k_rows(uint32_t s_tile, const float *g, long long ld, int k0,
+                                            int c0, int K, int Ccount, int tid)
 {
     if constexpr (VEC) {
-        constexpr int CPR = COLS / 4;  // 16-byte chunks per row
-        constexpr int ITERS = ROWS * CPR / THREADS;
+        constexpr int CPR = COLS / 4;
+        constexpr int ITERS = BK * CPR / THREADS;
 #pragma unroll
         for (int it = 0; it < ITERS; ++it) {
             const int idx = tid + it * THREADS;
             const int r = idx / CPR, cc = (idx % CPR) * 4;
-            const long long gr = r0 + r, gc = c0 + cc;
-            const int bytes = gr < R ? clamp_bytes(Ccount - gc) : 0;
-            const float *src = bytes ? g + gr * ld + gc : g;
+            const int gk = k0 + r, gc = c0 + cc;
+            const int bytes = gk < K ? clamp_bytes((long long)Ccount - gc) : 0;
+            const float *src = bytes ? g + (long long)gk * ld + gc : g;
             cp_async_16(s_tile + (r * S_LD + cc) * 4, src, bytes);
         }
     } else {
-        constexpr int ITERS = ROWS * COLS / THREADS;
+        constexpr int ITERS = BK * COLS / THREADS;
 #pragma unroll
         for (int it = 0; it < ITERS; ++it) {
             const int idx = tid + it * THREADS;
             const int r = idx / COLS, cc = idx % COLS;
-            const long long gr = r0 + r, gc = c0 + cc;
-            const bool ok = gr < R && gc < Ccount;
-            cp_async_4(s_tile + (r * S_LD + cc) * 4, ok ? g + gr * ld + gc : g, ok ? 4 : 0);
+            const int gk = k0 + r, gc = c0 + cc;
+            const bool ok = gk < K && gc < Ccount;
+            cp_async_4(s_tile + (r * S_LD + cc) * 4, ok ? g + (long long)gk * ld + gc : g, ok ? 4 : 0);
         }
+    }
+}
+
+// Stored block whose rows run along m (or n) with k contiguous (MN x K storage):
+// rows [r0, r0+ROWS) x k [k0, k0+BK) -> s[k][r] (a transpose).  Each warp moves
+// an 8 (k) x 4 (rows) patch: lane&7 picks k, lane>>3 picks the row.
+template <int BK, int ROWS, int S_LD, int THREADS>
+__device__ __forceinline__ void load_k_cols(uint32_t s_tile, const float *g, long long ld, int r0,
+                                            int k0, int R, int K, int tid)
+{
+    constexpr int PATCHES_K = BK / 8;
+    constexpr int ITERS = BK * ROWS / THREADS;
+    const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+    for (int it = 0; it < ITERS; ++it) {
+        const int w = warp + it * (THREADS / 32);
+        const int k = (w % PATCHES_K) * 8 + (lane & 7);
+        const int r = (w / PATCHES_K) * 4 + (lane >> 3);
+        const int gr = r0 + r, gk = k0 + k;
+        const bool ok = gr < R && gk < K;
+        cp_async_4(s_tile + (k * S_LD + r) * 4, ok ? g + (long long)gr * ld + gk : g, ok ? 4 : 0);
     }
 }
 
@@ -164,38 +204,31 @@ __device__ __forceinline__ void load_stage(uint32_t sA, uint32_t sB, const GemmP
                                            const float *A, const float *B, int m0, int n0, int k0,
                                            int tid)
 {
-    if constexpr (Cfg::TA == 0)  // A stored M x K: rows m, columns k
-        load_block<Cfg::BM, Cfg::BK, Cfg::A_LD, Cfg::THREADS, Cfg::VEC>(sA, A, p.lda, m0, k0, p.M,
-                                                                       p.K, tid);
-    else  // A stored K x M: rows k, columns m
-        load_block<Cfg::BK, Cfg::BM, Cfg::A_LD, Cfg::THREADS, Cfg::VEC>(sA, A, p.lda, k0, m0, p.K,
-                                                                       p.M, tid);
+    if constexpr (Cfg::TA == 1)  // A stored K x M: rows are k already
+        load_k_rows<Cfg::BK, Cfg::BM, Cfg::A_LD, Cfg::THREADS, Cfg::VEC>(sA, A, p.lda, k0, m0, p.K,
+                                                                        p.M, tid);
+    else  // A stored M x K: transpose while copying
+        load_k_cols<Cfg::BK, Cfg::BM, Cfg::A_LD, Cfg::THREADS>(sA, A, p.lda, m0, k0, p.M, p.K, tid);
     if constexpr (Cfg::TB == 0)  // B stored K x N
-        load_block<Cfg::BK, Cfg::BN, Cfg::B_LD, Cfg::THREADS, Cfg::VEC>(sB, B, p.ldb, k0, n0, p.K,
-                                                                       p.N, tid);
-    else  // B stored N x K
-        load_block<Cfg::BN, Cfg::BK, Cfg::B_LD, Cfg::THREADS, Cfg::VEC>(sB, B, p.ldb, n0, k0, p.N,
-                                                                       p.K, tid);
+        load_k_rows<Cfg::BK, Cfg::BN, Cfg::B_LD, Cfg::THREADS, Cfg::VEC>(sB, B, p.ldb, k0, n0, p.K,
+                                                                        p.N, tid);
+    else  // B stored N x K: transpose while copying
+        load_k_cols<Cfg::BK, Cfg::BN, Cfg::B_LD, Cfg::THREADS>(sB, B, p.ldb, n0, k0, p.N, p.K, tid);
 }
 
 // Row (within the CTA tile) of the thread's i-th accumulator row, and column of
-// its j-th accumulator column.
+// its j-th accumulator column: groups of 4 consecutive rows/columns, one 16-byte
+// fragment load each.
 template <class Cfg>
 __device__ __forceinline__ int frag_row(int wm0, int lr, int i)
 {
-    if constexpr (Cfg::TA == 0)
-        return wm0 + lr + i * Cfg::LR;  // K-contiguous tile: one row per 16-byte load
-    else
-        return wm0 + (i / 4) * (Cfg::LR * 4) + lr * 4 + (i % 4);  // 4 rows per load
+    return wm0 + (i / 4) * (Cfg::LR * 4) + lr * 4 + (i % 4);
 }
 
 template <class Cfg>
 __device__ __forceinline__ int frag_col(int wn0, int lc, int j)
 {
-    if constexpr (Cfg::TB == 1)
-        return wn0 + lc + j * Cfg::LC;
-    else
-        return wn0 + (j / 4) * (Cfg::LC * 4) + lc * 4 + (j % 4);
+    return wn0 + (j / 4) * (Cfg::LC * 4) + lc * 4 + (j % 4);
 }
 
 // ---- The kernel ----------------------------------------------------------------
@@ -206,12 +239,12 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
     extern __shared__ __align__(128) float smem[];
     float *const sA_all = smem;
     float *const sB_all = smem + Cfg::STAGES * Cfg::A_STAGE;
+    constexpr int TM = Cfg::TM, TN = Cfg::TN;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
-    const int warp_m = warp / Cfg::WARPS_N, warp_n = warp % Cfg::WARPS_N;
     const int lr = lane / Cfg::LC, lc = lane % Cfg::LC;
-    const int wm0 = warp_m * Cfg::WM, wn0 = warp_n * Cfg::WN;
+    const int wm0 = (warp / Cfg::WARPS_N) * Cfg::WM, wn0 = (warp % Cfg::WARPS_N) * Cfg::WN;
 
     // Grouped tile order: GROUP_M consecutive tile-rows are swept column by column.
     int tile_m, tile_n;
@@ -231,162 +264,124 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
     const float *const B = p.B + bz * p.strideB;
     float *const C = p.C + bz * p.strideC;
 
-    float acc[Cfg::TM][Cfg::TN];
+    unsigned long long acc[TM][TN / 2];  // acc[i][j] = (c[i][2j], c[i][2j+1])
 #pragma unroll
-    for (int i = 0; i < Cfg::TM; ++i)
+    for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < Cfg::TN; ++j) acc[i][j] = 0.0f;
+        for (int j = 0; j < TN / 2; ++j) acc[i][j] = 0ull;
 
     const uint32_t sA_base = smem_addr(sA_all), sB_base = smem_addr(sB_all);
     const int KT = (p.K + Cfg::BK - 1) / Cfg::BK;
 
-    // Prologue: fill STAGES-1 slots.
+    if (KT > 0) {
+        // Prologue: fill STAGES-1 slots, then wait for the first.
 #pragma unroll
-    for (int s = 0; s < Cfg::STAGES - 1; ++s) {
-        if (s < KT)
-            load_stage<Cfg>(sA_base + s * Cfg::A_STAGE * 4, sB_base + s * Cfg::B_STAGE * 4, p, A, B,
-                            m0, n0, s * Cfg::BK, tid);
-        cp_async_commit();
-    }
-
-    for (int kt = 0; kt < KT; ++kt) {
-        cp_async_wait<Cfg::STAGES - 2>();
-        __syncthreads();  // slot kt is visible to all; slot kt-1 is no longer read by anyone
-        {
-            const int nk = kt + Cfg::STAGES - 1;
-            if (nk < KT) {
-                const int slot = nk % Cfg::STAGES;
-                load_stage<Cfg>(sA_base + slot * Cfg::A_STAGE * 4, sB_base + slot * Cfg::B_STAGE * 4,
-                                p, A, B, m0, n0, nk * Cfg::BK, tid);
-            }
+        for (int s = 0; s < Cfg::STAGES - 1; ++s) {
+            if (s < KT)
+                load_stage<Cfg>(sA_base + s * Cfg::A_STAGE * 4, sB_base + s * Cfg::B_STAGE * 4, p,
+                                A, B, m0, n0, s * Cfg::BK, tid);
             cp_async_commit();
         }
-        const int slot = kt % Cfg::STAGES;
-        const float *const sA = sA_all + slot * Cfg::A_STAGE;
-        const float *const sB = sB_all + slot * Cfg::B_STAGE;
+        cp_async_wait<Cfg::STAGES - 2>();
+        __syncthreads();
 
+        float4 fa[2][TM / 4], fb[2][TN / 4];
+        auto load_frag = [&](int buf, int slot, int k) {
+            const float *a = sA_all + slot * Cfg::A_STAGE + k * Cfg::A_LD;
+            const float *b = sB_all + slot * Cfg::B_STAGE + k * Cfg::B_LD;
 #pragma unroll
-        for (int kg = 0; kg < Cfg::BK; kg += 4) {
-            float a[4][Cfg::TM], b[4][Cfg::TN];
-            if constexpr (Cfg::TA == 0) {
+            for (int g = 0; g < TM / 4; ++g)
+                fa[buf][g] = *reinterpret_cast<const float4 *>(a + frag_row<Cfg>(wm0, lr, 4 * g));
 #pragma unroll
-                for (int i = 0; i < Cfg::TM; ++i) {
-                    const float4 v = *reinterpret_cast<const float4 *>(
-                        sA + frag_row<Cfg>(wm0, lr, i) * Cfg::A_LD + kg);
-                    a[0][i] = v.x;
-                    a[1][i] = v.y;
-                    a[2][i] = v.z;
-                    a[3][i] = v.w;
+            for (int g = 0; g < TN / 4; ++g)
+                fb[buf][g] = *reinterpret_cast<const float4 *>(b + frag_col<Cfg>(wn0, lc, 4 * g));
+        };
+        load_frag(0, 0, 0);
+
+        int slot = 0;
+        for (int kt = 0; kt < KT; ++kt) {
+#pragma unroll
+            for (int k = 0; k < Cfg::BK; ++k) {
+                const int cur = k & 1;
+                if (k == Cfg::BK - 1) {
+                    // Stage kt+1 must have landed, and every thread must be done with
+                    // the slot the next copy overwrites.
+                    cp_async_wait<Cfg::STAGES - 2>();
+                    __syncthreads();
+                    slot = (slot + 1 == Cfg::STAGES) ? 0 : slot + 1;
+                    if (kt + 1 < KT) load_frag(cur ^ 1, slot, 0);
+                } else {
+                    load_frag(cur ^ 1, slot, k + 1);
                 }
-            } else {
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                    for (int g = 0; g < Cfg::TM / 4; ++g) {
-                        const float4 v = *reinterpret_cast<const float4 *>(
-                            sA + (kg + kk) * Cfg::A_LD + frag_row<Cfg>(wm0, lr, 4 * g));
-                        a[kk][4 * g + 0] = v.x;
-                        a[kk][4 * g + 1] = v.y;
-                        a[kk][4 * g + 2] = v.z;
-                        a[kk][4 * g + 3] = v.w;
+                if (k == 0) {
+                    const int nk = kt + Cfg::STAGES - 1;
+                    if (nk < KT) {
+                        int ws = slot + Cfg::STAGES - 1;
+                        if (ws >= Cfg::STAGES) ws -= Cfg::STAGES;
+                        load_stage<Cfg>(sA_base + ws * Cfg::A_STAGE * 4,
+                                        sB_base + ws * Cfg::B_STAGE * 4, p, A, B, m0, n0,
+                                        nk * Cfg::BK, tid);
                     }
-            }
-            if constexpr (Cfg::TB == 1) {
-#pragma unroll
-                for (int j = 0; j < Cfg::TN; ++j) {
-                    const float4 v = *reinterpret_cast<const float4 *>(
-                        sB + frag_col<Cfg>(wn0, lc, j) * Cfg::B_LD + kg);
-                    b[0][j] = v.x;
-                    b[1][j] = v.y;
-                    b[2][j] = v.z;
-                    b[3][j] = v.w;
+                    cp_async_commit();
                 }
-            } else {
+                const float *a = reinterpret_cast<const float *>(&fa[cur][0]);
+                const unsigned long long *b2 = reinterpret_cast<const unsigned long long *>(&fb[cur][0]);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
+                for (int i = 0; i < TM; ++i) {
+                    const unsigned long long ai = dup_pair(a[i]);
 #pragma unroll
-                    for (int g = 0; g < Cfg::TN / 4; ++g) {
-                        const float4 v = *reinterpret_cast<const float4 *>(
-                            sB + (kg + kk) * Cfg::B_LD + frag_col<Cfg>(wn0, lc, 4 * g));
-                        b[kk][4 * g + 0] = v.x;
-                        b[kk][4 * g + 1] = v.y;
-                        b[kk][4 * g + 2] = v.z;
-                        b[kk][4 * g + 3] = v.w;
-                    }
+                    for (int j = 0; j < TN / 2; ++j) ffma2(acc[i][j], ai, b2[j]);
+                }
             }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-#pragma unroll
-                for (int i = 0; i < Cfg::TM; ++i)
-#pragma unroll
-                    for (int j = 0; j < Cfg::TN; ++j) acc[i][j] = fmaf(a[kk][i], b[kk][j], acc[i][j]);
         }
+        cp_async_wait<0>();
     }
-    cp_async_wait<0>();
 
     // ---- Epilogue: alpha, beta, bias, ReLU in registers; vector stores where possible.
-    const bool products = p.K > 0;
-    float bias_v[Cfg::TN];
+    const bool products = KT > 0;
+    float bias_v[TN];
 #pragma unroll
-    for (int j = 0; j < Cfg::TN; ++j) {
+    for (int j = 0; j < TN; ++j) {
         const int gc = n0 + frag_col<Cfg>(wn0, lc, j);
         bias_v[j] = (p.bias != nullptr && gc < p.N) ? __ldg(p.bias + gc) : 0.0f;
     }
 #pragma unroll
-    for (int i = 0; i < Cfg::TM; ++i) {
+    for (int i = 0; i < TM; ++i) {
         const int gr = m0 + frag_row<Cfg>(wm0, lr, i);
         if (gr >= p.M) continue;
         float *const crow = C + (long long)gr * p.ldc;
-        float v[Cfg::TN];
 #pragma unroll
-        for (int j = 0; j < Cfg::TN; ++j) v[j] = products ? p.alpha * acc[i][j] : 0.0f;
-        if constexpr (Cfg::TB == 0) {
+        for (int g = 0; g < TN / 4; ++g) {
+            const int gc = n0 + frag_col<Cfg>(wn0, lc, 4 * g);
+            float v[4] = {pair_lo(acc[i][2 * g]), pair_hi(acc[i][2 * g]), pair_lo(acc[i][2 * g + 1]),
+                          pair_hi(acc[i][2 * g + 1])};
 #pragma unroll
-            for (int g = 0; g < Cfg::TN / 4; ++g) {
-                const int gc = n0 + frag_col<Cfg>(wn0, lc, 4 * g);
-                float *const dst = crow + gc;
-                if (p.c_vec && gc + 3 < p.N) {
-                    float4 o = make_float4(v[4 * g], v[4 * g + 1], v[4 * g + 2], v[4 * g + 3]);
-                    if (p.beta != 0.0f) {
-                        const float4 c = *reinterpret_cast<const float4 *>(dst);
-                        o.x = fmaf(p.beta, c.x, o.x);
-                        o.y = fmaf(p.beta, c.y, o.y);
-                        o.z = fmaf(p.beta, c.z, o.z);
-                        o.w = fmaf(p.beta, c.w, o.w);
-                    }
-                    o.x += bias_v[4 * g];
-                    o.y += bias_v[4 * g + 1];
-                    o.z += bias_v[4 * g + 2];
-                    o.w += bias_v[4 * g + 3];
-                    if (p.relu) {
-                        o.x = fmaxf(o.x, 0.0f);
-                        o.y = fmaxf(o.y, 0.0f);
-                        o.z = fmaxf(o.z, 0.0f);
-                        o.w = fmaxf(o.w, 0.0f);
-                    }
-                    *reinterpret_cast<float4 *>(dst) = o;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (gc + e >= p.N) break;
-                        float o = v[4 * g + e];
-                        if (p.beta != 0.0f) o = fmaf(p.beta, dst[e], o);
-                        o += bias_v[4 * g + e];
-                        if (p.relu) o = fmaxf(o, 0.0f);
-                        dst[e] = o;
-                    }
+            for (int e = 0; e < 4; ++e) v[e] = products ? p.alpha * v[e] : 0.0f;
+            float *const dst = crow + gc;
+            if (p.c_vec && gc + 3 < p.N) {
+                if (p.beta != 0.0f) {
+                    const float4 c = *reinterpret_cast<const float4 *>(dst);
+                    v[0] = fmaf(p.beta, c.x, v[0]);
+                    v[1] = fmaf(p.beta, c.y, v[1]);
+                    v[2] = fmaf(p.beta, c.z, v[2]);
+                    v[3] = fmaf(p.beta, c.w, v[3]);
                 }
-            }
-        } else {
 #pragma unroll
-            for (int j = 0; j < Cfg::TN; ++j) {
-                const int gc = n0 + frag_col<Cfg>(wn0, lc, j);
-                if (gc >= p.N) continue;
-                float o = v[j];
-                if (p.beta != 0.0f) o = fmaf(p.beta, crow[gc], o);
-                o += bias_v[j];
-                if (p.relu) o = fmaxf(o, 0.0f);
-                crow[gc] = o;
+                for (int e = 0; e < 4; ++e) {
+                    v[e] += bias_v[4 * g + e];
+                    if (p.relu) v[e] = fmaxf(v[e], 0.0f);
+                }
+                *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    if (gc + e >= p.N) break;
+                    float o = v[e];
+                    if (p.beta != 0.0f) o = fmaf(p.beta, dst[e], o);
+                    o += bias_v[4 * g + e];
+                    if (p.relu) o = fmaxf(o, 0.0f);
+                    dst[e] = o;
+                }
             }
         }
     }

@@ -9,28 +9,26 @@
 
 namespace fgemm {
 
-// The tile shapes behind each ConfigId.  The lane arrangement follows the B
-// layout: a warp is 8 x 4 lanes when B is N-contiguous (so each thread stores
-// float4 runs of C) and 4 x 8 lanes when B is K-contiguous (so a warp's scalar
-// stores cover 32-byte runs of a row).
+// The tile shapes behind each ConfigId.  Every configuration uses warps of
+// 8 x 4 lanes; each thread owns groups of 4 consecutive rows and columns.
 template <int ID, int TA, int TB>
 struct ConfigOf;
 
 template <int TA, int TB>
-struct ConfigOf<CFG_128x128, TA, TB> {
-    using type = SimtCfg<128, 128, 16, TB ? 32 : 64, TB ? 64 : 32, 8, 8, 4, 1, TA, TB, true>;
+struct ConfigOf<CFG_128x128, TA, TB> {  // 256 threads, two CTAs per SM
+    using type = SimtCfg<128, 128, 16, 64, 32, 8, 8, 4, 2, TA, TB, true>;
 };
 template <int TA, int TB>
-struct ConfigOf<CFG_128x64, TA, TB> {
-    using type = SimtCfg<128, 64, 16, TB ? 32 : 64, TB ? 64 : 32, 8, 8, 4, 2, TA, TB, true>;
+struct ConfigOf<CFG_128x64, TA, TB> {  // 128 threads, three CTAs per SM
+    using type = SimtCfg<128, 64, 16, 64, 32, 8, 8, 4, 3, TA, TB, true>;
 };
 template <int TA, int TB>
-struct ConfigOf<CFG_64x64, TA, TB> {
-    using type = SimtCfg<64, 64, 16, TB ? 16 : 32, TB ? 32 : 16, 4, 4, 4, 2, TA, TB, true>;
+struct ConfigOf<CFG_64x64, TA, TB> {  // 256 threads, 4 x 4 per thread
+    using type = SimtCfg<64, 64, 16, 32, 16, 4, 4, 4, 2, TA, TB, true>;
 };
 template <int TA, int TB>
-struct ConfigOf<CFG_64x64_SCALAR, TA, TB> {
-    using type = SimtCfg<64, 64, 16, TB ? 16 : 32, TB ? 32 : 16, 4, 4, 4, 2, TA, TB, false>;
+struct ConfigOf<CFG_64x64_SCALAR, TA, TB> {  // element-wise copies: any alignment
+    using type = SimtCfg<64, 64, 16, 32, 16, 4, 4, 4, 2, TA, TB, false>;
 };
 
 // Opt the kernel in to its dynamic shared memory once per device.
