@@ -99,38 +99,6 @@ bool aligned16(const void *ptr, long long ld, long long stride, int batch)
     return true;
 }
 
-long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
-
-int select_config(int ta, int tb, long long M, long long N, long long K, long long batch, bool aligned,
-                  int num_sms)
-{
-    (void)ta;
-    (void)tb;
-    (void)K;
-    if (!aligned) return CFG_64x64_SCALAR;
-    if (num_sms < 1) num_sms = 1;
-    const long long b = batch > 0 ? batch : 1;
-    if (ceil_div(M, 128) * ceil_div(N, 128) * b >= num_sms) return CFG_128x128;
-    if (ceil_div(M, 128) * ceil_div(N, 64) * b >= num_sms) return CFG_128x64;
-    return CFG_64x64;
-}
-
-int device_sm_count(int *out)
-{
-    static std::atomic<int> cache[64];
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
-    const int slot = dev & 63;
-    int v = cache[slot].load(std::memory_order_relaxed);
-    if (v <= 0) {
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-            return -1;
-        cache[slot].store(v, std::memory_order_relaxed);
-    }
-    *out = v;
-    return 0;
-}
-
 fgemm_status run(int config, const Problem &p)
 {
     bool noop = false;

@@ -4,7 +4,7 @@
 
 #include <cuda_runtime.h>
 
-#include "../../include/fgemm.h"
+#include "fgemm.h"
 
 namespace fgemm {
 
@@ -29,6 +29,13 @@ struct ConfigInfo {
 };
 
 extern const ConfigInfo kConfigs[NUM_CONFIGS];
+
+// SM count of the current device (cached per device).  Returns 0 on success.
+int device_sm_count(int *out);
+
+// The configuration for a problem (host-only; see fgemm_select_config).
+int select_config(int ta, int tb, long long M, long long N, long long K, long long batch,
+                  bool aligned, int num_sms);
 
 // Launch tables, one per transpose combination (defined in inst_<ta><tb>.cu).
 extern const LaunchFn kLaunchNN[NUM_CONFIGS];

@@ -1,0 +1,51 @@
+// plan.cu -- host-side planning: kernel configuration by shape.  Plain integer
+// host code; no CUDA call except the cached SM-count query.
+//
+// Size classes follow GEMM 优化详解, "矩阵大小选择策略" (small matrices get small
+// blocks, large ones large blocks), re-derived for a GPU whose SM count is read at
+// run time: the largest tile that still gives every SM a CTA is used.
+#include <cuda_runtime.h>
+
+#include <atomic>
+
+#include "fgemm_internal.h"
+
+namespace fgemm {
+
+namespace {
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+}  // namespace
+
+int select_config(int ta, int tb, long long M, long long N, long long K, long long batch,
+                  bool aligned, int num_sms)
+{
+    (void)ta;
+    (void)tb;
+    (void)K;
+    if (!aligned) return CFG_64x64_SCALAR;
+    if (num_sms < 1) num_sms = 1;
+    const long long b = batch > 0 ? batch : 1;
+    if (ceil_div(M, 128) * ceil_div(N, 128) * b >= num_sms) return CFG_128x128;
+    if (ceil_div(M, 128) * ceil_div(N, 64) * b >= num_sms) return CFG_128x64;
+    return CFG_64x64;
+}
+
+int device_sm_count(int *out)
+{
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    const int slot = dev & 63;
+    int v = cache[slot].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return -1;
+        cache[slot].store(v, std::memory_order_relaxed);
+    }
+    *out = v;
+    return 0;
+}
+
+}  // namespace fgemm

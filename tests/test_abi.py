@@ -121,3 +121,4 @@ def test_selector():
             for n in (1, 7, 64, 255, 1000, 5000):
                 c = sel(ta, tb, n, n, n, 1, 1, 152)
                 assert 0 <= c < fg.num_configs()
+

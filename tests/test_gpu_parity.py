@@ -134,3 +134,4 @@ def test_rejects_vector_config_on_unaligned_device_pointer():
     st = fg.gemm_explicit(0, 0, 0, 4, 4, 4, 1.0, A.data_ptr() + 4, 4, 0, A, 4, 0, 0.0, A, 4, 0, 1,
                           check=False)
     assert st == fg.ERR_NOT_SUPPORTED
+
