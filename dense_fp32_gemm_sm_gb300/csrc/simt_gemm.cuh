@@ -324,14 +324,17 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
                     }
                     cp_async_commit();
                 }
+                // Duplicate all of a[] first, then sweep the b pairs: each duplicate is
+                // produced well before its first use.
                 const float *a = reinterpret_cast<const float *>(&fa[cur][0]);
                 const unsigned long long *b2 = reinterpret_cast<const unsigned long long *>(&fb[cur][0]);
+                unsigned long long ad[TM];
 #pragma unroll
-                for (int i = 0; i < TM; ++i) {
-                    const unsigned long long ai = dup_pair(a[i]);
+                for (int i = 0; i < TM; ++i) ad[i] = dup_pair(a[i]);
 #pragma unroll
-                    for (int j = 0; j < TN / 2; ++j) ffma2(acc[i][j], ai, b2[j]);
-                }
+                for (int j = 0; j < TN / 2; ++j)
+#pragma unroll
+                    for (int i = 0; i < TM; ++i) ffma2(acc[i][j], ad[i], b2[j]);
             }
         }
         cp_async_wait<0>();

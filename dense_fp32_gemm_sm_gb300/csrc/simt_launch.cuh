@@ -16,7 +16,7 @@ struct ConfigOf;
 
 template <int TA, int TB>
 struct ConfigOf<CFG_128x128, TA, TB> {  // 256 threads, two CTAs per SM
-    using type = SimtCfg<128, 128, 16, 64, 32, 8, 8, 4, 2, TA, TB, true>;
+    using type = SimtCfg<128, 128, 32, 64, 32, 8, 8, 3, 2, TA, TB, true>;
 };
 template <int TA, int TB>
 struct ConfigOf<CFG_128x64, TA, TB> {  // 128 threads, three CTAs per SM
