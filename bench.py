@@ -26,6 +26,8 @@ and ``value`` counts the work of all ranks.
 from __future__ import annotations
 
 import argparse
+import glob
+import hashlib
 import json
 import os
 import statistics
@@ -69,7 +71,36 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--epilogue", choices=("workload", "none"), default="workload",
+                    help="'none' drops the workload's bias/ReLU (plain sgemm at the same shape)")
     return ap.parse_args(argv)
+
+
+def kernel_source_hash() -> str:
+    """Short hash of the CUDA sources; profile summaries record the hash they measured."""
+    m = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "dense_fp32_gemm_sm_gb300", "csrc", "*"))):
+        if f.endswith((".cu", ".cuh", ".h")):
+            m.update(os.path.basename(f).encode())
+            with open(f, "rb") as fh:
+                m.update(fh.read())
+    return m.hexdigest()[:16]
+
+
+def recorded_traffic(config_name: str, workload: str):
+    """DRAM bytes per launch from profiles/<config>_<workload>.md, if measured on these sources."""
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (config_name, workload))
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path, encoding="utf-8") as f:
+        for line in f:
+            key, sep, val = line.strip().partition(":")
+            if sep and key in ("source_sha256", "traffic_bytes_per_launch"):
+                fields[key] = val.strip()
+    if fields.get("source_sha256") != kernel_source_hash() or "traffic_bytes_per_launch" not in fields:
+        return None
+    return int(fields["traffic_bytes_per_launch"])
 
 
 # ---- distributed plumbing (one process per GPU, replicas) -----------------------------------
@@ -223,6 +254,8 @@ def run_fgemm(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     fg.library()
     w = workloads.make(args.workload)
+    if args.epilogue == "none":
+        w.bias, w.relu = None, False
     stream = torch.cuda.Stream(dev)
     sh = stream.cuda_stream
 
@@ -310,7 +343,8 @@ def run_fgemm(args, rank, world, local_rank):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "gpu_launches": args.steps * n_batch_launches,
         "roofline": {"bound": "alu", "achieved": round(achieved, 4), "peak": round(peak, 3),
-                     "unit": UNIT, "frac": round(achieved / peak, 4), "traffic": None,
+                     "unit": UNIT, "frac": round(achieved / peak, 4),
+                     "traffic": recorded_traffic(fg.config_name(chosen), args.workload),
                      "peak_source": "derived: %d SMs x %d FP32 FMA/clk x 2 FLOP x %.0f MHz" % (
                          sms, FMA_PER_CLK_PER_SM, STATED_SM_MHZ)},
         "e2e": {"value": round(e2e_flops / e2e_max / 1e12, 4), "unit": UNIT,
@@ -329,6 +363,7 @@ def run_fgemm(args, rank, world, local_rank):
 
 
 def describe(w):
+    """One-line description of a workload (name, shape, scalars, epilogue, seed)."""
     s = "%s: M=%d N=%d K=%d alpha=%g beta=%g op(A)=%s op(B)=%s" % (
         w.name, w.M, w.N, w.K, w.alpha, w.beta, "T" if w.ta else "N", "T" if w.tb else "N")
     if w.batch:
