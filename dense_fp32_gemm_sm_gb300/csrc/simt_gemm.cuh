@@ -146,75 +146,130 @@ struct SimtCfg {
 };
 
 // ---- Tile loaders --------------------------------------------------------------
+//
+// Each loader is set up once per tile (base pointer, edge masks) and then issues
+// one stage per call, advancing its pointer by BK along k.  Elements outside the
+// matrix are zero-filled (src-size 0, with an in-bounds dummy address).
 
 // Stored block whose rows run along k (K x MN storage, MN contiguous): rows
-// [k0, k0+BK) x columns [c0, c0+COLS) -> s[k][c] with row stride S_LD.
+// [k0, k0+BK) x columns [c0, c0+COLS) -> s[k][c] with row stride S_LD.  Thread t
+// always copies the same column chunk, in rows r_base + it * RSTEP.
 template <int BK, int COLS, int S_LD, int THREADS, bool VEC>
-__device__ __forceinline__ void load_k_rows(uint32_t s_tile, const float *g, long long ld, int k0,
-                                            int c0, int K, int Ccount, int tid)
-{
-    if constexpr (VEC) {
-        constexpr int CPR = COLS / 4;
-        constexpr int ITERS = BK * CPR / THREADS;
-#pragma unroll
-        for (int it = 0; it < ITERS; ++it) {
-            const int idx = tid + it * THREADS;
-            const int r = idx / CPR, cc = (idx % CPR) * 4;
-            const int gk = k0 + r, gc = c0 + cc;
-            const int bytes = gk < K ? clamp_bytes((long long)Ccount - gc) : 0;
-            const float *src = bytes ? g + (long long)gk * ld + gc : g;
-            cp_async_16(s_tile + (r * S_LD + cc) * 4, src, bytes);
-        }
-    } else {
-        constexpr int ITERS = BK * COLS / THREADS;
-#pragma unroll
-        for (int it = 0; it < ITERS; ++it) {
-            const int idx = tid + it * THREADS;
-            const int r = idx / COLS, cc = idx % COLS;
-            const int gk = k0 + r, gc = c0 + cc;
-            const bool ok = gk < K && gc < Ccount;
-            cp_async_4(s_tile + (r * S_LD + cc) * 4, ok ? g + (long long)gk * ld + gc : g, ok ? 4 : 0);
-        }
+struct KRowsCopy {
+    static constexpr int W = VEC ? 4 : 1;          // elements per copy
+    static constexpr int CPR = COLS / W;           // copies per row
+    static constexpr int RSTEP = THREADS / CPR;    // rows between a thread's copies
+    static constexpr int ITERS = BK / RSTEP;
+    static_assert(THREADS % CPR == 0 && BK % RSTEP == 0, "copies divide evenly over the threads");
+
+    const float *p;  // this thread's element in row (k0 + r_base) of the next stage
+    int bytes_c;     // bytes of the chunk inside the matrix along the columns (0 .. 4*W)
+    int r_base;
+
+    __device__ __forceinline__ void init(const float *g, long long ld, int c0, int Ccount, int tid)
+    {
+        r_base = tid / CPR;
+        const int c = c0 + (tid % CPR) * W;
+        bytes_c = VEC ? clamp_bytes((long long)Ccount - c) : (c < Ccount ? 4 : 0);
+        p = g + (long long)r_base * ld + c;
     }
-}
+
+    __device__ __forceinline__ void issue(uint32_t s_tile, const float *g, long long ld, int k0,
+                                          int K, int tid)
+    {
+        const uint32_t s0 = s_tile + (r_base * S_LD + (tid % CPR) * W) * 4;
+#pragma unroll
+        for (int it = 0; it < ITERS; ++it) {
+            const bool ok = k0 + r_base + it * RSTEP < K && bytes_c > 0;
+            const float *src = ok ? p + (long long)(it * RSTEP) * ld : g;
+            if constexpr (VEC)
+                cp_async_16(s0 + it * RSTEP * S_LD * 4, src, ok ? bytes_c : 0);
+            else
+                cp_async_4(s0 + it * RSTEP * S_LD * 4, src, ok ? 4 : 0);
+        }
+        p += (long long)BK * ld;
+    }
+};
 
 // Stored block whose rows run along m (or n) with k contiguous (MN x K storage):
 // rows [r0, r0+ROWS) x k [k0, k0+BK) -> s[k][r] (a transpose).  Each warp moves
-// an 8 (k) x 4 (rows) patch: lane&7 picks k, lane>>3 picks the row.
+// 8 (k) x 4 (rows) patches: lane&7 picks k, lane>>3 picks the row, so a warp reads
+// four full 32-byte sectors and writes 32 distinct banks.  A thread keeps one k and
+// copies rows r_base + it * RSTEP.
 template <int BK, int ROWS, int S_LD, int THREADS>
-__device__ __forceinline__ void load_k_cols(uint32_t s_tile, const float *g, long long ld, int r0,
-                                            int k0, int R, int K, int tid)
-{
-    constexpr int PATCHES_K = BK / 8;
-    constexpr int ITERS = BK * ROWS / THREADS;
-    const int lane = tid & 31, warp = tid >> 5;
-#pragma unroll
-    for (int it = 0; it < ITERS; ++it) {
-        const int w = warp + it * (THREADS / 32);
-        const int k = (w % PATCHES_K) * 8 + (lane & 7);
-        const int r = (w / PATCHES_K) * 4 + (lane >> 3);
-        const int gr = r0 + r, gk = k0 + k;
-        const bool ok = gr < R && gk < K;
-        cp_async_4(s_tile + (k * S_LD + r) * 4, ok ? g + (long long)gr * ld + gk : g, ok ? 4 : 0);
-    }
-}
+struct KColsCopy {
+    static constexpr int WARPS = THREADS / 32;
+    static constexpr int PATCHES_K = BK / 8;
+    static constexpr int RSTEP = 4 * WARPS / PATCHES_K;
+    static constexpr int ITERS = ROWS / RSTEP;
+    static_assert(WARPS % PATCHES_K == 0 && ROWS % RSTEP == 0 && ITERS <= 32,
+                  "patches divide evenly over the warps");
 
+    const float *p;  // this thread's element (row r0 + r_base, column k_local) of the next stage
+    unsigned rmask;  // bit it: row r0 + r_base + it * RSTEP is inside the matrix
+
+    __device__ __forceinline__ static int k_local(int tid) { return ((tid >> 5) % PATCHES_K) * 8 + (tid & 7); }
+    __device__ __forceinline__ static int r_base(int tid)
+    {
+        return ((tid >> 5) / PATCHES_K) * 4 + ((tid & 31) >> 3);
+    }
+
+    __device__ __forceinline__ void init(const float *g, long long ld, int r0, int R, int tid)
+    {
+        const int rb = r0 + r_base(tid);
+        rmask = 0;
+#pragma unroll
+        for (int it = 0; it < ITERS; ++it)
+            if (rb + it * RSTEP < R) rmask |= 1u << it;
+        p = g + (long long)rb * ld + k_local(tid);
+    }
+
+    __device__ __forceinline__ void issue(uint32_t s_tile, const float *g, long long ld, int k0,
+                                          int K, int tid)
+    {
+        const uint32_t s0 = s_tile + (k_local(tid) * S_LD + r_base(tid)) * 4;
+        const bool kok = k0 + k_local(tid) < K;
+#pragma unroll
+        for (int it = 0; it < ITERS; ++it) {
+            const bool ok = kok && ((rmask >> it) & 1u);
+            cp_async_4(s0 + it * RSTEP * 4, ok ? p + (long long)(it * RSTEP) * ld : g, ok ? 4 : 0);
+        }
+        p += BK;
+    }
+};
+
+// The two loaders of a configuration: A into sA[k][m], B into sB[k][n].
 template <class Cfg>
-__device__ __forceinline__ void load_stage(uint32_t sA, uint32_t sB, const GemmParams &p,
-                                           const float *A, const float *B, int m0, int n0, int k0,
-                                           int tid)
-{
-    if constexpr (Cfg::TA == 1)  // A stored K x M: rows are k already
-        load_k_rows<Cfg::BK, Cfg::BM, Cfg::A_LD, Cfg::THREADS, Cfg::VEC>(sA, A, p.lda, k0, m0, p.K,
-                                                                        p.M, tid);
-    else  // A stored M x K: transpose while copying
-        load_k_cols<Cfg::BK, Cfg::BM, Cfg::A_LD, Cfg::THREADS>(sA, A, p.lda, m0, k0, p.M, p.K, tid);
-    if constexpr (Cfg::TB == 0)  // B stored K x N
-        load_k_rows<Cfg::BK, Cfg::BN, Cfg::B_LD, Cfg::THREADS, Cfg::VEC>(sB, B, p.ldb, k0, n0, p.K,
-                                                                        p.N, tid);
-    else  // B stored N x K: transpose while copying
-        load_k_cols<Cfg::BK, Cfg::BN, Cfg::B_LD, Cfg::THREADS>(sB, B, p.ldb, n0, k0, p.N, p.K, tid);
-}
+struct StageCopy {
+    using ACopy = typename std::conditional<Cfg::TA == 1,
+                                            KRowsCopy<Cfg::BK, Cfg::BM, Cfg::A_LD, Cfg::THREADS, Cfg::VEC>,
+                                            KColsCopy<Cfg::BK, Cfg::BM, Cfg::A_LD, Cfg::THREADS>>::type;
+    using BCopy = typename std::conditional<Cfg::TB == 0,
+                                            KRowsCopy<Cfg::BK, Cfg::BN, Cfg::B_LD, Cfg::THREADS, Cfg::VEC>,
+                                            KColsCopy<Cfg::BK, Cfg::BN, Cfg::B_LD, Cfg::THREADS>>::type;
+    ACopy a;
+    BCopy b;
+
+    __device__ __forceinline__ void init(const GemmParams &p, const float *A, const float *B, int m0,
+                                         int n0, int tid)
+    {
+        if constexpr (Cfg::TA == 1)
+            a.init(A, p.lda, m0, p.M, tid);
+        else
+            a.init(A, p.lda, m0, p.M, tid);
+        if constexpr (Cfg::TB == 0)
+            b.init(B, p.ldb, n0, p.N, tid);
+        else
+            b.init(B, p.ldb, n0, p.N, tid);
+    }
+
+    __device__ __forceinline__ void issue(uint32_t sA, uint32_t sB, const GemmParams &p,
+                                          const float *A, const float *B, int k0, int tid)
+    {
+        a.issue(sA, A, p.lda, k0, p.K, tid);
+        b.issue(sB, B, p.ldb, k0, p.K, tid);
+    }
+};
 
 // Row (within the CTA tile) of the thread's i-th accumulator row, and column of
 // its j-th accumulator column: groups of 4 consecutive rows/columns, one 16-byte
@@ -274,12 +329,14 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
     const int KT = (p.K + Cfg::BK - 1) / Cfg::BK;
 
     if (KT > 0) {
+        StageCopy<Cfg> copy;
+        copy.init(p, A, B, m0, n0, tid);
         // Prologue: fill STAGES-1 slots, then wait for the first.
 #pragma unroll
         for (int s = 0; s < Cfg::STAGES - 1; ++s) {
             if (s < KT)
-                load_stage<Cfg>(sA_base + s * Cfg::A_STAGE * 4, sB_base + s * Cfg::B_STAGE * 4, p,
-                                A, B, m0, n0, s * Cfg::BK, tid);
+                copy.issue(sA_base + s * Cfg::A_STAGE * 4, sB_base + s * Cfg::B_STAGE * 4, p, A, B,
+                           s * Cfg::BK, tid);
             cp_async_commit();
         }
         cp_async_wait<Cfg::STAGES - 2>();
@@ -318,9 +375,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
                     if (nk < KT) {
                         int ws = slot + Cfg::STAGES - 1;
                         if (ws >= Cfg::STAGES) ws -= Cfg::STAGES;
-                        load_stage<Cfg>(sA_base + ws * Cfg::A_STAGE * 4,
-                                        sB_base + ws * Cfg::B_STAGE * 4, p, A, B, m0, n0,
-                                        nk * Cfg::BK, tid);
+                        copy.issue(sA_base + ws * Cfg::A_STAGE * 4, sB_base + ws * Cfg::B_STAGE * 4,
+                                   p, A, B, nk * Cfg::BK, tid);
                     }
                     cp_async_commit();
                 }
