@@ -18,7 +18,7 @@
 namespace fgemm {
 
 const ConfigInfo kConfigs[NUM_CONFIGS] = {
-    {"simt_128x128x32_t8x8_s3", 128, 128, true},
+    {"simt_128x128_t8x8", 128, 128, true},
     {"simt_128x64x16_t8x8_s4", 128, 64, true},
     {"simt_64x64x16_t4x4_s4", 64, 64, true},
     {"simt_64x64x16_t4x4_s4_scalar", 64, 64, false},

@@ -18,6 +18,13 @@ template <int TA, int TB>
 struct ConfigOf<CFG_128x128, TA, TB> {  // 256 threads, two CTAs per SM
     using type = SimtCfg<128, 128, 32, 64, 32, 8, 8, 3, 2, TA, TB, true>;
 };
+// A stored M x K and B stored N x K are both transposed while copying (32
+// element copies per thread per 32-deep stage); a 16-deep stage keeps that
+// under the 128-register budget, and five stages keep the same data in flight.
+template <>
+struct ConfigOf<CFG_128x128, 0, 1> {
+    using type = SimtCfg<128, 128, 16, 64, 32, 8, 8, 5, 2, 0, 1, true>;
+};
 template <int TA, int TB>
 struct ConfigOf<CFG_128x64, TA, TB> {  // 128 threads, three CTAs per SM
     using type = SimtCfg<128, 64, 16, 64, 32, 8, 8, 4, 3, TA, TB, true>;
