@@ -71,6 +71,8 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--math", choices=("fp32", "tf32", "3xtf32"), default="fp32",
+                    help="arithmetic: FP32 CUDA cores (the metric) or the tcgen05 tensor-core path")
     ap.add_argument("--epilogue", choices=("workload", "none"), default="workload",
                     help="'none' drops the workload's bias/ReLU (plain sgemm at the same shape)")
     return ap.parse_args(argv)
@@ -196,18 +198,39 @@ class ClockSampler:
 
 # ---- the library arm ----------------------------------------------------------------------
 
+def tensor_peak_tflops(math: str):
+    """Dense TF32 tensor peak from the measured BF16 peak (MEASURED_PEAKS.json, burst)
+    times the nominal TF32/BF16 ratio 1.1/2.25; 3xTF32 does three TF32 products per
+    FP32 product, so its FP32-equivalent peak is a third of that."""
+    bf16, src = 1900.0, "fallback 1.9 PFLOP/s bf16"
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            bf16, src = float(json.load(f)["bf16_tflops"]), "measured bf16 burst"
+    tf32 = bf16 * 1.1 / 2.25
+    div = 3.0 if math == "3xtf32" else 1.0
+    return tf32 / div, "%s %.1f TFLOP/s x 1.1/2.25 (nominal TF32/BF16)%s" % (
+        src, bf16, " / 3 products" if div == 3.0 else "")
+
+
 def stated_peak_tflops(device) -> tuple:
     sms = torch.cuda.get_device_properties(device).multi_processor_count
     return sms * FMA_PER_CLK_PER_SM * 2 * STATED_SM_MHZ * 1e6 / 1e12, sms
 
 
-def _launch(fg, w, cfg, dA, dB, dC, dbias, stream):
+MATHS = {"fp32": 0, "tf32": 1, "3xtf32": 2}
+
+
+def _launch(fg, w, cfg, dA, dB, dC, dbias, stream, math="fp32"):
     """One step: the library call of the workload (the bench's unit of work)."""
     nb = max(1, w.batch)
     sA = w.M * w.K if w.batch else 0
     sB = w.N * w.K if w.batch else 0
     sC = w.M * w.N if w.batch else 0
-    if cfg >= 0:
+    if math != "fp32":
+        fg.gemm_math(MATHS[math], w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, sA, dB, w.ldb, sB,
+                     w.beta, dC, w.ldc, sC, nb, dbias, w.relu, stream=stream)
+    elif cfg >= 0:
         fg.gemm_explicit(cfg, w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, sA, dB, w.ldb, sB,
                          w.beta, dC, w.ldc, sC, nb, dbias, w.relu, stream=stream)
     elif w.batch:
@@ -270,7 +293,7 @@ def run_fgemm(args, rank, world, local_rank):
     def step():
         if dC0 is not None:  # beta != 0: restore C so every step computes the same thing
             dC.copy_(dC0)
-        _launch(fg, w, args.config, dA, dB, dC, dbias, sh)
+        _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -290,7 +313,7 @@ def run_fgemm(args, rank, world, local_rank):
             if dC0 is not None:
                 dC.copy_(dC0)
             starts[i].record(stream)
-            _launch(fg, w, args.config, dA, dB, dC, dbias, sh)
+            _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math)
             ends[i].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
@@ -319,7 +342,7 @@ def run_fgemm(args, rank, world, local_rank):
             dB.copy_(hB, non_blocking=True)
             if hC0 is not None:
                 dC.copy_(hC0, non_blocking=True)
-            _launch(fg, w, args.config, dA, dB, dC, dbias, sh)
+            _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math)
             hC.copy_(dC, non_blocking=True)
         e_end.record(stream)
     torch.cuda.synchronize()
@@ -330,6 +353,10 @@ def run_fgemm(args, rank, world, local_rank):
     if chosen < 0:
         aligned = True
         chosen = fg.select_config(w.ta, w.tb, w.M, w.N, w.K, max(1, w.batch), aligned, sms)
+    kernel_name = fg.config_name(chosen)
+    tensor_path = args.math != "fp32" and w.ta == 0 and w.tb == 1
+    if tensor_path:
+        kernel_name = "tcgen05_%s_128x128" % args.math
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_s * 1e3 /
@@ -337,8 +364,10 @@ def run_fgemm(args, rank, world, local_rank):
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": (round(value / PAGES_4096_TFLOPS, 3)
                         if args.workload == "square4096" else None),
-        "dtype": "f32", "data": "synthetic",
-        "config": {"workload": describe(w), "kernel_config": fg.config_name(chosen),
+        "dtype": {"fp32": "f32", "tf32": "tf32 (fp32 accumulate)",
+                  "3xtf32": "3xtf32 (tf32 hi/lo split, fp32 accumulate)"}[args.math]
+        if tensor_path else "f32", "data": "synthetic",
+        "config": {"workload": describe(w), "kernel_config": kernel_name,
                    "l2": "flushed between steps (256 MiB memset outside the timed event pair)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "gpu_launches": args.steps * n_batch_launches,
@@ -351,10 +380,17 @@ def run_fgemm(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "wall_s_timed_region": round(wall, 3),
     }
+    if tensor_path:
+        tpeak, tsrc = tensor_peak_tflops(args.math)
+        line["roofline"] = {"bound": "tensor", "achieved": round(achieved, 4),
+                            "peak": round(tpeak, 2), "unit": UNIT,
+                            "frac": round(achieved / tpeak, 4),
+                            "traffic": recorded_traffic(kernel_name, args.workload),
+                            "peak_source": tsrc}
     clk = sampler.summary()
     if clk is not None:
         line["clocks"] = clk
-        if clk.get("sm_mhz"):
+        if clk.get("sm_mhz") and not tensor_path:
             line["roofline"]["frac_at_measured_clock"] = round(
                 achieved / (peak * clk["sm_mhz"] / STATED_SM_MHZ), 4)
     if rank == 0 and not args.no_cpu_baseline:

@@ -9,11 +9,17 @@ from ._binding import (  # noqa: F401
     ERR_INVALID_VALUE,
     ERR_LAUNCH,
     ERR_NOT_SUPPORTED,
+    ERR_TIMEOUT,
+    MATH_3XTF32,
+    MATH_FP32,
+    MATH_TF32,
     OK,
     OP_N,
     OP_T,
     FgemmError,
     config_name,
+    device_status,
+    gemm_math,
     gemm_explicit,
     library,
     num_configs,

@@ -18,7 +18,8 @@ import threading
 from . import _build
 
 OP_N, OP_T = 0, 1
-OK, ERR_INVALID_VALUE, ERR_LAUNCH, ERR_NOT_SUPPORTED = 0, 1, 2, 3
+OK, ERR_INVALID_VALUE, ERR_LAUNCH, ERR_NOT_SUPPORTED, ERR_TIMEOUT = 0, 1, 2, 3, 4
+MATH_FP32, MATH_TF32, MATH_3XTF32 = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -51,6 +52,10 @@ def library() -> ctypes.CDLL:
                 "fgemm_gemm_explicit": [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                         _c_vp, _c_int, _c_ll, _c_vp, _c_int, _c_ll, _c_float,
                                         _c_vp, _c_int, _c_ll, _c_int, _c_vp, _c_int, _c_vp],
+                "fgemm_gemm_math": [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                    _c_vp, _c_int, _c_ll, _c_vp, _c_int, _c_ll, _c_float,
+                                    _c_vp, _c_int, _c_ll, _c_int, _c_vp, _c_int, _c_vp],
+                "fgemm_device_status": [_c_int],
                 "fgemm_select_config": [_c_int] * 8,
                 "fgemm_num_configs": [],
                 "fgemm_config_name": [_c_int],
@@ -156,3 +161,20 @@ def gemm_explicit(config, transa, transb, M, N, K, alpha, A, lda, strideA, B, ld
     if check:
         _check(st, "fgemm_gemm_explicit")
     return st
+
+
+def gemm_math(math, transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C,
+              ldc, strideC, batch, bias=None, apply_relu=False, stream=None, check=True) -> int:
+    """``fgemm_gemm_math``: FP32 CUDA cores (MATH_FP32) or tcgen05 TF32 / 3xTF32."""
+    st = library().fgemm_gemm_math(
+        int(math), int(transa), int(transb), M, N, K, alpha, _ptr(A), lda, strideA, _ptr(B), ldb,
+        strideB, beta, _ptr(C), ldc, strideC, batch, _ptr(bias), 1 if apply_relu else 0,
+        _stream(stream, C, A, B))
+    if check:
+        _check(st, "fgemm_gemm_math")
+    return st
+
+
+def device_status(clear=True) -> int:
+    """``fgemm_device_status``: ERR_TIMEOUT if a tensor-core wait ran out (call after a sync)."""
+    return library().fgemm_device_status(1 if clear else 0)

@@ -177,6 +177,43 @@ Problem make_problem(fgemm_op ta, fgemm_op tb, int M, int N, int K, float alpha,
 using fgemm::make_problem;
 using fgemm::run;
 
+namespace fgemm {
+namespace {
+
+fgemm_status run_math(fgemm_math math, const Problem &p)
+{
+    if (math == FGEMM_MATH_FP32) return run(-1, p);
+    if (math != FGEMM_MATH_TF32 && math != FGEMM_MATH_3XTF32) return FGEMM_ERR_INVALID_VALUE;
+    bool noop = false;
+    const fgemm_status st = validate(p, &noop);
+    if (st != FGEMM_OK || noop) return st;
+    TcProblem q;
+    q.ta = p.ta;
+    q.tb = p.tb;
+    q.M = p.M;
+    q.N = p.N;
+    q.K = p.K;
+    q.alpha = p.alpha;
+    q.beta = p.beta;
+    q.A = p.A;
+    q.lda = p.lda;
+    q.sA = p.sA;
+    q.B = p.B;
+    q.ldb = p.ldb;
+    q.sB = p.sB;
+    q.C = p.C;
+    q.ldc = p.ldc;
+    q.sC = p.sC;
+    q.batch = p.batch;
+    q.bias = p.bias;
+    q.relu = p.relu;
+    if (!tc_supported(q)) return run(-1, p);
+    return launch_tc(math == FGEMM_MATH_3XTF32 ? 3 : 1, q, p.stream);
+}
+
+}  // namespace
+}  // namespace fgemm
+
 extern "C" {
 
 fgemm_status fgemm_sgemm(fgemm_op transa, fgemm_op transb, int M, int N, int K, float alpha,
@@ -217,6 +254,19 @@ fgemm_status fgemm_gemm_explicit(int config, fgemm_op transa, fgemm_op transb, i
                             C, ldc, strideC, batch, bias, apply_relu, stream));
 }
 
+fgemm_status fgemm_gemm_math(fgemm_math math, fgemm_op transa, fgemm_op transb, int M, int N,
+                             int K, float alpha, const float *A, int lda, long long strideA,
+                             const float *B, int ldb, long long strideB, float beta, float *C,
+                             int ldc, long long strideC, int batch, const float *bias,
+                             int apply_relu, cudaStream_t stream)
+{
+    return fgemm::run_math(math, make_problem(transa, transb, M, N, K, alpha, A, lda, strideA, B,
+                                              ldb, strideB, beta, C, ldc, strideC, batch, bias,
+                                              apply_relu, stream));
+}
+
+fgemm_status fgemm_device_status(int clear) { return fgemm::tc_device_status(clear); }
+
 const char *fgemm_status_string(fgemm_status status)
 {
     switch (status) {
@@ -225,6 +275,8 @@ const char *fgemm_status_string(fgemm_status status)
     case FGEMM_ERR_LAUNCH: return "FGEMM_ERR_LAUNCH: a CUDA call or kernel launch failed";
     case FGEMM_ERR_NOT_SUPPORTED:
         return "FGEMM_ERR_NOT_SUPPORTED: the configuration cannot run this call";
+    case FGEMM_ERR_TIMEOUT:
+        return "FGEMM_ERR_TIMEOUT: a tensor-core kernel gave up waiting; its output is undefined";
     }
     return "unknown fgemm_status";
 }

@@ -38,6 +38,29 @@ int device_sm_count(int *out);
 int select_config(int ta, int tb, long long M, long long N, long long K, long long batch,
                   bool aligned, int num_sms);
 
+// A validated problem for the tensor-core path (tc_gemm.cu).
+struct TcProblem {
+    int ta, tb, M, N, K;
+    float alpha, beta;
+    const float *A;
+    long long lda, sA;
+    const float *B;
+    long long ldb, sB;
+    float *C;
+    long long ldc, sC;
+    int batch;
+    const float *bias;
+    int relu;
+};
+
+// Whether the tcgen05 kernels can run this problem (layout, alignment, sizes).
+bool tc_supported(const TcProblem &q);
+// Launch the tcgen05 kernel: mode 1 = TF32, 3 = 3xTF32.
+fgemm_status launch_tc(int mode, const TcProblem &q, cudaStream_t stream);
+// FGEMM_ERR_TIMEOUT if a tensor-core kernel on the current device recorded a wait
+// that ran out (cleared when `clear`), FGEMM_OK otherwise.
+fgemm_status tc_device_status(int clear);
+
 // Launch tables, one per transpose combination (defined in inst_<ta><tb>.cu).
 extern const LaunchFn kLaunchNN[NUM_CONFIGS];
 extern const LaunchFn kLaunchNT[NUM_CONFIGS];

@@ -1,0 +1,191 @@
+// tc_gemm.cu -- host side of the tensor-core path: TMA tensor maps, launch, and the
+// device error word that bounded waits report into.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cstdint>
+#include <cstring>
+
+#include "fgemm_internal.h"
+#include "tc_gemm.cuh"
+
+namespace fgemm {
+
+// Bits set by a tensor-core kernel whose mbarrier wait ran out (see tc::ERR_*).
+__device__ unsigned g_tc_error;
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static std::atomic<void *> fn{nullptr};
+    void *f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        fn.store(f, std::memory_order_release);
+    }
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+}
+
+// One operand as a 3-D tensor map (inner, outer, batch), `batch` problems `stride`
+// elements apart.  K-major storage (rows x K, K contiguous): inner = K, boxes of
+// 32 x 128 with the 128-byte swizzle (the canonical UMMA layout).  MN-major storage
+// (K x rows, rows contiguous): inner = rows, plain 128 x 32 boxes that the kernel
+// transposes on chip.
+bool make_operand_map(CUtensorMap *map, const float *base, bool kmajor, long long rows, long long K,
+                      long long ld, long long batch, long long stride)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    const long long outer = kmajor ? rows : K;
+    if (batch <= 1) stride = ld * outer;  // unused extent-1 dimension; any legal stride
+    const cuuint64_t dims[3] = {(cuuint64_t)(kmajor ? K : rows), (cuuint64_t)outer,
+                                (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)stride * 4};
+    const cuuint32_t box[3] = {kmajor ? (cuuint32_t)tc::BK : 128u, kmajor ? 128u : (cuuint32_t)tc::BK,
+                               1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    const CUresult r =
+        enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            kmajor ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+int current_device(int *dev) { return cudaGetDevice(dev) == cudaSuccess ? 0 : -1; }
+
+// Device address of g_tc_error on the current device (looked up once per device).
+unsigned *error_word()
+{
+    static std::atomic<unsigned *> cache[64];
+    int dev = 0;
+    if (current_device(&dev) != 0) return nullptr;
+    unsigned *p = cache[dev & 63].load(std::memory_order_acquire);
+    if (!p) {
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_tc_error) != cudaSuccess) return nullptr;
+        p = static_cast<unsigned *>(addr);
+        cache[dev & 63].store(p, std::memory_order_release);
+    }
+    return p;
+}
+
+template <int MODE, int TA, int TB>
+cudaError_t prepare_tc()
+{
+    static std::atomic<unsigned long long> ready{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (ready.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(tc::tc_gemm_kernel<MODE, TA, TB>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Layout<MODE>::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    ready.fetch_or(bit, std::memory_order_acq_rel);
+    return cudaSuccess;
+}
+
+template <int MODE, int TA, int TB>
+fgemm_status launch_tc_mode(tc::TcParams &p, int batch, cudaStream_t stream)
+{
+    unsigned *err = error_word();
+    if (!err || prepare_tc<MODE, TA, TB>() != cudaSuccess) {
+        (void)cudaGetLastError();
+        return FGEMM_ERR_LAUNCH;
+    }
+    const long long tiles = (long long)p.tiles_m * p.tiles_n;
+    const int kMaxZ = 65535;
+    for (int b0 = 0; b0 < batch; b0 += kMaxZ) {
+        const int nb = batch - b0 < kMaxZ ? batch - b0 : kMaxZ;
+        p.batch0 = b0;
+        tc::tc_gemm_kernel<MODE, TA, TB><<<dim3((unsigned)tiles, 1, (unsigned)nb), tc::THREADS,
+                                           tc::Layout<MODE>::SMEM_BYTES, stream>>>(p, err);
+        if (cudaGetLastError() != cudaSuccess) return FGEMM_ERR_LAUNCH;
+    }
+    return FGEMM_OK;
+}
+
+}  // namespace
+
+bool tc_supported(const TcProblem &q)
+{
+    if (q.K <= 0 || q.alpha == 0.0f || q.M <= 0 || q.N <= 0 || q.batch <= 0) return false;
+    if ((q.ta != 0 && q.ta != 1) || (q.tb != 0 && q.tb != 1)) return false;
+    auto ok16 = [](const void *ptr) { return reinterpret_cast<uintptr_t>(ptr) % 16 == 0; };
+    if (!ok16(q.A) || !ok16(q.B) || q.lda % 4 || q.ldb % 4) return false;
+    if (q.batch > 1 && (q.sA % 4 || q.sB % 4)) return false;
+    const long long lim = 1ll << 38;  // tensor-map strides are below 2^40 bytes
+    if (q.lda >= lim || q.ldb >= lim || q.sA >= lim || q.sB >= lim) return false;
+    if ((long long)((q.M + tc::BM - 1) / tc::BM) * ((q.N + tc::BN - 1) / tc::BN) > INT_MAX) return false;
+    return encode_fn() != nullptr;
+}
+
+fgemm_status launch_tc(int mode, const TcProblem &q, cudaStream_t stream)
+{
+    tc::TcParams p;
+    std::memset(&p, 0, sizeof(p));
+    if (!make_operand_map(&p.tmA, q.A, q.ta == 0, q.M, q.K, q.lda, q.batch, q.sA) ||
+        !make_operand_map(&p.tmB, q.B, q.tb == 1, q.N, q.K, q.ldb, q.batch, q.sB))
+        return FGEMM_ERR_NOT_SUPPORTED;
+    p.C = q.C;
+    p.bias = q.bias;
+    p.ldc = q.ldc;
+    p.strideC = q.batch > 1 ? q.sC : 0;
+    p.M = q.M;
+    p.N = q.N;
+    p.K = q.K;
+    p.alpha = q.alpha;
+    p.beta = q.beta;
+    p.relu = q.relu ? 1 : 0;
+    p.c_vec = (reinterpret_cast<uintptr_t>(q.C) % 16 == 0 && q.ldc % 4 == 0 &&
+               (q.batch <= 1 || q.sC % 4 == 0))
+                  ? 1
+                  : 0;
+    p.tiles_m = (q.M + tc::BM - 1) / tc::BM;
+    p.tiles_n = (q.N + tc::BN - 1) / tc::BN;
+    const int layout = q.ta * 2 + q.tb;  // 0: NN, 1: NT, 2: TN, 3: TT
+    if (mode == tc::MODE_3XTF32) {
+        switch (layout) {
+        case 0: return launch_tc_mode<tc::MODE_3XTF32, 0, 0>(p, q.batch, stream);
+        case 1: return launch_tc_mode<tc::MODE_3XTF32, 0, 1>(p, q.batch, stream);
+        case 2: return launch_tc_mode<tc::MODE_3XTF32, 1, 0>(p, q.batch, stream);
+        default: return launch_tc_mode<tc::MODE_3XTF32, 1, 1>(p, q.batch, stream);
+        }
+    }
+    switch (layout) {
+    case 0: return launch_tc_mode<tc::MODE_TF32, 0, 0>(p, q.batch, stream);
+    case 1: return launch_tc_mode<tc::MODE_TF32, 0, 1>(p, q.batch, stream);
+    case 2: return launch_tc_mode<tc::MODE_TF32, 1, 0>(p, q.batch, stream);
+    default: return launch_tc_mode<tc::MODE_TF32, 1, 1>(p, q.batch, stream);
+    }
+}
+
+fgemm_status tc_device_status(int clear)
+{
+    int dev = 0;
+    if (current_device(&dev) != 0) return FGEMM_ERR_LAUNCH;
+    unsigned v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_tc_error, sizeof(v)) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return FGEMM_ERR_LAUNCH;
+    }
+    if (v != 0 && clear) {
+        const unsigned zero = 0;
+        if (cudaMemcpyToSymbol(g_tc_error, &zero, sizeof(zero)) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return FGEMM_ERR_LAUNCH;
+        }
+    }
+    return v ? FGEMM_ERR_TIMEOUT : FGEMM_OK;
+}
+
+}  // namespace fgemm

@@ -1,0 +1,509 @@
+// tc_gemm.cuh -- the same GEMM on the 5th-generation tensor cores of sm_103a
+// (tcgen05), in TF32 or in 3xTF32.
+//
+// The pages name tensor cores as the next step after the CUDA-core ladder
+// (GEMM 优化详解, "进一步优化方向 / Tensor Core"; GPU架构下的矩阵乘法深入优化,
+// "6. fp32 + tensor core" uses FP16 WMMA on V100).  Here the contraction stays FP32
+// in, FP32 out:
+//
+//   TF32   : D += A * B with each FP32 operand read as TF32 (10 explicit mantissa bits).
+//   3xTF32 : every operand x is split on chip into hi = x with the low 13 mantissa
+//            bits cleared (exactly representable in TF32) and lo = x - hi (exact in
+//            FP32), and D += A_lo*B_hi + A_hi*B_lo + A_hi*B_hi.  The dropped term
+//            A_lo*B_lo and the TF32 rounding of lo are about 2^-21 relative to |a||b|:
+//            close to FP32 accuracy (the split of Ootomo & Yokota, "Recovering single
+//            precision accuracy from Tensor Cores while surpassing the FP32 theoretical
+//            peak performance", 2022).
+//
+// Structure (one CTA per 128 x 128 tile of C, six warps):
+//   warp 0     TMA producer: one lane streams 128 x 32 tiles of A and B (128-byte
+//              swizzled, the canonical K-major operand layout) into a ring of stages.
+//   warp 1     allocates the 128 x 128 FP32 accumulator in tensor memory; one lane
+//              issues tcgen05.mma (M=128, N=128, K=8) and commits each stage back to
+//              the producer through an mbarrier.
+//   warps 2-5  3xTF32: split each stage into hi/lo in place; then, for every mode,
+//              the epilogue: tcgen05.ld of their 32 accumulator lanes, alpha, beta*C,
+//              bias, ReLU, stores.
+// Operands stored K-major (A as M x K, B as N x K) arrive by TMA already in the
+// canonical layout.  An operand stored MN-major (A as K x M, B as K x N) arrives as a
+// plain 32 x 128 tile and warps 2-5 transpose it in place into the canonical K-major
+// layout (splitting it too in 3xTF32), so every MMA reads K-major descriptors.
+// Every mbarrier wait is bounded by a
+// wall-clock limit: on expiry the kernel records the failure in a device error word,
+// drains its own copies and MMAs, frees its tensor memory and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fgemm {
+namespace tc {
+
+constexpr int BM = 128, BN = 128, BK = 32;  // BK FP32 values = one 128-byte swizzle row
+constexpr int UMMA_K = 8;                   // K of one kind::tf32 MMA (32 bytes)
+constexpr int TILE_A_BYTES = BM * BK * 4;   // 16 KB
+constexpr int TILE_B_BYTES = BN * BK * 4;   // 16 KB
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = BN;          // FP32 accumulator: 128 lanes x BN columns
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per wait
+
+// Error bits recorded in the device error word.
+constexpr unsigned ERR_PRODUCER = 1u, ERR_MMA_WAIT = 2u, ERR_SPLIT_WAIT = 4u, ERR_EPILOGUE = 8u,
+                   ERR_DRAIN = 16u;
+
+enum Mode { MODE_TF32 = 1, MODE_3XTF32 = 3 };
+
+template <int MODE>
+struct Layout {
+    static constexpr int STAGES = MODE == MODE_3XTF32 ? 3 : 3;
+    // Per stage: A, B (raw, or hi after the split), then A_lo, B_lo in 3xTF32.
+    static constexpr int STAGE_BYTES =
+        (TILE_A_BYTES + TILE_B_BYTES) * (MODE == MODE_3XTF32 ? 2 : 1);
+    static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
+    // full[S], split[S], empty[S], acc_full, drain, read_done (8 bytes each) + TMEM slot
+    static constexpr int BAR_BYTES = (3 * STAGES + 3) * 8 + 8;
+    static constexpr int SMEM_BYTES = 1024 + BAR_OFFSET + BAR_BYTES;  // + alignment slack
+};
+
+struct TcParams {
+    // K-major operand: dims (K, rows, batch), box (32, 128, 1), 128-byte swizzle.
+    // MN-major operand: dims (rows, K, batch), box (128, 32, 1), no swizzle.
+    CUtensorMap tmA;
+    CUtensorMap tmB;
+    float *C;
+    const float *bias;
+    long long ldc, strideC;
+    int M, N, K;
+    float alpha, beta;
+    int relu;
+    int c_vec;
+    int tiles_m, tiles_n;
+    int batch0;  // first problem of this launch (the launch covers gridDim.z problems)
+};
+
+// ---- PTX wrappers ----------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t cvta_smem(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t global_timer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Wait until the phase with the given parity has completed, for at most
+// kWaitLimitNs.  With `give_up_on_error`, stop early once any CTA has recorded an
+// error (drain waits must not: they guard copies still landing in shared memory).
+// On expiry, record `code` and return false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err,
+                                          unsigned code, bool give_up_on_error = true)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer();
+    for (uint32_t spin = 1;; ++spin) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((spin & 255u) == 0) {
+            if (give_up_on_error && *(volatile unsigned *)err != 0u) return false;
+            if (global_timer() - t0 > kWaitLimitNs) {
+                atomicOr(err, code);
+                return false;
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
+                                            int c0, int c1, int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile in the canonical 128-byte
+// swizzled layout: rows of 128 bytes (32 FP32 along K), groups of 8 rows 1024 bytes
+// apart (stride byte offset), 1024-byte aligned base, descriptor version 1.
+__device__ __forceinline__ uint64_t kmajor_sw128_desc(uint32_t smem_addr)
+{
+    return (uint64_t)((smem_addr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) |
+           ((uint64_t)(1024 >> 4) << 32) | ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// Instruction descriptor of kind::tf32: D FP32, A and B TF32, both K-major, M x N.
+__host__ __device__ constexpr uint32_t make_idesc(int m, int n)
+{
+    return (1u << 4) | (2u << 7) | (2u << 10) | ((uint32_t)(n >> 3) << 17) |
+           ((uint32_t)(m >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_tf32(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n"
+        "}\n" ::"r"(tmem_d),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar)
+{
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                     bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+          "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+          "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// hi = x with the 13 low mantissa bits cleared (a TF32 value); lo = x - hi, exact.
+__device__ __forceinline__ void split_tf32(float x, float &hi, float &lo)
+{
+    hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+    lo = x - hi;
+}
+
+// ---- Split / transpose of one stage (warps 2-5, thread t in 0..127) --------------
+
+// K-major operand tile (already in the canonical swizzled layout): split in place,
+// element by element; lo goes to the same offsets of the lo tile.
+__device__ __forceinline__ void split_kmajor(float4 *tile, float4 *lo, int t)
+{
+#pragma unroll 4
+    for (int c = t; c < TILE_A_BYTES / 16; c += 128) {
+        const float4 v = tile[c];
+        float4 h, l;
+        split_tf32(v.x, h.x, l.x);
+        split_tf32(v.y, h.y, l.y);
+        split_tf32(v.z, h.z, l.z);
+        split_tf32(v.w, h.w, l.w);
+        tile[c] = h;
+        lo[c] = l;
+    }
+}
+
+// Byte offset of element (row r, k) in a 128-row K-major tile with 128-byte rows and
+// the 128-byte swizzle (16-byte chunk index XOR row % 8, 8-row groups of 1024 bytes).
+__device__ __forceinline__ int kmajor_offset(int r, int kq)
+{
+    return (r >> 3) * 1024 + (r & 7) * 128 + ((kq ^ (r & 7)) << 4);
+}
+
+// MN-major tile: 32 rows of k, each 128 floats along m (or n), as TMA wrote it.  Each
+// thread reads 8 (row, k-quad) pairs -- rows lane + 32j, k-quads 2*wq + i -- so a warp
+// reads 32 consecutive floats of one k row per load; after every converter thread has
+// read (bounded wait on read_done), it writes its values back K-major (swizzled
+// 16-byte chunks, conflict-free per quarter warp), and the lo parts for 3xTF32.
+template <bool SPLIT>
+__device__ __forceinline__ bool transpose_mnmajor(uint8_t *tile, uint8_t *lo, int t, uint32_t read_done,
+                                                  uint32_t parity, unsigned *err)
+{
+    const int lane = t & 31, wq = t >> 5;
+    const float *src = reinterpret_cast<const float *>(tile);
+    float v[8][4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int r = lane + 32 * j, kq = 2 * wq + i;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[2 * j + i][e] = src[(4 * kq + e) * 128 + r];
+        }
+    mbar_arrive(read_done);
+    if (!mbar_wait(read_done, parity, err, ERR_SPLIT_WAIT)) return false;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int r = lane + 32 * j, kq = 2 * wq + i;
+            const float *x = v[2 * j + i];
+            float4 h, l;
+            if constexpr (SPLIT) {
+                split_tf32(x[0], h.x, l.x);
+                split_tf32(x[1], h.y, l.y);
+                split_tf32(x[2], h.z, l.z);
+                split_tf32(x[3], h.w, l.w);
+                *reinterpret_cast<float4 *>(lo + kmajor_offset(r, kq)) = l;
+            } else {
+                h = make_float4(x[0], x[1], x[2], x[3]);
+            }
+            *reinterpret_cast<float4 *>(tile + kmajor_offset(r, kq)) = h;
+        }
+    return true;
+}
+
+// ---- The kernel ------------------------------------------------------------------
+
+// MODE: MODE_TF32 or MODE_3XTF32.  TA = 0: A stored M x K (K-major), 1: K x M.
+// TB = 1: B stored N x K (K-major), 0: K x N.
+template <int MODE, int TA, int TB>
+__global__ void __launch_bounds__(THREADS, 1)
+    tc_gemm_kernel(const __grid_constant__ TcParams p, unsigned *err)
+{
+    using L = Layout<MODE>;
+    constexpr int S = L::STAGES;
+    constexpr bool A_K = TA == 0, B_K = TB == 1;
+    constexpr bool THREE = MODE == MODE_3XTF32;
+    constexpr bool CONVERT = THREE || !A_K || !B_K;  // warps 2-5 touch each stage
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte alignment of the operand tiles (the swizzle atom).
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const uint32_t sbase = cvta_smem(smem);
+    const uint32_t bar0 = sbase + L::BAR_OFFSET;
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto split_bar = [&](int s) { return bar0 + 8u * (S + s); };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
+    const uint32_t acc_bar = bar0 + 8u * (3 * S);
+    const uint32_t drain_bar = acc_bar + 8u;
+    const uint32_t read_bar = acc_bar + 16u;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::BAR_OFFSET + 8 * (3 * S + 3));
+
+    auto a_off = [&](int s) { return s * L::STAGE_BYTES; };
+    auto b_off = [&](int s) { return s * L::STAGE_BYTES + TILE_A_BYTES; };
+    auto alo_off = [&](int s) { return s * L::STAGE_BYTES + TILE_A_BYTES + TILE_B_BYTES; };
+    auto blo_off = [&](int s) { return s * L::STAGE_BYTES + 2 * TILE_A_BYTES + TILE_B_BYTES; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int tile = blockIdx.x;
+    const int tm = tile / p.tiles_n, tn = tile % p.tiles_n;
+    const int m0 = tm * BM, n0 = tn * BN;
+    const int bz = p.batch0 + blockIdx.z;
+    const int KT = (p.K + BK - 1) / BK;
+
+    if (warp == 0 && lane == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(split_bar(s), 128);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(acc_bar, 1);
+        mbar_init(drain_bar, 1);
+        mbar_init(read_bar, 128);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         cvta_smem(tmem_slot)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
+
+    if (warp == 0) {
+        // ---- TMA producer ----
+        if (lane == 0) {
+            int issued = 0;
+            for (int kb = 0; kb < KT; ++kb) {
+                const int s = kb % S, round = kb / S;
+                if (round > 0 && !mbar_wait(empty_bar(s), (round - 1) & 1, err, ERR_PRODUCER)) break;
+                mbar_arrive_expect_tx(full_bar(s), TILE_A_BYTES + TILE_B_BYTES);
+                if constexpr (A_K)
+                    tma_load_3d(sbase + a_off(s), &p.tmA, full_bar(s), kb * BK, m0, bz);
+                else
+                    tma_load_3d(sbase + a_off(s), &p.tmA, full_bar(s), m0, kb * BK, bz);
+                if constexpr (B_K)
+                    tma_load_3d(sbase + b_off(s), &p.tmB, full_bar(s), kb * BK, n0, bz);
+                else
+                    tma_load_3d(sbase + b_off(s), &p.tmB, full_bar(s), n0, kb * BK, bz);
+                ++issued;
+            }
+            // Never leave with copies in flight into this CTA's shared memory.
+            for (int kb = issued - S < 0 ? 0 : issued - S; kb < issued; ++kb)
+                mbar_wait(full_bar(kb % S), (kb / S) & 1, err, ERR_DRAIN, false);
+        }
+    } else if (warp == 1) {
+        // ---- MMA issuer ----
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc(BM, BN);
+            int done = 0;
+            for (int kb = 0; kb < KT; ++kb) {
+                const int s = kb % S, round = kb / S;
+                const bool ok = CONVERT ? mbar_wait(split_bar(s), round & 1, err, ERR_MMA_WAIT)
+                                        : mbar_wait(full_bar(s), round & 1, err, ERR_MMA_WAIT);
+                if (!ok) break;
+                tc_fence_after();
+                const uint64_t ad = kmajor_sw128_desc(sbase + a_off(s));
+                const uint64_t bd = kmajor_sw128_desc(sbase + b_off(s));
+#pragma unroll
+                for (int k = 0; k < BK / UMMA_K; ++k) {
+                    const uint64_t koff = (uint64_t)((k * UMMA_K * 4) >> 4);  // 32 bytes per step
+                    if constexpr (THREE) {
+                        const uint64_t ald = kmajor_sw128_desc(sbase + alo_off(s));
+                        const uint64_t bld = kmajor_sw128_desc(sbase + blo_off(s));
+                        umma_tf32(tmem, ald + koff, bd + koff, idesc, (kb | k) != 0);
+                        umma_tf32(tmem, ad + koff, bld + koff, idesc, 1u);
+                        umma_tf32(tmem, ad + koff, bd + koff, idesc, 1u);
+                    } else {
+                        umma_tf32(tmem, ad + koff, bd + koff, idesc, (kb | k) != 0);
+                    }
+                }
+                umma_commit(empty_bar(s));  // the stage is free once these MMAs have read it
+                ++done;
+            }
+            if (done == KT) {
+                umma_commit(acc_bar);
+            } else {
+                // Give up: make sure nothing issued is still running before teardown.
+                umma_commit(drain_bar);
+                mbar_wait(drain_bar, 0, err, ERR_DRAIN, false);
+            }
+        }
+    } else {
+        // ---- warps 2..5: split / transpose, then the epilogue ----
+        const int t = threadIdx.x - 64;  // 0..127
+        if constexpr (CONVERT) {
+            int transposes = 0;  // uses of read_bar so far (its phase)
+            for (int kb = 0; kb < KT; ++kb) {
+                const int s = kb % S, round = kb / S;
+                if (!mbar_wait(full_bar(s), round & 1, err, ERR_SPLIT_WAIT)) break;
+                bool ok = true;
+                if constexpr (A_K) {
+                    if constexpr (THREE)
+                        split_kmajor(reinterpret_cast<float4 *>(smem + a_off(s)),
+                                     reinterpret_cast<float4 *>(smem + alo_off(s)), t);
+                } else {
+                    ok = transpose_mnmajor<THREE>(smem + a_off(s), smem + alo_off(s), t, read_bar,
+                                                  transposes & 1, err);
+                    ++transposes;
+                }
+                if (!ok) break;
+                if constexpr (B_K) {
+                    if constexpr (THREE)
+                        split_kmajor(reinterpret_cast<float4 *>(smem + b_off(s)),
+                                     reinterpret_cast<float4 *>(smem + blo_off(s)), t);
+                } else {
+                    ok = transpose_mnmajor<THREE>(smem + b_off(s), smem + blo_off(s), t, read_bar,
+                                                  transposes & 1, err);
+                    ++transposes;
+                }
+                if (!ok) break;
+                // Generic-proxy writes must be visible to the tensor core (async proxy).
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(split_bar(s));
+            }
+        }
+        // Epilogue: warp w reads accumulator lanes 32*(w%4) .. +31 (rows of the tile).
+        const int q = warp & 3;
+        const int row = m0 + q * 32 + lane;
+        const bool acc_ok = KT > 0 && mbar_wait(acc_bar, 0, err, ERR_EPILOGUE);
+        if (acc_ok) {
+            tc_fence_after();
+            float *const C = p.C + (long long)bz * p.strideC;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
+                if (row < p.M) {
+                    float *const crow = C + (long long)row * p.ldc;
+#pragma unroll
+                    for (int g = 0; g < 8; ++g) {
+                        const int gc = n0 + c0 + 4 * g;
+                        float v[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) v[e] = p.alpha * __uint_as_float(r[4 * g + e]);
+                        if (p.c_vec && gc + 3 < p.N) {
+                            if (p.beta != 0.0f) {
+                                const float4 c = *reinterpret_cast<const float4 *>(crow + gc);
+                                v[0] = fmaf(p.beta, c.x, v[0]);
+                                v[1] = fmaf(p.beta, c.y, v[1]);
+                                v[2] = fmaf(p.beta, c.z, v[2]);
+                                v[3] = fmaf(p.beta, c.w, v[3]);
+                            }
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if (p.bias) v[e] += __ldg(p.bias + gc + e);
+                                if (p.relu) v[e] = fmaxf(v[e], 0.0f);
+                            }
+                            *reinterpret_cast<float4 *>(crow + gc) = make_float4(v[0], v[1], v[2], v[3]);
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                if (gc + e >= p.N) break;
+                                float o = v[e];
+                                if (p.beta != 0.0f) o = fmaf(p.beta, crow[gc + e], o);
+                                if (p.bias) o += __ldg(p.bias + gc + e);
+                                if (p.relu) o = fmaxf(o, 0.0f);
+                                crow[gc + e] = o;
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    // Teardown: the allocating warp frees the tensor memory once every thread is done.
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                     "r"(TMEM_COLS)
+                     : "memory");
+    }
+}
+
+}  // namespace tc
+}  // namespace fgemm

@@ -49,6 +49,7 @@ typedef enum fgemm_status {
     FGEMM_ERR_INVALID_VALUE = 1, /* an argument breaks the rules above; nothing launched */
     FGEMM_ERR_LAUNCH = 2,        /* the CUDA launch (or a CUDA query before it) failed */
     FGEMM_ERR_NOT_SUPPORTED = 3, /* e.g. no sm_103a device, or a config that cannot run the call */
+    FGEMM_ERR_TIMEOUT = 4,       /* a tensor-core kernel gave up waiting (fgemm_device_status) */
 } fgemm_status;
 
 typedef enum fgemm_op { FGEMM_OP_N = 0, FGEMM_OP_T = 1 } fgemm_op;
@@ -90,6 +91,46 @@ fgemm_status fgemm_sgemm_strided_batched(fgemm_op transa, fgemm_op transb, int M
                                          const float *B, int ldb, long long strideB, float beta,
                                          float *C, int ldc, long long strideC, int batch,
                                          cudaStream_t stream);
+
+/*
+ * Arithmetic of the contraction (GEMM 优化详解, "进一步优化方向": tensor cores are the
+ * next step after the CUDA-core ladder):
+ *   FGEMM_MATH_FP32    FP32 FMA on the CUDA cores (the plain entry points use this).
+ *   FGEMM_MATH_TF32    tcgen05 tensor cores, each operand read as TF32 (10 mantissa
+ *                      bits); error within 2e-3 * sum_k |a_ik||b_kj| per element.
+ *   FGEMM_MATH_3XTF32  tensor cores with each operand split on chip into a TF32 high
+ *                      part and a residual, three products per term (hi*hi, hi*lo,
+ *                      lo*hi): near-FP32 accuracy.
+ */
+typedef enum fgemm_math {
+    FGEMM_MATH_FP32 = 0,
+    FGEMM_MATH_TF32 = 1,
+    FGEMM_MATH_3XTF32 = 2,
+} fgemm_math;
+
+/*
+ * The general call with a choice of arithmetic.  Arguments, conventions and
+ * validation are those of fgemm_gemm_explicit (bias may be NULL; batch = 1 with
+ * zero strides is a single GEMM).  The tensor-core modes take every transpose
+ * combination; they need 16-byte aligned A and B and lda, ldb, strideA, strideB
+ * multiples of 4.  A call they cannot run (unaligned operands, K == 0, alpha == 0)
+ * uses the FP32 CUDA-core kernel instead (at least as accurate).  A tensor-core kernel bounds
+ * every internal wait; if one runs out it stops, leaves C undefined and records it
+ * for fgemm_device_status.
+ */
+fgemm_status fgemm_gemm_math(fgemm_math math, fgemm_op transa, fgemm_op transb, int M, int N,
+                             int K, float alpha, const float *A, int lda, long long strideA,
+                             const float *B, int ldb, long long strideB, float beta, float *C,
+                             int ldc, long long strideC, int batch, const float *bias,
+                             int apply_relu, cudaStream_t stream);
+
+/*
+ * FGEMM_ERR_TIMEOUT if a tensor-core kernel on the current device recorded a wait
+ * that ran out since the word was last cleared, FGEMM_OK if not.  Reads device
+ * memory synchronously: call it after the streams that ran the kernels have
+ * finished.  Nonzero `clear` resets the record.
+ */
+fgemm_status fgemm_device_status(int clear);
 
 /* Static, human-readable text for a status code (never NULL). */
 const char *fgemm_status_string(fgemm_status status);

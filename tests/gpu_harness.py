@@ -45,6 +45,7 @@ class Case:
     config: int = -1
     seed: int = 0
     align_ld: bool = True  # round leading dimensions and batch strides up to 16 bytes
+    math: int = -1  # >= 0: call fgemm_gemm_math with this arithmetic instead of gemm_explicit
     c_nan: bool = False  # fill the initial C with NaN (only meaningful for beta == 0)
     a_nan: bool = False  # fill A with NaN (only meaningful for alpha == 0)
 
@@ -101,10 +102,15 @@ def run(case: Case):
     dB, pB = _device(B, case.offset[1])
     dC, pC = _device(C0, case.offset[2])
     dbias, pbias = _device(bias, 0) if bias is not None else (None, None)
-    fg.gemm_explicit(case.config, case.ta, case.tb, M, N, K, case.alpha, pA, lda, sA, pB, ldb, sB,
-                     case.beta, pC, ldc, sC, nb, pbias, case.relu,
-                     stream=torch.cuda.current_stream().cuda_stream)
+    stream = torch.cuda.current_stream().cuda_stream
+    if case.math >= 0:
+        fg.gemm_math(case.math, case.ta, case.tb, M, N, K, case.alpha, pA, lda, sA, pB, ldb, sB,
+                     case.beta, pC, ldc, sC, nb, pbias, case.relu, stream=stream)
+    else:
+        fg.gemm_explicit(case.config, case.ta, case.tb, M, N, K, case.alpha, pA, lda, sA, pB, ldb,
+                         sB, case.beta, pC, ldc, sC, nb, pbias, case.relu, stream=stream)
     torch.cuda.synchronize()
+    assert fg.device_status() == fg.OK, "a tensor-core wait ran out"
     Cout = dC[case.offset[2]:case.offset[2] + C0.size].cpu().numpy()
 
     got = np.zeros((nb, M, N), np.float32)
@@ -123,7 +129,7 @@ def run(case: Case):
     return got, want, mag, bool(same[untouched].all())
 
 
-def check(case: Case):
+def check(case: Case, rel_tol=REL_TOL):
     got, want, mag, untouched_ok = run(case)
     assert untouched_ok, "the call wrote outside the M x N region of C"
     assert not np.isnan(got).any(), "NaN in the result"
@@ -133,7 +139,8 @@ def check(case: Case):
             bad.sum(), bad.size, np.argwhere(bad)[0], got[bad][0], want[bad][0])
     else:
         err = np.abs(got.astype(np.float64) - want)
-        bound = REL_TOL * mag + FLT_MIN
+        bound = rel_tol * mag + FLT_MIN
         bad = err > bound
-        assert not bad.any(), "outside 1e-5*mag: %d of %d, worst ratio %g" % (
-            bad.sum(), bad.size, (err / bound).max())
+        assert not bad.any(), "outside %g*mag: %d of %d, worst ratio %g" % (
+            rel_tol, bad.sum(), bad.size, (err / bound).max())
+    return float((np.abs(got.astype(np.float64) - want) / (mag + FLT_MIN)).max())

@@ -122,3 +122,15 @@ def test_selector():
                 c = sel(ta, tb, n, n, n, 1, 1, 152)
                 assert 0 <= c < fg.num_configs()
 
+
+
+def test_gemm_math_validates_before_launch():
+    st = fg.gemm_math(fg.MATH_3XTF32, 0, 1, -1, 4, 4, 1.0, FAKE, 4, 0, FAKE, 4, 0, 0.0, FAKE, 4, 0,
+                      1, check=False)
+    assert st == fg.ERR_INVALID_VALUE
+    st = fg.gemm_math(9, 0, 1, 4, 4, 4, 1.0, FAKE, 4, 0, FAKE, 4, 0, 0.0, FAKE, 4, 0, 1,
+                      check=False)
+    assert st == fg.ERR_INVALID_VALUE
+    st = fg.gemm_math(fg.MATH_TF32, 0, 1, 0, 4, 4, 1.0, FAKE, 4, 0, FAKE, 4, 0, 0.0, FAKE, 4, 0, 1,
+                      check=False)
+    assert st == fg.OK
