@@ -354,7 +354,8 @@ def run_fgemm(args, rank, world, local_rank):
         aligned = True
         chosen = fg.select_config(w.ta, w.tb, w.M, w.N, w.K, max(1, w.batch), aligned, sms)
     kernel_name = fg.config_name(chosen)
-    tensor_path = args.math != "fp32" and w.ta == 0 and w.tb == 1
+    # The tensor-core kernels take every layout of these (16-byte aligned) workloads.
+    tensor_path = args.math != "fp32"
     if tensor_path:
         kernel_name = "tcgen05_%s_128x128" % args.math
     line = {
