@@ -26,7 +26,6 @@ and ``value`` counts the work of all ranks.
 from __future__ import annotations
 
 import argparse
-import glob
 import hashlib
 import json
 import os
@@ -78,14 +77,21 @@ def parse_args(argv=None):
     return ap.parse_args(argv)
 
 
-def kernel_source_hash() -> str:
-    """Short hash of the CUDA sources; profile summaries record the hash they measured."""
+KERNEL_SOURCES = {
+    "simt": ("simt_gemm.cuh", "simt_launch.cuh", "inst_nn.cu", "inst_nt.cu", "inst_tn.cu",
+             "inst_tt.cu"),
+    "tcgen05": ("tc_gemm.cuh", "tc_gemm.cu"),
+}
+
+
+def kernel_source_hash(family: str) -> str:
+    """Short hash of one kernel family's CUDA sources; profile summaries record the
+    hash of the sources they measured."""
     m = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "dense_fp32_gemm_sm_gb300", "csrc", "*"))):
-        if f.endswith((".cu", ".cuh", ".h")):
-            m.update(os.path.basename(f).encode())
-            with open(f, "rb") as fh:
-                m.update(fh.read())
+    for name in KERNEL_SOURCES[family]:
+        m.update(name.encode())
+        with open(os.path.join(ROOT, "dense_fp32_gemm_sm_gb300", "csrc", name), "rb") as fh:
+            m.update(fh.read())
     return m.hexdigest()[:16]
 
 
@@ -100,7 +106,11 @@ def recorded_traffic(config_name: str, workload: str):
             key, sep, val = line.strip().partition(":")
             if sep and key in ("source_sha256", "traffic_bytes_per_launch"):
                 fields[key] = val.strip()
-    if fields.get("source_sha256") != kernel_source_hash() or "traffic_bytes_per_launch" not in fields:
+    family = config_name.split("_")[0]
+    if family not in KERNEL_SOURCES:
+        return None
+    if (fields.get("source_sha256") != kernel_source_hash(family)
+            or "traffic_bytes_per_launch" not in fields):
         return None
     return int(fields["traffic_bytes_per_launch"])
 
