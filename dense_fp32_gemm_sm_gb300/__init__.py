@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     OP_T,
     FgemmError,
     config_name,
+    debug_withhold_tensor_core,
     device_status,
     gemm_math,
     gemm_explicit,

@@ -65,6 +65,8 @@ def library() -> ctypes.CDLL:
                 fn = getattr(lib, name)
                 fn.argtypes = argtypes
                 fn.restype = _c_int
+            lib.fgemm_debug_withhold_tensor_core.argtypes = [_c_int, _c_ll]
+            lib.fgemm_debug_withhold_tensor_core.restype = None
             lib.fgemm_config_name.restype = ctypes.c_char_p
             lib.fgemm_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -178,3 +180,8 @@ def gemm_math(math, transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, str
 def device_status(clear=True) -> int:
     """``fgemm_device_status``: ERR_TIMEOUT if a tensor-core wait ran out (call after a sync)."""
     return library().fgemm_device_status(1 if clear else 0)
+
+
+def debug_withhold_tensor_core(k_block: int, wait_limit_ns: int = 0) -> None:
+    """Testing: ``fgemm_debug_withhold_tensor_core`` (k_block < 0 restores normal runs)."""
+    library().fgemm_debug_withhold_tensor_core(int(k_block), int(wait_limit_ns))

@@ -267,6 +267,11 @@ fgemm_status fgemm_gemm_math(fgemm_math math, fgemm_op transa, fgemm_op transb, 
 
 fgemm_status fgemm_device_status(int clear) { return fgemm::tc_device_status(clear); }
 
+void fgemm_debug_withhold_tensor_core(int k_block, long long wait_limit_ns)
+{
+    fgemm::tc_debug_withhold(k_block, wait_limit_ns);
+}
+
 const char *fgemm_status_string(fgemm_status status)
 {
     switch (status) {

@@ -60,6 +60,8 @@ fgemm_status launch_tc(int mode, const TcProblem &q, cudaStream_t stream);
 // FGEMM_ERR_TIMEOUT if a tensor-core kernel on the current device recorded a wait
 // that ran out (cleared when `clear`), FGEMM_OK otherwise.
 fgemm_status tc_device_status(int clear);
+// Testing: withhold one k-block in later tensor-core launches (k_block < 0: normal).
+void tc_debug_withhold(int k_block, long long wait_limit_ns);
 
 // Launch tables, one per transpose combination (defined in inst_<ta><tb>.cu).
 extern const LaunchFn kLaunchNN[NUM_CONFIGS];

@@ -19,6 +19,11 @@ __device__ unsigned g_tc_error;
 
 namespace {
 
+// Testing hook (fgemm_debug_withhold_tensor_core): k-block the producer withholds,
+// and the wait bound to use meanwhile.
+std::atomic<int> g_withhold_kb{-1};
+std::atomic<unsigned long long> g_wait_limit_ns{tc::kWaitLimitNs};
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 {
     static std::atomic<void *> fn{nullptr};
@@ -152,6 +157,8 @@ fgemm_status launch_tc(int mode, const TcProblem &q, cudaStream_t stream)
                   : 0;
     p.tiles_m = (q.M + tc::BM - 1) / tc::BM;
     p.tiles_n = (q.N + tc::BN - 1) / tc::BN;
+    p.withhold_kb = g_withhold_kb.load(std::memory_order_relaxed);
+    p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     const int layout = q.ta * 2 + q.tb;  // 0: NN, 1: NT, 2: TN, 3: TT
     if (mode == tc::MODE_3XTF32) {
         switch (layout) {
@@ -166,6 +173,18 @@ fgemm_status launch_tc(int mode, const TcProblem &q, cudaStream_t stream)
     case 1: return launch_tc_mode<tc::MODE_TF32, 0, 1>(p, q.batch, stream);
     case 2: return launch_tc_mode<tc::MODE_TF32, 1, 0>(p, q.batch, stream);
     default: return launch_tc_mode<tc::MODE_TF32, 1, 1>(p, q.batch, stream);
+    }
+}
+
+void tc_debug_withhold(int k_block, long long wait_limit_ns)
+{
+    if (k_block < 0) {
+        g_withhold_kb.store(-1);
+        g_wait_limit_ns.store(tc::kWaitLimitNs);
+    } else {
+        g_withhold_kb.store(k_block);
+        g_wait_limit_ns.store(wait_limit_ns > 0 ? (unsigned long long)wait_limit_ns
+                                                : tc::kWaitLimitNs);
     }
 }
 

@@ -46,7 +46,7 @@ constexpr int TILE_A_BYTES = BM * BK * 4;   // 16 KB
 constexpr int TILE_B_BYTES = BN * BK * 4;   // 16 KB
 constexpr int THREADS = 192;
 constexpr uint32_t TMEM_COLS = BN;          // FP32 accumulator: 128 lanes x BN columns
-constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // 4 s per wait
+constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // default: 4 s per wait
 
 // Error bits recorded in the device error word.
 constexpr unsigned ERR_PRODUCER = 1u, ERR_MMA_WAIT = 2u, ERR_SPLIT_WAIT = 4u, ERR_EPILOGUE = 8u,
@@ -80,6 +80,8 @@ struct TcParams {
     int c_vec;
     int tiles_m, tiles_n;
     int batch0;  // first problem of this launch (the launch covers gridDim.z problems)
+    unsigned long long wait_limit_ns;  // bound of every mbarrier wait
+    int withhold_kb;  // testing: the producer never issues this k-block (-1: none)
 };
 
 // ---- PTX wrappers ----------------------------------------------------------------
@@ -128,11 +130,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 }
 
 // Wait until the phase with the given parity has completed, for at most
-// kWaitLimitNs.  With `give_up_on_error`, stop early once any CTA has recorded an
+// limit_ns.  With `give_up_on_error`, stop early once any CTA has recorded an
 // error (drain waits must not: they guard copies still landing in shared memory).
 // On expiry, record `code` and return false.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned *err,
-                                          unsigned code, bool give_up_on_error = true)
+                                          unsigned code, unsigned long long limit_ns,
+                                          bool give_up_on_error = true)
 {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer();
@@ -140,7 +143,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigne
         if (mbar_try_wait(bar, parity)) return true;
         if ((spin & 255u) == 0) {
             if (give_up_on_error && *(volatile unsigned *)err != 0u) return false;
-            if (global_timer() - t0 > kWaitLimitNs) {
+            if (global_timer() - t0 > limit_ns) {
                 atomicOr(err, code);
                 return false;
             }
@@ -252,7 +255,8 @@ __device__ __forceinline__ int kmajor_offset(int r, int kq)
 // 16-byte chunks, conflict-free per quarter warp), and the lo parts for 3xTF32.
 template <bool SPLIT>
 __device__ __forceinline__ bool transpose_mnmajor(uint8_t *tile, uint8_t *lo, int t, uint32_t read_done,
-                                                  uint32_t parity, unsigned *err)
+                                                  uint32_t parity, unsigned *err,
+                                                  unsigned long long limit_ns)
 {
     const int lane = t & 31, wq = t >> 5;
     const float *src = reinterpret_cast<const float *>(tile);
@@ -266,7 +270,7 @@ __device__ __forceinline__ bool transpose_mnmajor(uint8_t *tile, uint8_t *lo, in
             for (int e = 0; e < 4; ++e) v[2 * j + i][e] = src[(4 * kq + e) * 128 + r];
         }
     mbar_arrive(read_done);
-    if (!mbar_wait(read_done, parity, err, ERR_SPLIT_WAIT)) return false;
+    if (!mbar_wait(read_done, parity, err, ERR_SPLIT_WAIT, limit_ns)) return false;
 #pragma unroll
     for (int j = 0; j < 4; ++j)
 #pragma unroll
@@ -326,6 +330,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int m0 = tm * BM, n0 = tn * BN;
     const int bz = p.batch0 + blockIdx.z;
     const int KT = (p.K + BK - 1) / BK;
+    const unsigned long long lim = p.wait_limit_ns;
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < S; ++s) {
@@ -357,7 +362,9 @@ __global__ void __launch_bounds__(THREADS, 1)
             int issued = 0;
             for (int kb = 0; kb < KT; ++kb) {
                 const int s = kb % S, round = kb / S;
-                if (round > 0 && !mbar_wait(empty_bar(s), (round - 1) & 1, err, ERR_PRODUCER)) break;
+                if (round > 0 && !mbar_wait(empty_bar(s), (round - 1) & 1, err, ERR_PRODUCER, lim))
+                    break;
+                if (kb == p.withhold_kb) break;  // testing: as if this copy never arrived
                 mbar_arrive_expect_tx(full_bar(s), TILE_A_BYTES + TILE_B_BYTES);
                 if constexpr (A_K)
                     tma_load_3d(sbase + a_off(s), &p.tmA, full_bar(s), kb * BK, m0, bz);
@@ -371,7 +378,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             // Never leave with copies in flight into this CTA's shared memory.
             for (int kb = issued - S < 0 ? 0 : issued - S; kb < issued; ++kb)
-                mbar_wait(full_bar(kb % S), (kb / S) & 1, err, ERR_DRAIN, false);
+                mbar_wait(full_bar(kb % S), (kb / S) & 1, err, ERR_DRAIN, lim, false);
         }
     } else if (warp == 1) {
         // ---- MMA issuer ----
@@ -380,8 +387,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             int done = 0;
             for (int kb = 0; kb < KT; ++kb) {
                 const int s = kb % S, round = kb / S;
-                const bool ok = CONVERT ? mbar_wait(split_bar(s), round & 1, err, ERR_MMA_WAIT)
-                                        : mbar_wait(full_bar(s), round & 1, err, ERR_MMA_WAIT);
+                const bool ok = CONVERT ? mbar_wait(split_bar(s), round & 1, err, ERR_MMA_WAIT, lim)
+                                        : mbar_wait(full_bar(s), round & 1, err, ERR_MMA_WAIT, lim);
                 if (!ok) break;
                 tc_fence_after();
                 const uint64_t ad = kmajor_sw128_desc(sbase + a_off(s));
@@ -407,7 +414,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             } else {
                 // Give up: make sure nothing issued is still running before teardown.
                 umma_commit(drain_bar);
-                mbar_wait(drain_bar, 0, err, ERR_DRAIN, false);
+                mbar_wait(drain_bar, 0, err, ERR_DRAIN, lim, false);
             }
         }
     } else {
@@ -417,7 +424,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             int transposes = 0;  // uses of read_bar so far (its phase)
             for (int kb = 0; kb < KT; ++kb) {
                 const int s = kb % S, round = kb / S;
-                if (!mbar_wait(full_bar(s), round & 1, err, ERR_SPLIT_WAIT)) break;
+                if (!mbar_wait(full_bar(s), round & 1, err, ERR_SPLIT_WAIT, lim)) break;
                 bool ok = true;
                 if constexpr (A_K) {
                     if constexpr (THREE)
@@ -425,7 +432,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                      reinterpret_cast<float4 *>(smem + alo_off(s)), t);
                 } else {
                     ok = transpose_mnmajor<THREE>(smem + a_off(s), smem + alo_off(s), t, read_bar,
-                                                  transposes & 1, err);
+                                                  transposes & 1, err, lim);
                     ++transposes;
                 }
                 if (!ok) break;
@@ -435,7 +442,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                      reinterpret_cast<float4 *>(smem + blo_off(s)), t);
                 } else {
                     ok = transpose_mnmajor<THREE>(smem + b_off(s), smem + blo_off(s), t, read_bar,
-                                                  transposes & 1, err);
+                                                  transposes & 1, err, lim);
                     ++transposes;
                 }
                 if (!ok) break;
@@ -447,7 +454,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         // Epilogue: warp w reads accumulator lanes 32*(w%4) .. +31 (rows of the tile).
         const int q = warp & 3;
         const int row = m0 + q * 32 + lane;
-        const bool acc_ok = KT > 0 && mbar_wait(acc_bar, 0, err, ERR_EPILOGUE);
+        const bool acc_ok = KT > 0 && mbar_wait(acc_bar, 0, err, ERR_EPILOGUE, lim);
         if (acc_ok) {
             tc_fence_after();
             float *const C = p.C + (long long)bz * p.strideC;

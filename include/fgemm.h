@@ -132,6 +132,17 @@ fgemm_status fgemm_gemm_math(fgemm_math math, fgemm_op transa, fgemm_op transb, 
  */
 fgemm_status fgemm_device_status(int clear);
 
+/*
+ * Testing only (failure detection without a GPU fault).  Makes later tensor-core
+ * launches of this process behave as if the copy of k-block `k_block` never arrived:
+ * the producer withholds it, the kernel's bounded wait runs out after
+ * `wait_limit_ns` (<= 0: the default 4 s), the kernel drains its own copies and
+ * MMAs, frees its tensor memory, records FGEMM_ERR_TIMEOUT for fgemm_device_status
+ * and returns with C undefined; the CUDA context stays usable.  k_block < 0 restores
+ * normal operation.  Not thread-safe with concurrent tensor-core calls.
+ */
+void fgemm_debug_withhold_tensor_core(int k_block, long long wait_limit_ns);
+
 /* Static, human-readable text for a status code (never NULL). */
 const char *fgemm_status_string(fgemm_status status);
 
