@@ -72,6 +72,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--math", choices=("fp32", "tf32", "3xtf32"), default="fp32",
                     help="arithmetic: FP32 CUDA cores (the metric) or the tcgen05 tensor-core path")
+    ap.add_argument("--splitk", type=int, default=0,
+                    help="S > 1: split-K GEMM into S slices with a workspace (single problems)")
     ap.add_argument("--epilogue", choices=("workload", "none"), default="workload",
                     help="'none' drops the workload's bias/ReLU (plain sgemm at the same shape)")
     return ap.parse_args(argv)
@@ -231,13 +233,17 @@ def stated_peak_tflops(device) -> tuple:
 MATHS = {"fp32": 0, "tf32": 1, "3xtf32": 2}
 
 
-def _launch(fg, w, cfg, dA, dB, dC, dbias, stream, math="fp32"):
+def _launch(fg, w, cfg, dA, dB, dC, dbias, stream, math="fp32", splitk=None):
     """One step: the library call of the workload (the bench's unit of work)."""
     nb = max(1, w.batch)
     sA = w.M * w.K if w.batch else 0
     sB = w.N * w.K if w.batch else 0
     sC = w.M * w.N if w.batch else 0
-    if math != "fp32":
+    if splitk is not None:
+        splits, ws, need = splitk
+        fg.sgemm_splitk(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, dB, w.ldb, w.beta, dC,
+                        w.ldc, dbias, w.relu, splits, ws, need, stream=stream)
+    elif math != "fp32":
         fg.gemm_math(MATHS[math], w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, sA, dB, w.ldb, sB,
                      w.beta, dC, w.ldc, sC, nb, dbias, w.relu, stream=stream)
     elif cfg >= 0:
@@ -298,12 +304,18 @@ def run_fgemm(args, rank, world, local_rank):
     dC = torch.zeros(c_shape, device=dev)
     dC0 = w.C0.to(dev) if w.C0 is not None else None
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    splitk = None
+    if args.splitk > 1:
+        if w.batch:
+            raise SystemExit("bench.py: --splitk takes single problems")
+        need = fg.splitk_workspace_size(w.M, w.N, w.K, args.splitk)
+        splitk = (args.splitk, torch.empty(need // 4, device=dev), need)
     torch.cuda.synchronize()
 
     def step():
         if dC0 is not None:  # beta != 0: restore C so every step computes the same thing
             dC.copy_(dC0)
-        _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math)
+        _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math, splitk)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -313,6 +325,9 @@ def run_fgemm(args, rank, world, local_rank):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     n_batch_launches = (max(1, w.batch) + 65534) // 65535
+    if splitk is not None:  # partial GEMMs (one or two launches) + the reduction
+        Ks = -(-(-(-w.K // args.splitk)) // 32) * 32
+        n_batch_launches = (1 if w.K % Ks == 0 else 2) + 1
     sampler = ClockSampler(local_rank, enabled=not args.no_clocks)
     barrier(world)
     torch.cuda.synchronize()
@@ -323,7 +338,7 @@ def run_fgemm(args, rank, world, local_rank):
             if dC0 is not None:
                 dC.copy_(dC0)
             starts[i].record(stream)
-            _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math)
+            _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math, splitk)
             ends[i].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
@@ -352,7 +367,7 @@ def run_fgemm(args, rank, world, local_rank):
             dB.copy_(hB, non_blocking=True)
             if hC0 is not None:
                 dC.copy_(hC0, non_blocking=True)
-            _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math)
+            _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math, splitk)
             hC.copy_(dC, non_blocking=True)
         e_end.record(stream)
     torch.cuda.synchronize()
@@ -364,6 +379,8 @@ def run_fgemm(args, rank, world, local_rank):
         aligned = True
         chosen = fg.select_config(w.ta, w.tb, w.M, w.N, w.K, max(1, w.batch), aligned, sms)
     kernel_name = fg.config_name(chosen)
+    if splitk is not None:
+        kernel_name = "%s_splitk%d" % (kernel_name, args.splitk)
     # The tensor-core kernels take every layout of these (16-byte aligned) workloads.
     tensor_path = args.math != "fp32"
     if tensor_path:

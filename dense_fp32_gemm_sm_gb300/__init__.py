@@ -27,6 +27,8 @@ from ._binding import (  # noqa: F401
     select_config,
     sgemm,
     sgemm_bias_relu,
+    sgemm_splitk,
+    splitk_workspace_size,
     sgemm_strided_batched,
     status_string,
 )

@@ -65,6 +65,13 @@ def library() -> ctypes.CDLL:
                 fn = getattr(lib, name)
                 fn.argtypes = argtypes
                 fn.restype = _c_int
+            lib.fgemm_sgemm_splitk.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                               _c_vp, _c_int, _c_vp, _c_int, _c_float, _c_vp,
+                                               _c_int, _c_vp, _c_int, _c_int, _c_vp,
+                                               ctypes.c_size_t, _c_vp]
+            lib.fgemm_sgemm_splitk.restype = _c_int
+            lib.fgemm_splitk_workspace_size.argtypes = [_c_int, _c_int, _c_int, _c_int]
+            lib.fgemm_splitk_workspace_size.restype = ctypes.c_size_t
             lib.fgemm_debug_withhold_tensor_core.argtypes = [_c_int, _c_ll]
             lib.fgemm_debug_withhold_tensor_core.restype = None
             lib.fgemm_config_name.restype = ctypes.c_char_p
@@ -185,3 +192,20 @@ def device_status(clear=True) -> int:
 def debug_withhold_tensor_core(k_block: int, wait_limit_ns: int = 0) -> None:
     """Testing: ``fgemm_debug_withhold_tensor_core`` (k_block < 0 restores normal runs)."""
     library().fgemm_debug_withhold_tensor_core(int(k_block), int(wait_limit_ns))
+
+
+def splitk_workspace_size(M, N, K, splits) -> int:
+    """``fgemm_splitk_workspace_size``: bytes of workspace fgemm_sgemm_splitk needs (0: invalid)."""
+    return int(library().fgemm_splitk_workspace_size(M, N, K, splits))
+
+
+def sgemm_splitk(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias, apply_relu,
+                 splits, workspace, workspace_bytes, stream=None, check=True) -> int:
+    """``fgemm_sgemm_splitk``: split-K GEMM with a caller-owned workspace."""
+    st = library().fgemm_sgemm_splitk(
+        int(transa), int(transb), M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C), ldc,
+        _ptr(bias), 1 if apply_relu else 0, int(splits), _ptr(workspace), int(workspace_bytes),
+        _stream(stream, C, A, B))
+    if check:
+        _check(st, "fgemm_sgemm_splitk")
+    return st

@@ -180,6 +180,65 @@ using fgemm::run;
 namespace fgemm {
 namespace {
 
+// Split-K: the K range is cut into slices of Ks (a multiple of 32) and slice s,
+// covering k in [s*Ks, min(K, (s+1)*Ks)), is an independent GEMM whose unscaled
+// product lands in workspace slice s (M x N, leading dimension N).  Slices of equal
+// length run as one strided batch of the CUDA-core kernel, the shorter last slice as
+// a second launch; a reduction kernel then sums the slices in order and applies the
+// epilogue.  Nothing is atomic: the result is the same on every run.
+long long splitk_slice(long long K, int splits)
+{
+    long long ks = (K + splits - 1) / splits;
+    return (ks + 31) / 32 * 32;
+}
+
+fgemm_status run_splitk(const Problem &p, int splits, float *W, size_t ws_bytes)
+{
+    bool noop = false;
+    fgemm_status st = validate(p, &noop);
+    if (st != FGEMM_OK || noop) return st;
+    if (p.batch != 1 || splits < 1 || splits > 64) return FGEMM_ERR_INVALID_VALUE;
+    const bool products = p.K > 0 && p.alpha != 0.0f;
+    if (splits == 1 || !products) return run(-1, p);
+    const long long Ks = splitk_slice(p.K, splits);
+    const int S = (int)((p.K + Ks - 1) / Ks);  // slices actually used
+    const long long slice = (long long)p.M * p.N;
+    if (W == nullptr || ws_bytes < (size_t)S * (size_t)slice * sizeof(float))
+        return FGEMM_ERR_INVALID_VALUE;
+    // Offsets of one K slice in A and B.
+    const long long dA = p.ta ? Ks * p.lda : Ks;
+    const long long dB = p.tb ? Ks : Ks * p.ldb;
+    const long long Klast = p.K - (long long)(S - 1) * Ks;
+    Problem q = p;
+    q.alpha = 1.0f;
+    q.beta = 0.0f;
+    q.bias = nullptr;
+    q.relu = 0;
+    q.C = W;
+    q.ldc = p.N;
+    q.sC = slice;
+    q.sA = dA;
+    q.sB = dB;
+    const int full = Klast == Ks ? S : S - 1;
+    if (full > 0) {
+        q.K = (int)Ks;
+        q.batch = full;
+        st = run(-1, q);
+        if (st != FGEMM_OK) return st;
+    }
+    if (full < S) {
+        q.K = (int)Klast;
+        q.batch = 1;
+        q.A = p.A + (long long)(S - 1) * dA;
+        q.B = p.B + (long long)(S - 1) * dB;
+        q.C = W + (long long)(S - 1) * slice;
+        st = run(-1, q);
+        if (st != FGEMM_OK) return st;
+    }
+    return launch_splitk_reduce(W, S, p.C, p.ldc, p.M, p.N, p.alpha, p.beta, p.bias, p.relu,
+                                p.stream);
+}
+
 fgemm_status run_math(fgemm_math math, const Problem &p)
 {
     if (math == FGEMM_MATH_FP32) return run(-1, p);
@@ -266,6 +325,25 @@ fgemm_status fgemm_gemm_math(fgemm_math math, fgemm_op transa, fgemm_op transb, 
 }
 
 fgemm_status fgemm_device_status(int clear) { return fgemm::tc_device_status(clear); }
+
+size_t fgemm_splitk_workspace_size(int M, int N, int K, int splits)
+{
+    if (M < 0 || N < 0 || K < 0 || splits < 1 || splits > 64) return 0;
+    if (K == 0) return 0;
+    const long long Ks = fgemm::splitk_slice(K, splits);
+    const long long S = (K + Ks - 1) / Ks;
+    return (size_t)S * (size_t)M * (size_t)N * sizeof(float);
+}
+
+fgemm_status fgemm_sgemm_splitk(fgemm_op transa, fgemm_op transb, int M, int N, int K, float alpha,
+                                const float *A, int lda, const float *B, int ldb, float beta,
+                                float *C, int ldc, const float *bias, int apply_relu, int splits,
+                                float *workspace, size_t workspace_bytes, cudaStream_t stream)
+{
+    return fgemm::run_splitk(make_problem(transa, transb, M, N, K, alpha, A, lda, 0, B, ldb, 0,
+                                          beta, C, ldc, 0, 1, bias, apply_relu, stream),
+                             splits, workspace, workspace_bytes);
+}
 
 void fgemm_debug_withhold_tensor_core(int k_block, long long wait_limit_ns)
 {

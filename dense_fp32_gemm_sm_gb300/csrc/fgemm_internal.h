@@ -63,6 +63,11 @@ fgemm_status tc_device_status(int clear);
 // Testing: withhold one k-block in later tensor-core launches (k_block < 0: normal).
 void tc_debug_withhold(int k_block, long long wait_limit_ns);
 
+// C = act(alpha * sum_s W[s] + beta * C + bias), W: S slices of M x N (ld N).
+fgemm_status launch_splitk_reduce(const float *W, int S, float *C, long long ldc, int M, int N,
+                                  float alpha, float beta, const float *bias, int relu,
+                                  cudaStream_t stream);
+
 // Launch tables, one per transpose combination (defined in inst_<ta><tb>.cu).
 extern const LaunchFn kLaunchNN[NUM_CONFIGS];
 extern const LaunchFn kLaunchNT[NUM_CONFIGS];

@@ -80,10 +80,11 @@ class Workload:
         return 2.0 * self.M * self.N * self.K * max(1, self.batch)
 
 
-# The five workloads, smallest first.  Sizes and value distributions follow the
-# pages' shapes: square 256/1024/4096 problems, a fully-connected layer
-# Y = ReLU(X W + b) and batched attention scores S = Q K^T.
-WORKLOADS = ("square256", "square1024", "square4096", "fc8192x4096x11008", "qkt128x2048x128")
+# The workloads, smallest first.  Sizes and value distributions follow the pages'
+# shapes: square 256/1024/4096 problems, a fully-connected layer Y = ReLU(X W + b),
+# batched attention scores S = Q K^T, and the second attention GEMM O = P V.
+WORKLOADS = ("square256", "square1024", "square4096", "fc8192x4096x11008", "qkt128x2048x128",
+             "pv128x2048x2048x128")
 
 
 def make(name: str) -> Workload:
@@ -117,4 +118,12 @@ def make(name: str) -> Workload:
         # alpha = 1/sqrt(128), computed in double and rounded once to float32.
         alpha = float(torch.tensor(1.0 / math.sqrt(D), dtype=torch.float32))
         return Workload(name, S, S, D, alpha, 0.0, ta=0, tb=1, batch=batch, seed=4, A=Q, B=Kt)
+    if name == "pv128x2048x2048x128":
+        # O = P V per (sequence, head): P 2048 x 2048 attention weights, uniform[0, 1) /
+        # 2048 (rows of nonnegative weights summing to about 1/2), V 2048 x 128 ~ N(0, 1).
+        g = generator(5)
+        batch, S, D = 128, 2048, 128
+        P = uniform(g, (batch, S, S), 0.0, 1.0 / S)
+        V = normal(g, (batch, S, D))
+        return Workload(name, S, D, S, 1.0, 0.0, ta=0, tb=0, batch=batch, seed=5, A=P, B=V)
     raise KeyError("unknown workload %r (known: %s)" % (name, ", ".join(WORKLOADS)))

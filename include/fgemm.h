@@ -39,6 +39,7 @@
 #define FGEMM_H
 
 #include <cuda_runtime_api.h>
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -91,6 +92,29 @@ fgemm_status fgemm_sgemm_strided_batched(fgemm_op transa, fgemm_op transb, int M
                                          const float *B, int ldb, long long strideB, float beta,
                                          float *C, int ldc, long long strideC, int batch,
                                          cudaStream_t stream);
+
+/*
+ * Split-K GEMM for problems with few output tiles and a long K (small squares,
+ * skinny outputs): the small-matrix strategy of GEMM 优化详解, "矩阵大小选择策略",
+ * where one tile per SM would leave most of the GPU idle.  The K range is cut into
+ * `splits` slices (each a multiple of 32 deep); every slice's partial product is
+ * written to `workspace` by the CUDA-core kernel, then one reduction kernel sums the
+ * slices in a fixed order and applies the epilogue:
+ *     C = act( alpha * sum_s P_s + beta * C + bias[col] )    (bias may be NULL)
+ * The sum order is fixed, so results are the same on every run (they may differ in
+ * the last bits from fgemm_sgemm, whose sum order differs).
+ * workspace: caller-owned device memory of at least fgemm_splitk_workspace_size()
+ * bytes, 16-byte aligned, not overlapping A, B, C or bias; its contents are
+ * overwritten.  splits in [1, 64] (1 = fgemm_sgemm_bias_relu); a single problem
+ * (no batch).  Other rules as for fgemm_sgemm_bias_relu; a missing or too small
+ * workspace returns FGEMM_ERR_INVALID_VALUE before anything is launched.
+ */
+size_t fgemm_splitk_workspace_size(int M, int N, int K, int splits);
+
+fgemm_status fgemm_sgemm_splitk(fgemm_op transa, fgemm_op transb, int M, int N, int K, float alpha,
+                                const float *A, int lda, const float *B, int ldb, float beta,
+                                float *C, int ldc, const float *bias, int apply_relu, int splits,
+                                float *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * Arithmetic of the contraction (GEMM 优化详解, "进一步优化方向": tensor cores are the

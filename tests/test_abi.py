@@ -134,3 +134,26 @@ def test_gemm_math_validates_before_launch():
     st = fg.gemm_math(fg.MATH_TF32, 0, 1, 0, 4, 4, 1.0, FAKE, 4, 0, FAKE, 4, 0, 0.0, FAKE, 4, 0, 1,
                       check=False)
     assert st == fg.OK
+
+
+def test_splitk_workspace_size():
+    assert fg.splitk_workspace_size(4, 8, 100, 1) == 4 * 8 * 4
+    # K = 100 in 4 slices -> slices of 32: ceil(100/32) = 4 slices
+    assert fg.splitk_workspace_size(4, 8, 100, 4) == 4 * 4 * 8 * 4
+    # K = 64 in 4 slices -> slices of 32: only 2 slices are used
+    assert fg.splitk_workspace_size(4, 8, 64, 4) == 2 * 4 * 8 * 4
+    assert fg.splitk_workspace_size(4, 8, 0, 4) == 0
+    assert fg.splitk_workspace_size(-1, 8, 64, 4) == 0
+    assert fg.splitk_workspace_size(4, 8, 64, 0) == 0
+    assert fg.splitk_workspace_size(4, 8, 64, 65) == 0
+
+
+def test_splitk_rejects_missing_workspace_before_launch():
+    args = (0, 0, 64, 64, 256, 1.0, FAKE, 256, FAKE, 64, 0.0, FAKE, 64, None, 0)
+    assert fg.sgemm_splitk(*args, 4, None, 0, check=False) == fg.ERR_INVALID_VALUE
+    need = fg.splitk_workspace_size(64, 64, 256, 4)
+    assert fg.sgemm_splitk(*args, 4, FAKE, need - 4, check=False) == fg.ERR_INVALID_VALUE
+    assert fg.sgemm_splitk(*args, 0, FAKE, need, check=False) == fg.ERR_INVALID_VALUE
+    assert fg.sgemm_splitk(*args, 65, FAKE, need, check=False) == fg.ERR_INVALID_VALUE
+    bad_ld = (0, 0, 64, 64, 256, 1.0, FAKE, 255, FAKE, 64, 0.0, FAKE, 64, None, 0)
+    assert fg.sgemm_splitk(*bad_ld, 4, FAKE, need, check=False) == fg.ERR_INVALID_VALUE

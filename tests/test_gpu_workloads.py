@@ -64,14 +64,15 @@ def test_single_workload_sampled(name):
         assert (C[rows] == 0).any() and (C[rows] > 0).any()
 
 
-def test_batched_qkt_sampled():
+@pytest.mark.parametrize("name", ["qkt128x2048x128", "pv128x2048x2048x128"])
+def test_batched_attention_sampled(name):
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
-    w = workloads.make("qkt128x2048x128")
+    w = workloads.make(name)
     C = run_workload(w)
-    Q, Kt = w.A.numpy(), w.B.numpy()
+    A, B = w.A.numpy(), w.B.numpy()
     for b in (0, 1, 63, 127):
         rows = sample_rows(w.M, 24, seed=b)
-        want, mag = oracle.gemm(w.ta, w.tb, w.M, w.N, w.K, w.alpha, Q[b].reshape(-1), w.lda,
-                                Kt[b].reshape(-1), w.ldb, rows=rows)
+        want, mag = oracle.gemm(w.ta, w.tb, w.M, w.N, w.K, w.alpha, A[b].reshape(-1), w.lda,
+                                B[b].reshape(-1), w.ldb, rows=rows)
         compare(C[b][rows], want, mag)
