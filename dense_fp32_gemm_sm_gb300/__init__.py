@@ -27,7 +27,9 @@ from ._binding import (  # noqa: F401
     select_config,
     sgemm,
     sgemm_bias_relu,
+    NOALLOC_SCRATCH_BYTES,
     sgemm_splitk,
+    sgemm_splitk_noalloc,
     splitk_workspace_size,
     sgemm_strided_batched,
     status_string,

@@ -70,6 +70,11 @@ def library() -> ctypes.CDLL:
                                                _c_int, _c_vp, _c_int, _c_int, _c_vp,
                                                ctypes.c_size_t, _c_vp]
             lib.fgemm_sgemm_splitk.restype = _c_int
+            lib.fgemm_sgemm_splitk_noalloc.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int,
+                                                       _c_float, _c_vp, _c_int, _c_vp, _c_int,
+                                                       _c_float, _c_vp, _c_int, _c_vp, _c_int,
+                                                       _c_int, _c_vp]
+            lib.fgemm_sgemm_splitk_noalloc.restype = _c_int
             lib.fgemm_splitk_workspace_size.argtypes = [_c_int, _c_int, _c_int, _c_int]
             lib.fgemm_splitk_workspace_size.restype = ctypes.c_size_t
             lib.fgemm_debug_withhold_tensor_core.argtypes = [_c_int, _c_ll]
@@ -208,4 +213,22 @@ def sgemm_splitk(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, b
         _stream(stream, C, A, B))
     if check:
         _check(st, "fgemm_sgemm_splitk")
+    return st
+
+
+# FGEMM_NOALLOC_SCRATCH_BYTES of include/fgemm.h: the fixed scratch array behind
+# fgemm_sgemm_splitk_noalloc.
+NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
+
+
+def sgemm_splitk_noalloc(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, bias,
+                         apply_relu, splits, stream=None, check=True) -> int:
+    """``fgemm_sgemm_splitk_noalloc``: split-K GEMM whose partial products live in the
+    library's fixed device array instead of a caller workspace (for callers that may
+    not allocate device memory)."""
+    st = library().fgemm_sgemm_splitk_noalloc(
+        int(transa), int(transb), M, N, K, alpha, _ptr(A), lda, _ptr(B), ldb, beta, _ptr(C), ldc,
+        _ptr(bias), 1 if apply_relu else 0, int(splits), _stream(stream, C, A, B))
+    if check:
+        _check(st, "fgemm_sgemm_splitk_noalloc")
     return st

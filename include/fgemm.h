@@ -117,6 +117,35 @@ fgemm_status fgemm_sgemm_splitk(fgemm_op transa, fgemm_op transb, int M, int N, 
                                 float *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Split-K without any device allocation, for callers that are not allowed to call
+ * cudaMalloc (a plugin inside a program that owns all GPU memory through its own
+ * pool, a latency-critical loop that cannot afford cudaMalloc's synchronisation and
+ * cost, a process with a fixed memory budget).  The source pages have no
+ * counterpart; this is a property of the library, not of the method.
+ *
+ * Same arguments and result as fgemm_sgemm_splitk, without the workspace: the
+ * partial products go to one fixed array of FGEMM_NOALLOC_SCRATCH_BYTES in the
+ * global memory of every GPU that loads the library, held until the process exits.
+ *   - A problem needing more than that (fgemm_splitk_workspace_size(M, N, K, splits)
+ *     > FGEMM_NOALLOC_SCRATCH_BYTES) is rejected with FGEMM_ERR_NOT_SUPPORTED before
+ *     anything else happens; 16 MiB holds, e.g., 4 slices of a 1024 x 1024 C.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call before
+ *     any stream capture.
+ *   - Every call uses the same array and leaves its contents behind; nothing in it has
+ *     to start at zero (each partial product is written before it is read).  Calls
+ *     whose kernels overlap on the GPU -- on different streams, or from different
+ *     host threads -- race on the array and give wrong results: order them.
+ *   - It calls no cudaMalloc, cudaFree or allocating library routine.
+ */
+#define FGEMM_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+fgemm_status fgemm_sgemm_splitk_noalloc(fgemm_op transa, fgemm_op transb, int M, int N, int K,
+                                        float alpha, const float *A, int lda, const float *B,
+                                        int ldb, float beta, float *C, int ldc, const float *bias,
+                                        int apply_relu, int splits, cudaStream_t stream);
+
+/*
  * Arithmetic of the contraction (GEMM 优化详解, "进一步优化方向": tensor cores are the
  * next step after the CUDA-core ladder):
  *   FGEMM_MATH_FP32    FP32 FMA on the CUDA cores (the plain entry points use this).
