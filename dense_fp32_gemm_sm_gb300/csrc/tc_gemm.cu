@@ -65,6 +65,23 @@ bool make_operand_map(CUtensorMap *map, const float *base, bool kmajor, long lon
     return r == CUDA_SUCCESS;
 }
 
+// C as the 3-D tensor map (N, M, batch) of the TMA-store epilogue: 32 x 32 boxes
+// with the 128-byte swizzle.
+bool make_output_map(CUtensorMap *map, float *base, long long M, long long N, long long ldc,
+                     long long batch, long long stride)
+{
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    if (batch <= 1) stride = ldc * M;
+    const cuuint64_t dims[3] = {(cuuint64_t)N, (cuuint64_t)M, (cuuint64_t)batch};
+    const cuuint64_t strides[2] = {(cuuint64_t)ldc * 4, (cuuint64_t)stride * 4};
+    const cuuint32_t box[3] = {32, 32, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int current_device(int *dev) { return cudaGetDevice(dev) == cudaSuccess ? 0 : -1; }
 
 // Device address of g_tc_error on the current device (looked up once per device).
@@ -153,6 +170,10 @@ fgemm_status launch_tc(int mode, const TcProblem &q, cudaStream_t stream)
     p.relu = q.relu ? 1 : 0;
     p.c_vec = (reinterpret_cast<uintptr_t>(q.C) % 16 == 0 && q.ldc % 4 == 0 &&
                (q.batch <= 1 || q.sC % 4 == 0))
+                  ? 1
+                  : 0;
+    p.c_tma = (q.beta == 0.0f && p.c_vec && q.ldc < (1ll << 38) && q.sC < (1ll << 38) &&
+               make_output_map(&p.tmC, q.C, q.M, q.N, q.ldc, q.batch, q.sC))
                   ? 1
                   : 0;
     p.tiles_m = (q.M + tc::BM - 1) / tc::BM;

@@ -23,7 +23,8 @@
 //              the producer through an mbarrier.
 //   warps 2-5  3xTF32: split each stage into hi/lo in place; then, for every mode,
 //              the epilogue: tcgen05.ld of their 32 accumulator lanes, alpha, beta*C,
-//              bias, ReLU, stores.
+//              bias, ReLU; with beta == 0 the rows are staged in shared memory and
+//              written by TMA stores, otherwise stored directly.
 // Operands stored K-major (A as M x K, B as N x K) arrive by TMA already in the
 // canonical layout.  An operand stored MN-major (A as K x M, B as K x N) arrives as a
 // plain 32 x 128 tile and warps 2-5 transpose it in place into the canonical K-major
@@ -71,6 +72,7 @@ struct TcParams {
     // MN-major operand: dims (rows, K, batch), box (128, 32, 1), no swizzle.
     CUtensorMap tmA;
     CUtensorMap tmB;
+    CUtensorMap tmC;  // C: dims (N, M, batch), box (32, 32, 1), 128-byte swizzle (stores)
     float *C;
     const float *bias;
     long long ldc, strideC;
@@ -78,6 +80,7 @@ struct TcParams {
     float alpha, beta;
     int relu;
     int c_vec;
+    int c_tma;  // beta == 0 and C allows TMA stores: stage rows in shared memory
     int tiles_m, tiles_n;
     int batch0;  // first problem of this launch (the launch covers gridDim.z problems)
     unsigned long long wait_limit_ns;  // bound of every mbarrier wait
@@ -159,6 +162,17 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
         "[%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
         : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, uint32_t src, int c0, int c1,
+                                             int c2)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(src), "r"(c0), "r"(c1), "r"(c2)
+        : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile in the canonical 128-byte
@@ -455,7 +469,47 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int q = warp & 3;
         const int row = m0 + q * 32 + lane;
         const bool acc_ok = KT > 0 && mbar_wait(acc_bar, 0, err, ERR_EPILOGUE, lim);
-        if (acc_ok) {
+        if (acc_ok && p.c_tma) {
+            // beta == 0: alpha, bias, ReLU in registers; each 32 x 32 chunk is staged in
+            // shared memory (128-byte swizzle: lane = row, 16-byte chunk index XOR
+            // row % 8, conflict-free) and written by one TMA store, which clips the
+            // rows and columns outside C.  Two buffers per warp; the operand stages are
+            // free once every MMA has completed.
+            tc_fence_after();
+            const uint32_t stage0 = sbase + (uint32_t)q * 8192u;
+#pragma unroll 1
+            for (int c0 = 0; c0 < BN; c0 += 32) {
+                const int buf = (c0 >> 5) & 1;
+                if (c0 >= 64) {
+                    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                    __syncwarp();
+                }
+                uint32_t r[32];
+                tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
+                uint8_t *const rowbuf = smem + q * 8192 + buf * 4096 + lane * 128;
+#pragma unroll
+                for (int g = 0; g < 8; ++g) {
+                    float v[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int gc = n0 + c0 + 4 * g + e;
+                        float o = p.alpha * __uint_as_float(r[4 * g + e]);
+                        if (p.bias && gc < p.N) o += __ldg(p.bias + gc);
+                        if (p.relu) o = fmaxf(o, 0.0f);
+                        v[e] = o;
+                    }
+                    *reinterpret_cast<float4 *>(rowbuf + ((g ^ (lane & 7)) << 4)) =
+                        make_float4(v[0], v[1], v[2], v[3]);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                // (a chunk entirely outside C is not stored at all)
+                if (lane == 0 && n0 + c0 < p.N && m0 + q * 32 < p.M)
+                    tma_store_3d(&p.tmC, stage0 + (uint32_t)buf * 4096u, n0 + c0, m0 + q * 32, bz);
+            }
+            if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+            __syncwarp();
+        } else if (acc_ok) {
             tc_fence_after();
             float *const C = p.C + (long long)bz * p.strideC;
 #pragma unroll 1
