@@ -117,23 +117,20 @@ cudaError_t prepare_tc()
 }
 
 template <int MODE, int TA, int TB>
-fgemm_status launch_tc_mode(tc::TcParams &p, int batch, cudaStream_t stream)
+fgemm_status launch_tc_mode(tc::TcParams &p, cudaStream_t stream)
 {
     unsigned *err = error_word();
-    if (!err || prepare_tc<MODE, TA, TB>() != cudaSuccess) {
+    int sms = 0;
+    if (!err || prepare_tc<MODE, TA, TB>() != cudaSuccess || device_sm_count(&sms) != 0) {
         (void)cudaGetLastError();
         return FGEMM_ERR_LAUNCH;
     }
-    const long long tiles = (long long)p.tiles_m * p.tiles_n;
-    const int kMaxZ = 65535;
-    for (int b0 = 0; b0 < batch; b0 += kMaxZ) {
-        const int nb = batch - b0 < kMaxZ ? batch - b0 : kMaxZ;
-        p.batch0 = b0;
-        tc::tc_gemm_kernel<MODE, TA, TB><<<dim3((unsigned)tiles, 1, (unsigned)nb), tc::THREADS,
-                                           tc::Layout<MODE>::SMEM_BYTES, stream>>>(p, err);
-        if (cudaGetLastError() != cudaSuccess) return FGEMM_ERR_LAUNCH;
-    }
-    return FGEMM_OK;
+    // Persistent: one CTA per SM (or per tile, if there are fewer tiles).
+    const long long tiles = (long long)p.tiles_m * p.tiles_n * p.batch;
+    const long long grid = tiles < sms ? tiles : sms;
+    tc::tc_gemm_kernel<MODE, TA, TB><<<(unsigned)grid, tc::THREADS, tc::Layout<MODE>::SMEM_BYTES,
+                                       stream>>>(p, err);
+    return cudaGetLastError() == cudaSuccess ? FGEMM_OK : FGEMM_ERR_LAUNCH;
 }
 
 }  // namespace
@@ -178,22 +175,23 @@ fgemm_status launch_tc(int mode, const TcProblem &q, cudaStream_t stream)
                   : 0;
     p.tiles_m = (q.M + tc::BM - 1) / tc::BM;
     p.tiles_n = (q.N + tc::BN - 1) / tc::BN;
+    p.batch = q.batch;
     p.withhold_kb = g_withhold_kb.load(std::memory_order_relaxed);
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     const int layout = q.ta * 2 + q.tb;  // 0: NN, 1: NT, 2: TN, 3: TT
     if (mode == tc::MODE_3XTF32) {
         switch (layout) {
-        case 0: return launch_tc_mode<tc::MODE_3XTF32, 0, 0>(p, q.batch, stream);
-        case 1: return launch_tc_mode<tc::MODE_3XTF32, 0, 1>(p, q.batch, stream);
-        case 2: return launch_tc_mode<tc::MODE_3XTF32, 1, 0>(p, q.batch, stream);
-        default: return launch_tc_mode<tc::MODE_3XTF32, 1, 1>(p, q.batch, stream);
+        case 0: return launch_tc_mode<tc::MODE_3XTF32, 0, 0>(p, stream);
+        case 1: return launch_tc_mode<tc::MODE_3XTF32, 0, 1>(p, stream);
+        case 2: return launch_tc_mode<tc::MODE_3XTF32, 1, 0>(p, stream);
+        default: return launch_tc_mode<tc::MODE_3XTF32, 1, 1>(p, stream);
         }
     }
     switch (layout) {
-    case 0: return launch_tc_mode<tc::MODE_TF32, 0, 0>(p, q.batch, stream);
-    case 1: return launch_tc_mode<tc::MODE_TF32, 0, 1>(p, q.batch, stream);
-    case 2: return launch_tc_mode<tc::MODE_TF32, 1, 0>(p, q.batch, stream);
-    default: return launch_tc_mode<tc::MODE_TF32, 1, 1>(p, q.batch, stream);
+    case 0: return launch_tc_mode<tc::MODE_TF32, 0, 0>(p, stream);
+    case 1: return launch_tc_mode<tc::MODE_TF32, 0, 1>(p, stream);
+    case 2: return launch_tc_mode<tc::MODE_TF32, 1, 0>(p, stream);
+    default: return launch_tc_mode<tc::MODE_TF32, 1, 1>(p, stream);
     }
 }
 

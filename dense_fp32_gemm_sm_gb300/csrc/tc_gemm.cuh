@@ -15,16 +15,22 @@
 //            precision accuracy from Tensor Cores while surpassing the FP32 theoretical
 //            peak performance", 2022).
 //
-// Structure (one CTA per 128 x 128 tile of C, six warps):
+// Structure: a persistent kernel, one CTA per SM, each CTA walking 128 x 128 tiles
+// of C (tile = blockIdx.x, + gridDim.x, ...), ten warps:
 //   warp 0     TMA producer: one lane streams 128 x 32 tiles of A and B (128-byte
-//              swizzled, the canonical K-major operand layout) into a ring of stages.
-//   warp 1     allocates the 128 x 128 FP32 accumulator in tensor memory; one lane
-//              issues tcgen05.mma (M=128, N=128, K=8) and commits each stage back to
-//              the producer through an mbarrier.
-//   warps 2-5  3xTF32: split each stage into hi/lo in place; then, for every mode,
-//              the epilogue: tcgen05.ld of their 32 accumulator lanes, alpha, beta*C,
-//              bias, ReLU; with beta == 0 the rows are staged in shared memory and
-//              written by TMA stores, otherwise stored directly.
+//              swizzled, the canonical K-major operand layout) into a ring of stages,
+//              running ahead across tile boundaries.
+//   warp 1     allocates two 128 x 128 FP32 accumulators in tensor memory; one lane
+//              issues tcgen05.mma (M=128, N=128, K=8) into them alternately and
+//              commits each stage back to the producer through an mbarrier.
+//   warps 2-5  3xTF32: split each stage into hi/lo in place; both modes: transpose
+//              MN-major operands on chip (idle otherwise).
+//   warps 6-9  epilogue of the previous tile while the next one is being multiplied
+//              (warps 2-5 join them when there is nothing to split or transpose):
+//              tcgen05.ld of their 32 accumulator lanes, alpha, beta*C, bias, ReLU;
+//              with beta == 0 the rows are staged in shared memory and written by
+//              TMA stores, otherwise stored directly; then the accumulator is handed
+//              back to the MMA warp.
 // Operands stored K-major (A as M x K, B as N x K) arrive by TMA already in the
 // canonical layout.  An operand stored MN-major (A as K x M, B as K x N) arrives as a
 // plain 32 x 128 tile and warps 2-5 transpose it in place into the canonical K-major
@@ -45,8 +51,8 @@ constexpr int BM = 128, BN = 128, BK = 32;  // BK FP32 values = one 128-byte swi
 constexpr int UMMA_K = 8;                   // K of one kind::tf32 MMA (32 bytes)
 constexpr int TILE_A_BYTES = BM * BK * 4;   // 16 KB
 constexpr int TILE_B_BYTES = BN * BK * 4;   // 16 KB
-constexpr int THREADS = 192;
-constexpr uint32_t TMEM_COLS = BN;          // FP32 accumulator: 128 lanes x BN columns
+constexpr int THREADS = 320;               // 10 warps, see the kernel
+constexpr uint32_t TMEM_COLS = 2 * BN;      // two FP32 accumulators of 128 lanes x BN columns
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // default: 4 s per wait
 
 // Error bits recorded in the device error word.
@@ -57,14 +63,19 @@ enum Mode { MODE_TF32 = 1, MODE_3XTF32 = 3 };
 
 template <int MODE>
 struct Layout {
-    static constexpr int STAGES = MODE == MODE_3XTF32 ? 3 : 3;
+    static constexpr int STAGES = MODE == MODE_3XTF32 ? 3 : 6;
     // Per stage: A, B (raw, or hi after the split), then A_lo, B_lo in 3xTF32.
     static constexpr int STAGE_BYTES =
         (TILE_A_BYTES + TILE_B_BYTES) * (MODE == MODE_3XTF32 ? 2 : 1);
-    static constexpr int BAR_OFFSET = STAGES * STAGE_BYTES;
-    // full[S], split[S], empty[S], acc_full, drain, read_done (8 bytes each) + TMEM slot
-    static constexpr int BAR_BYTES = (3 * STAGES + 3) * 8 + 8;
+    // Epilogue staging: 32 KB, two 4 KB chunk buffers per epilogue warp (four warps),
+    // or one per warp when eight warps share the epilogue.
+    static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;
+    static constexpr int EPI_BYTES = 4 * 8192;
+    static constexpr int BAR_OFFSET = EPI_OFFSET + EPI_BYTES;
+    // full[S], split[S], empty[S], acc_full[2], acc_empty[2], drain, read_done, TMEM slot
+    static constexpr int BAR_BYTES = (3 * STAGES + 6) * 8 + 8;
     static constexpr int SMEM_BYTES = 1024 + BAR_OFFSET + BAR_BYTES;  // + alignment slack
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory per CTA");
 };
 
 struct TcParams {
@@ -82,7 +93,7 @@ struct TcParams {
     int c_vec;
     int c_tma;  // beta == 0 and C allows TMA stores: stage rows in shared memory
     int tiles_m, tiles_n;
-    int batch0;  // first problem of this launch (the launch covers gridDim.z problems)
+    int batch;   // problems in the strided batch; tiles run over (batch, tile-row, tile-col)
     unsigned long long wait_limit_ns;  // bound of every mbarrier wait
     int withhold_kb;  // testing: the producer never issues this k-block (-1: none)
 };
@@ -319,6 +330,10 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr bool A_K = TA == 0, B_K = TB == 1;
     constexpr bool THREE = MODE == MODE_3XTF32;
     constexpr bool CONVERT = THREE || !A_K || !B_K;  // warps 2-5 touch each stage
+    // Without a split or transpose, warps 2-5 share the epilogue with warps 6-9.
+    constexpr int EPI_WARPS = CONVERT ? 4 : 8;
+    constexpr int EPI_COLS = BN * 4 / EPI_WARPS;  // columns of a tile per epilogue warp
+    constexpr int EPI_BUFS = 8 / (EPI_WARPS / 4) / 4;  // 4 KB buffers per epilogue warp
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment of the operand tiles (the swizzle atom).
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -328,10 +343,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto full_bar = [&](int s) { return bar0 + 8u * s; };
     auto split_bar = [&](int s) { return bar0 + 8u * (S + s); };
     auto empty_bar = [&](int s) { return bar0 + 8u * (2 * S + s); };
-    const uint32_t acc_bar = bar0 + 8u * (3 * S);
-    const uint32_t drain_bar = acc_bar + 8u;
-    const uint32_t read_bar = acc_bar + 16u;
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::BAR_OFFSET + 8 * (3 * S + 3));
+    auto acc_full_bar = [&](int a) { return bar0 + 8u * (3 * S + a); };
+    auto acc_empty_bar = [&](int a) { return bar0 + 8u * (3 * S + 2 + a); };
+    const uint32_t drain_bar = bar0 + 8u * (3 * S + 4);
+    const uint32_t read_bar = bar0 + 8u * (3 * S + 5);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::BAR_OFFSET + 8 * (3 * S + 6));
 
     auto a_off = [&](int s) { return s * L::STAGE_BYTES; };
     auto b_off = [&](int s) { return s * L::STAGE_BYTES + TILE_A_BYTES; };
@@ -339,12 +355,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     auto blo_off = [&](int s) { return s * L::STAGE_BYTES + 2 * TILE_A_BYTES + TILE_B_BYTES; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tile = blockIdx.x;
-    const int tm = tile / p.tiles_n, tn = tile % p.tiles_n;
-    const int m0 = tm * BM, n0 = tn * BN;
-    const int bz = p.batch0 + blockIdx.z;
     const int KT = (p.K + BK - 1) / BK;
+    const int tiles_per_problem = p.tiles_m * p.tiles_n;
+    const long long total_tiles = (long long)tiles_per_problem * p.batch;
     const unsigned long long lim = p.wait_limit_ns;
+    // The j-th tile of this CTA: problem bz, rows m0.., columns n0.. (grouped order:
+    // 8 tile-rows swept column by column, so resident CTAs share panels in L2).
+    auto tile_coords = [&](long long t, int &m0, int &n0, int &bz) {
+        bz = (int)(t / tiles_per_problem);
+        const int r = (int)(t - (long long)bz * tiles_per_problem);
+        const int per_group = 8 * p.tiles_n;
+        const int group = r / per_group;
+        const int first_m = group * 8;
+        const int rows_in_group = min(p.tiles_m - first_m, 8);
+        const int in_group = r - group * per_group;
+        m0 = (first_m + in_group % rows_in_group) * BM;
+        n0 = (in_group / rows_in_group) * BN;
+    };
 
     if (warp == 0 && lane == 0) {
         for (int s = 0; s < S; ++s) {
@@ -352,7 +379,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_init(split_bar(s), 128);
             mbar_init(empty_bar(s), 1);
         }
-        mbar_init(acc_bar, 1);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(acc_full_bar(a), 1);
+            mbar_init(acc_empty_bar(a), EPI_WARPS);  // one arrival per epilogue warp
+        }
         mbar_init(drain_bar, 1);
         mbar_init(read_bar, 128);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -371,188 +401,231 @@ __global__ void __launch_bounds__(THREADS, 1)
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(tmem_slot);
 
     if (warp == 0) {
-        // ---- TMA producer ----
+        // ---- TMA producer: every k-block of every tile of this CTA, in order ----
         if (lane == 0) {
-            int issued = 0;
-            for (int kb = 0; kb < KT; ++kb) {
-                const int s = kb % S, round = kb / S;
-                if (round > 0 && !mbar_wait(empty_bar(s), (round - 1) & 1, err, ERR_PRODUCER, lim))
-                    break;
-                if (kb == p.withhold_kb) break;  // testing: as if this copy never arrived
-                mbar_arrive_expect_tx(full_bar(s), TILE_A_BYTES + TILE_B_BYTES);
-                if constexpr (A_K)
-                    tma_load_3d(sbase + a_off(s), &p.tmA, full_bar(s), kb * BK, m0, bz);
-                else
-                    tma_load_3d(sbase + a_off(s), &p.tmA, full_bar(s), m0, kb * BK, bz);
-                if constexpr (B_K)
-                    tma_load_3d(sbase + b_off(s), &p.tmB, full_bar(s), kb * BK, n0, bz);
-                else
-                    tma_load_3d(sbase + b_off(s), &p.tmB, full_bar(s), n0, kb * BK, bz);
-                ++issued;
+            int g = 0;  // k-blocks issued so far (runs across tiles)
+            bool ok = true;
+            for (long long t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+                int m0, n0, bz;
+                tile_coords(t, m0, n0, bz);
+                for (int kb = 0; kb < KT; ++kb) {
+                    const int s = g % S, round = g / S;
+                    if (round > 0 && !mbar_wait(empty_bar(s), (round - 1) & 1, err, ERR_PRODUCER, lim)) {
+                        ok = false;
+                        break;
+                    }
+                    if (g == p.withhold_kb) {  // testing: as if this copy never arrived
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(full_bar(s), TILE_A_BYTES + TILE_B_BYTES);
+                    if constexpr (A_K)
+                        tma_load_3d(sbase + a_off(s), &p.tmA, full_bar(s), kb * BK, m0, bz);
+                    else
+                        tma_load_3d(sbase + a_off(s), &p.tmA, full_bar(s), m0, kb * BK, bz);
+                    if constexpr (B_K)
+                        tma_load_3d(sbase + b_off(s), &p.tmB, full_bar(s), kb * BK, n0, bz);
+                    else
+                        tma_load_3d(sbase + b_off(s), &p.tmB, full_bar(s), n0, kb * BK, bz);
+                    ++g;
+                }
             }
             // Never leave with copies in flight into this CTA's shared memory.
-            for (int kb = issued - S < 0 ? 0 : issued - S; kb < issued; ++kb)
-                mbar_wait(full_bar(kb % S), (kb / S) & 1, err, ERR_DRAIN, lim, false);
+            for (int k = g - S < 0 ? 0 : g - S; k < g; ++k)
+                mbar_wait(full_bar(k % S), (k / S) & 1, err, ERR_DRAIN, lim, false);
         }
     } else if (warp == 1) {
-        // ---- MMA issuer ----
+        // ---- MMA issuer: accumulator j & 1 for this CTA's j-th tile ----
         if (lane == 0) {
             constexpr uint32_t idesc = make_idesc(BM, BN);
-            int done = 0;
-            for (int kb = 0; kb < KT; ++kb) {
-                const int s = kb % S, round = kb / S;
-                const bool ok = CONVERT ? mbar_wait(split_bar(s), round & 1, err, ERR_MMA_WAIT, lim)
-                                        : mbar_wait(full_bar(s), round & 1, err, ERR_MMA_WAIT, lim);
-                if (!ok) break;
-                tc_fence_after();
-                const uint64_t ad = kmajor_sw128_desc(sbase + a_off(s));
-                const uint64_t bd = kmajor_sw128_desc(sbase + b_off(s));
-#pragma unroll
-                for (int k = 0; k < BK / UMMA_K; ++k) {
-                    const uint64_t koff = (uint64_t)((k * UMMA_K * 4) >> 4);  // 32 bytes per step
-                    if constexpr (THREE) {
-                        const uint64_t ald = kmajor_sw128_desc(sbase + alo_off(s));
-                        const uint64_t bld = kmajor_sw128_desc(sbase + blo_off(s));
-                        umma_tf32(tmem, ald + koff, bd + koff, idesc, (kb | k) != 0);
-                        umma_tf32(tmem, ad + koff, bld + koff, idesc, 1u);
-                        umma_tf32(tmem, ad + koff, bd + koff, idesc, 1u);
-                    } else {
-                        umma_tf32(tmem, ad + koff, bd + koff, idesc, (kb | k) != 0);
-                    }
+            int g = 0;
+            bool ok = true;
+            int j = 0;
+            for (long long t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++j) {
+                const int acc = j & 1, use = j >> 1;
+                // The epilogue must have drained this accumulator (tile j - 2).
+                if (use > 0 && !mbar_wait(acc_empty_bar(acc), (use - 1) & 1, err, ERR_MMA_WAIT, lim)) {
+                    ok = false;
+                    break;
                 }
-                umma_commit(empty_bar(s));  // the stage is free once these MMAs have read it
-                ++done;
+                tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < KT; ++kb, ++g) {
+                    const int s = g % S, round = g / S;
+                    ok = CONVERT ? mbar_wait(split_bar(s), round & 1, err, ERR_MMA_WAIT, lim)
+                                 : mbar_wait(full_bar(s), round & 1, err, ERR_MMA_WAIT, lim);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint64_t ad = kmajor_sw128_desc(sbase + a_off(s));
+                    const uint64_t bd = kmajor_sw128_desc(sbase + b_off(s));
+#pragma unroll
+                    for (int k = 0; k < BK / UMMA_K; ++k) {
+                        const uint64_t koff = (uint64_t)((k * UMMA_K * 4) >> 4);  // 32 bytes per step
+                        if constexpr (THREE) {
+                            const uint64_t ald = kmajor_sw128_desc(sbase + alo_off(s));
+                            const uint64_t bld = kmajor_sw128_desc(sbase + blo_off(s));
+                            umma_tf32(d, ald + koff, bd + koff, idesc, (kb | k) != 0);
+                            umma_tf32(d, ad + koff, bld + koff, idesc, 1u);
+                            umma_tf32(d, ad + koff, bd + koff, idesc, 1u);
+                        } else {
+                            umma_tf32(d, ad + koff, bd + koff, idesc, (kb | k) != 0);
+                        }
+                    }
+                    umma_commit(empty_bar(s));  // the stage is free once these MMAs have read it
+                }
+                if (ok) umma_commit(acc_full_bar(acc));  // accumulator j is complete
             }
-            if (done == KT) {
-                umma_commit(acc_bar);
-            } else {
+            if (!ok) {
                 // Give up: make sure nothing issued is still running before teardown.
                 umma_commit(drain_bar);
                 mbar_wait(drain_bar, 0, err, ERR_DRAIN, lim, false);
             }
         }
-    } else {
-        // ---- warps 2..5: split / transpose, then the epilogue ----
-        const int t = threadIdx.x - 64;  // 0..127
+    } else if (CONVERT && warp < 6) {
+        // ---- warps 2..5: split / transpose every stage ----
         if constexpr (CONVERT) {
-            int transposes = 0;  // uses of read_bar so far (its phase)
-            for (int kb = 0; kb < KT; ++kb) {
-                const int s = kb % S, round = kb / S;
-                if (!mbar_wait(full_bar(s), round & 1, err, ERR_SPLIT_WAIT, lim)) break;
-                bool ok = true;
-                if constexpr (A_K) {
-                    if constexpr (THREE)
-                        split_kmajor(reinterpret_cast<float4 *>(smem + a_off(s)),
-                                     reinterpret_cast<float4 *>(smem + alo_off(s)), t);
-                } else {
-                    ok = transpose_mnmajor<THREE>(smem + a_off(s), smem + alo_off(s), t, read_bar,
-                                                  transposes & 1, err, lim);
-                    ++transposes;
+            const int t = threadIdx.x - 64;  // 0..127
+            int g = 0, transposes = 0;
+            bool ok = true;
+            for (long long tl = blockIdx.x; ok && tl < total_tiles; tl += gridDim.x) {
+                for (int kb = 0; kb < KT; ++kb, ++g) {
+                    const int s = g % S, round = g / S;
+                    ok = mbar_wait(full_bar(s), round & 1, err, ERR_SPLIT_WAIT, lim);
+                    if (!ok) break;
+                    if constexpr (A_K) {
+                        if constexpr (THREE)
+                            split_kmajor(reinterpret_cast<float4 *>(smem + a_off(s)),
+                                         reinterpret_cast<float4 *>(smem + alo_off(s)), t);
+                    } else {
+                        ok = transpose_mnmajor<THREE>(smem + a_off(s), smem + alo_off(s), t,
+                                                      read_bar, transposes & 1, err, lim);
+                        ++transposes;
+                    }
+                    if (!ok) break;
+                    if constexpr (B_K) {
+                        if constexpr (THREE)
+                            split_kmajor(reinterpret_cast<float4 *>(smem + b_off(s)),
+                                         reinterpret_cast<float4 *>(smem + blo_off(s)), t);
+                    } else {
+                        ok = transpose_mnmajor<THREE>(smem + b_off(s), smem + blo_off(s), t,
+                                                      read_bar, transposes & 1, err, lim);
+                        ++transposes;
+                    }
+                    if (!ok) break;
+                    // Generic-proxy writes must be visible to the tensor core (async proxy).
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    mbar_arrive(split_bar(s));
                 }
-                if (!ok) break;
-                if constexpr (B_K) {
-                    if constexpr (THREE)
-                        split_kmajor(reinterpret_cast<float4 *>(smem + b_off(s)),
-                                     reinterpret_cast<float4 *>(smem + blo_off(s)), t);
-                } else {
-                    ok = transpose_mnmajor<THREE>(smem + b_off(s), smem + blo_off(s), t, read_bar,
-                                                  transposes & 1, err, lim);
-                    ++transposes;
-                }
-                if (!ok) break;
-                // Generic-proxy writes must be visible to the tensor core (async proxy).
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                mbar_arrive(split_bar(s));
             }
         }
-        // Epilogue: warp w reads accumulator lanes 32*(w%4) .. +31 (rows of the tile).
+    } else {
+        // ---- epilogue warps (6..9, or 2..9): tile j while tile j + 1 is multiplied ----
+        // Warp w reads accumulator lanes 32*(w%4) .. +31 (rows of the tile) and columns
+        // [c_first, c_first + EPI_COLS).
         const int q = warp & 3;
-        const int row = m0 + q * 32 + lane;
-        const bool acc_ok = KT > 0 && mbar_wait(acc_bar, 0, err, ERR_EPILOGUE, lim);
-        if (acc_ok && p.c_tma) {
-            // beta == 0: alpha, bias, ReLU in registers; each 32 x 32 chunk is staged in
-            // shared memory (128-byte swizzle: lane = row, 16-byte chunk index XOR
-            // row % 8, conflict-free) and written by one TMA store, which clips the
-            // rows and columns outside C.  Two buffers per warp; the operand stages are
-            // free once every MMA has completed.
+        const int ew = warp - (CONVERT ? 6 : 2);  // 0 .. EPI_WARPS-1
+        const int c_first = (ew / 4) * EPI_COLS;
+        const uint32_t stage0 = sbase + (uint32_t)(L::EPI_OFFSET + ew * EPI_BUFS * 4096);
+        uint8_t *const ebuf = smem + L::EPI_OFFSET + ew * EPI_BUFS * 4096;
+        int j = 0;
+        for (long long t = blockIdx.x; t < total_tiles; t += gridDim.x, ++j) {
+            int m0, n0, bz;
+            tile_coords(t, m0, n0, bz);
+            const int acc = j & 1, use = j >> 1;
+            if (!mbar_wait(acc_full_bar(acc), use & 1, err, ERR_EPILOGUE, lim)) break;
             tc_fence_after();
-            const uint32_t stage0 = sbase + (uint32_t)q * 8192u;
+            const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            const int row = m0 + q * 32 + lane;
+            if (p.c_tma) {
+                // beta == 0: alpha, bias, ReLU in registers; each 32 x 32 chunk is staged in
+                // shared memory (128-byte swizzle: lane = row, 16-byte chunk index XOR
+                // row % 8, conflict-free) and written by one TMA store, which clips the
+                // rows and columns outside C.  Two buffers per warp.
 #pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                const int buf = (c0 >> 5) & 1;
-                if (c0 >= 64) {
-                    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                    __syncwarp();
-                }
-                uint32_t r[32];
-                tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
-                uint8_t *const rowbuf = smem + q * 8192 + buf * 4096 + lane * 128;
-#pragma unroll
-                for (int g = 0; g < 8; ++g) {
-                    float v[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int gc = n0 + c0 + 4 * g + e;
-                        float o = p.alpha * __uint_as_float(r[4 * g + e]);
-                        if (p.bias && gc < p.N) o += __ldg(p.bias + gc);
-                        if (p.relu) o = fmaxf(o, 0.0f);
-                        v[e] = o;
+                for (int c0 = c_first; c0 < c_first + EPI_COLS; c0 += 32) {
+                    const int buf = EPI_BUFS == 2 ? (c0 >> 5) & 1 : 0;
+                    // the store that last read this buffer must have finished reading it
+                    if (lane == 0) {
+                        if constexpr (EPI_BUFS == 2)
+                            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                        else
+                            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                     }
-                    *reinterpret_cast<float4 *>(rowbuf + ((g ^ (lane & 7)) << 4)) =
-                        make_float4(v[0], v[1], v[2], v[3]);
-                }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
-                // (a chunk entirely outside C is not stored at all)
-                if (lane == 0 && n0 + c0 < p.N && m0 + q * 32 < p.M)
-                    tma_store_3d(&p.tmC, stage0 + (uint32_t)buf * 4096u, n0 + c0, m0 + q * 32, bz);
-            }
-            if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-            __syncwarp();
-        } else if (acc_ok) {
-            tc_fence_after();
-            float *const C = p.C + (long long)bz * p.strideC;
-#pragma unroll 1
-            for (int c0 = 0; c0 < BN; c0 += 32) {
-                uint32_t r[32];
-                tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)c0, r);
-                if (row < p.M) {
-                    float *const crow = C + (long long)row * p.ldc;
+                    __syncwarp();
+                    uint32_t r[32];
+                    tmem_ld_32cols(src + (uint32_t)c0, r);
+                    uint8_t *const rowbuf = ebuf + buf * 4096 + lane * 128;
 #pragma unroll
                     for (int g = 0; g < 8; ++g) {
-                        const int gc = n0 + c0 + 4 * g;
                         float v[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) v[e] = p.alpha * __uint_as_float(r[4 * g + e]);
-                        if (p.c_vec && gc + 3 < p.N) {
-                            if (p.beta != 0.0f) {
-                                const float4 c = *reinterpret_cast<const float4 *>(crow + gc);
-                                v[0] = fmaf(p.beta, c.x, v[0]);
-                                v[1] = fmaf(p.beta, c.y, v[1]);
-                                v[2] = fmaf(p.beta, c.z, v[2]);
-                                v[3] = fmaf(p.beta, c.w, v[3]);
-                            }
+                        for (int e = 0; e < 4; ++e) {
+                            const int gc = n0 + c0 + 4 * g + e;
+                            float o = p.alpha * __uint_as_float(r[4 * g + e]);
+                            if (p.bias && gc < p.N) o += __ldg(p.bias + gc);
+                            if (p.relu) o = fmaxf(o, 0.0f);
+                            v[e] = o;
+                        }
+                        *reinterpret_cast<float4 *>(rowbuf + ((g ^ (lane & 7)) << 4)) =
+                            make_float4(v[0], v[1], v[2], v[3]);
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    // (a chunk entirely outside C is not stored at all)
+                    if (lane == 0 && n0 + c0 < p.N && m0 + q * 32 < p.M)
+                        tma_store_3d(&p.tmC, stage0 + (uint32_t)buf * 4096u, n0 + c0, m0 + q * 32, bz);
+                }
+            } else {
+                float *const C = p.C + (long long)bz * p.strideC;
+#pragma unroll 1
+                for (int c0 = c_first; c0 < c_first + EPI_COLS; c0 += 32) {
+                    uint32_t r[32];
+                    tmem_ld_32cols(src + (uint32_t)c0, r);
+                    if (row < p.M) {
+                        float *const crow = C + (long long)row * p.ldc;
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                if (p.bias) v[e] += __ldg(p.bias + gc + e);
-                                if (p.relu) v[e] = fmaxf(v[e], 0.0f);
-                            }
-                            *reinterpret_cast<float4 *>(crow + gc) = make_float4(v[0], v[1], v[2], v[3]);
-                        } else {
+                        for (int g = 0; g < 8; ++g) {
+                            const int gc = n0 + c0 + 4 * g;
+                            float v[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                if (gc + e >= p.N) break;
-                                float o = v[e];
-                                if (p.beta != 0.0f) o = fmaf(p.beta, crow[gc + e], o);
-                                if (p.bias) o += __ldg(p.bias + gc + e);
-                                if (p.relu) o = fmaxf(o, 0.0f);
-                                crow[gc + e] = o;
+                            for (int e = 0; e < 4; ++e) v[e] = p.alpha * __uint_as_float(r[4 * g + e]);
+                            if (p.c_vec && gc + 3 < p.N) {
+                                if (p.beta != 0.0f) {
+                                    const float4 c = *reinterpret_cast<const float4 *>(crow + gc);
+                                    v[0] = fmaf(p.beta, c.x, v[0]);
+                                    v[1] = fmaf(p.beta, c.y, v[1]);
+                                    v[2] = fmaf(p.beta, c.z, v[2]);
+                                    v[3] = fmaf(p.beta, c.w, v[3]);
+                                }
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    if (p.bias) v[e] += __ldg(p.bias + gc + e);
+                                    if (p.relu) v[e] = fmaxf(v[e], 0.0f);
+                                }
+                                *reinterpret_cast<float4 *>(crow + gc) =
+                                    make_float4(v[0], v[1], v[2], v[3]);
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    if (gc + e >= p.N) break;
+                                    float o = v[e];
+                                    if (p.beta != 0.0f) o = fmaf(p.beta, crow[gc + e], o);
+                                    if (p.bias) o += __ldg(p.bias + gc + e);
+                                    if (p.relu) o = fmaxf(o, 0.0f);
+                                    crow[gc + e] = o;
+                                }
                             }
                         }
                     }
                 }
             }
+            // Hand the accumulator back: all of this warp's tensor-memory reads are done.
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acc_empty_bar(acc));
         }
+        if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+        __syncwarp();
     }
 
     // Teardown: the allocating warp frees the tensor memory once every thread is done.
