@@ -22,6 +22,7 @@ const ConfigInfo kConfigs[NUM_CONFIGS] = {
     {"simt_128x64x16_t8x8_s4", 128, 64, true},
     {"simt_64x64x16_t4x4_s4", 64, 64, true},
     {"simt_64x64x16_t4x4_s4_scalar", 64, 64, false},
+    {"simt_32x32x16_t4x4_s4", 32, 32, true},
 };
 
 namespace {

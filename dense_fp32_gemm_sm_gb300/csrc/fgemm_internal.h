@@ -20,7 +20,8 @@ enum ConfigId {
     CFG_128x64 = 1,         // 128x64x16, 8x8 per thread, 4 stages, 3 CTAs/SM (more CTAs for mid sizes)
     CFG_64x64 = 2,          // 64x64x16, 4x4 per thread, 4 stages (small problems)
     CFG_64x64_SCALAR = 3,   // 64x64x16 with element-wise copies: any alignment
-    NUM_CONFIGS = 4,
+    CFG_32x32 = 4,          // 32x32x16, 4x4 per thread, 64 threads (tiny problems)
+    NUM_CONFIGS = 5,
 };
 
 struct ConfigInfo {

@@ -38,6 +38,11 @@ struct ConfigOf<CFG_64x64_SCALAR, TA, TB> {  // element-wise copies: any alignme
     using type = SimtCfg<64, 64, 16, 32, 16, 4, 4, 4, 2, TA, TB, false>;
 };
 
+template <int TA, int TB>
+struct ConfigOf<CFG_32x32, TA, TB> {  // 64 threads, 4 x 4 per thread: tiny problems
+    using type = SimtCfg<32, 32, 16, 32, 16, 4, 4, 4, 8, TA, TB, true>;
+};
+
 // Opt the kernel in to its dynamic shared memory once per device.
 template <class Cfg>
 static cudaError_t prepare_kernel()
@@ -92,6 +97,7 @@ static fgemm_status launch_simt(const GemmParams &p0, int batch, cudaStream_t st
         &launch_simt<ConfigOf<CFG_128x64, TA, TB>::type>,                  \
         &launch_simt<ConfigOf<CFG_64x64, TA, TB>::type>,                   \
         &launch_simt<ConfigOf<CFG_64x64_SCALAR, TA, TB>::type>,            \
+        &launch_simt<ConfigOf<CFG_32x32, TA, TB>::type>,                   \
     };
 
 }  // namespace fgemm
