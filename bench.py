@@ -352,24 +352,46 @@ def run_fgemm(args, rank, world, local_rank):
     peak, sms = stated_peak_tflops(dev)
     achieved = w.flops / (kernel_ms / 1e3) / 1e12
 
-    # End to end: pinned host inputs -> device, the call, result -> pinned host.
+    # End to end: every step copies its inputs from pinned host memory to the device,
+    # runs the library call and reads its result back into pinned host memory.  The
+    # steps are pipelined as a user would: three streams (host->device copies, the
+    # GEMM, device->host copies) and two device buffer sets, so the copies of one step
+    # overlap the GEMM of its neighbours.  The timed region runs from the first copy
+    # of the first timed step to the end of the last result read.
     hA, hB = w.A.pin_memory(), w.B.pin_memory()
-    hC = torch.empty(c_shape, dtype=torch.float32).pin_memory()
+    hC = [torch.empty(c_shape, dtype=torch.float32).pin_memory() for _ in range(2)]
     hC0 = w.C0.pin_memory() if w.C0 is not None else None
     h2d = hA.numel() * 4 + hB.numel() * 4 + (hC0.numel() * 4 if hC0 is not None else 0)
-    d2h = hC.numel() * 4
+    d2h = hC[0].numel() * 4
+    sets = [(dA, dB, dC), (torch.empty_like(dA), torch.empty_like(dB), torch.empty_like(dC))]
+    h2d_s, d2h_s = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        for it in range(args.e2e_steps + 2):
-            if it == 2:
-                e_start.record(stream)
-            dA.copy_(hA, non_blocking=True)
-            dB.copy_(hB, non_blocking=True)
+    torch.cuda.synchronize()
+    for it in range(args.e2e_steps + 2):
+        b = it % 2
+        xA, xB, xC = sets[b]
+        if it >= 2:  # buffers of step it-2: its result must have been read back
+            h2d_s.wait_event(ev_out[b])
+        if it == 2:
+            e_start.record(h2d_s)
+        with torch.cuda.stream(h2d_s):
+            xA.copy_(hA, non_blocking=True)
+            xB.copy_(hB, non_blocking=True)
             if hC0 is not None:
-                dC.copy_(hC0, non_blocking=True)
-            _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math, splitk)
-            hC.copy_(dC, non_blocking=True)
-        e_end.record(stream)
+                xC.copy_(hC0, non_blocking=True)
+        ev_in[b].record(h2d_s)
+        stream.wait_event(ev_in[b])
+        with torch.cuda.stream(stream):
+            _launch(fg, w, args.config, xA, xB, xC, dbias, sh, args.math, splitk)
+        ev_done[b].record(stream)
+        d2h_s.wait_event(ev_done[b])
+        with torch.cuda.stream(d2h_s):
+            hC[b].copy_(xC, non_blocking=True)
+        ev_out[b].record(d2h_s)
+    e_end.record(d2h_s)
     torch.cuda.synchronize()
     e2e_s = e_start.elapsed_time(e_end) / 1e3 / args.e2e_steps
     e2e_flops, e2e_max = aggregate(w.flops, e2e_s, world, dev if world > 1 else None)
