@@ -6,11 +6,12 @@ The CUDA library never calls it and shares no code with it.
 
 What it computes is the plain definition (see ``oracle.c`` for the citations):
 
-    C[i][j] = relu?( alpha * sum_k op(A)[i][k] * op(B)[k][j] + beta * C0[i][j] + bias[j] )
+    C[i][j] = relu?( alpha * sum_k op(A)[i][k] * op(B)[k][j] + beta * C0[i][j] + bias[j]
+                     + row_bias[i] )
 
 evaluated in double, one element at a time, with the k-sum in ascending order.
 Each call also returns ``mag[i][j] = |alpha| sum_k |op(A)[i][k]| |op(B)[k][j]|
-+ |beta| |C0[i][j]| + |bias[j]|``, the scale of the per-element bound used by
++ |beta| |C0[i][j]| + |bias[j]| + |row_bias[i]|``, the scale of the per-element bound used by
 the tests (the bound itself lives in the tests).
 
 The C source is compiled with gcc on first use (``build()``) into a shared
@@ -84,7 +85,7 @@ class Oracle:
         lib.oracle_gemm.argtypes = [
             ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
             ctypes.c_float, _f32p, ctypes.c_int64, _f32p, ctypes.c_int64, ctypes.c_float,
-            _f32p, ctypes.c_int64, _f32p, ctypes.c_int, _i64p, ctypes.c_int64,
+            _f32p, ctypes.c_int64, _f32p, _f32p, ctypes.c_int, _i64p, ctypes.c_int64,
             _f64p, _f64p, ctypes.c_int]
         lib.oracle_gemm_strided_batched.restype = ctypes.c_int
         lib.oracle_gemm_strided_batched.argtypes = [
@@ -96,15 +97,17 @@ class Oracle:
         self._lib = lib
 
     def gemm(self, ta, tb, M, N, K, alpha, A, lda, B, ldb, beta=0.0, C0=None, ldc=None,
-             bias=None, relu=False, rows=None, threads=None, want_mag=True):
+             bias=None, relu=False, rows=None, threads=None, want_mag=True, row_bias=None):
         """FP64 reference of one (possibly fused) row-major GEMM.
 
         ``A``, ``B``, ``C0`` are the flat float32 storage the leading dimensions
-        index into; ``ta``/``tb`` are 0 (no transpose) or 1 (transpose).
+        index into; ``ta``/``tb`` are 0 (no transpose) or 1 (transpose).  ``bias``
+        has one value per column (length N), ``row_bias`` one per row (length M).
         Returns ``(out, mag)`` as float64 arrays of shape ``(len(rows) or M, N)``
         (``mag`` is None when ``want_mag`` is false).
         """
         A, B, C0, bias = _as_f32(A), _as_f32(B), _as_f32(C0), _as_f32(bias)
+        row_bias = _as_f32(row_bias)
         ldc = N if ldc is None else ldc
         if rows is None:
             nrows, rows_arr, rptr = M, None, None
@@ -115,7 +118,7 @@ class Oracle:
         mag = np.zeros((nrows, N), dtype=np.float64) if want_mag else None
         rc = self._lib.oracle_gemm(
             int(ta), int(tb), M, N, K, float(alpha), _fptr(A), lda, _fptr(B), ldb, float(beta),
-            _fptr(C0), ldc, _fptr(bias), 1 if relu else 0, rptr, nrows,
+            _fptr(C0), ldc, _fptr(bias), _fptr(row_bias), 1 if relu else 0, rptr, nrows,
             out.ctypes.data_as(_f64p), mag.ctypes.data_as(_f64p) if mag is not None else None,
             int(threads or default_threads()))
         if rc != 0:

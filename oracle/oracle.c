@@ -13,7 +13,9 @@
  *   第5章-基础Kernel, "1.1 什么是矩阵乘法":       C[i][j] = sum_{k=0}^{K-1} A[i][k] * B[k][j]
  *       (0-based k, row-major storage, A[i*K + k] indexing as in "2. Naive 矩阵乘法实现").
  *   GEMM 优化详解, "Level 6: Kernel Fusion":      the fused layer adds bias[col] to every
- *       element of column col and then applies ReLU(x) = max(0, x).
+ *       element of column col and then applies ReLU(x) = max(0, x).  Reading for the
+ *       row-broadcast variant of that epilogue: row_bias[row] is added to every element
+ *       of row row, in the same place as bias[col].
  *
  * Readings where the pages are silent (each is listed in the design notes):
  *   - op(A) / op(B) with BLAS-style row-major transposes and leading dimensions:
@@ -21,8 +23,8 @@
  *       op(B)(k,j) = tb ? B[j*ldb + k] : B[k*ldb + j]
  *   - beta == 0: C0 is not read (it may hold NaN or be NULL).
  *   - alpha == 0 or K == 0: the product term is not formed and A, B are not read.
- *   - the fused order is relu(alpha*sum + beta*C0 + bias[j]); ReLU maps NaN to 0
- *     (the page's fmaxf(0, val)).
+ *   - the fused order is relu(alpha*sum + beta*C0 + bias[j] + row_bias[i]); ReLU maps
+ *     NaN to 0 (the page's fmaxf(0, val)).
  *
  * Arithmetic: every product of two floats is exact in double (24+24 < 53 bits),
  * the k-sum runs in ascending k exactly as written in the definition, and the
@@ -32,6 +34,7 @@
  *
  * Besides the value it returns, per element,
  *     mag(i,j) = |alpha| * sum_k |op(A)(i,k)| * |op(B)(k,j)| + |beta| * |C0(i,j)| + |bias[j]|
+ *                + |row_bias[i]|
  * which scales the per-element acceptance bound of the tests.
  *
  * Rows of the output are split over POSIX threads; the thread count is an
@@ -57,7 +60,8 @@ typedef struct {
     int64_t ldb;
     const float *C0;
     int64_t ldc;
-    const float *bias;
+    const float *bias;     /* length N, per column, or NULL */
+    const float *row_bias; /* length M, per row, or NULL */
     int relu;
     const int64_t *rows; /* NULL: all M rows */
     int64_t nrows;
@@ -126,6 +130,10 @@ static void one_row(const job_t *j, int64_t i, double *orow, double *mrow, doubl
             v += (double)j->bias[c];
             m += fabs((double)j->bias[c]);
         }
+        if (j->row_bias) {
+            v += (double)j->row_bias[i];
+            m += fabs((double)j->row_bias[i]);
+        }
         if (j->relu) v = (v > 0.0) ? v : 0.0;
         orow[c] = v;
         if (mrow) mrow[c] = m;
@@ -157,7 +165,7 @@ static void *worker(void *arg)
  */
 int oracle_gemm(int ta, int tb, int64_t M, int64_t N, int64_t K, float alpha,
                 const float *A, int64_t lda, const float *B, int64_t ldb, float beta,
-                const float *C0, int64_t ldc, const float *bias, int relu,
+                const float *C0, int64_t ldc, const float *bias, const float *row_bias, int relu,
                 const int64_t *rows, int64_t nrows, double *out, double *mag, int nthreads)
 {
     job_t base;
@@ -191,6 +199,7 @@ int oracle_gemm(int ta, int tb, int64_t M, int64_t N, int64_t K, float alpha,
     base.C0 = C0;
     base.ldc = ldc;
     base.bias = bias;
+    base.row_bias = row_bias;
     base.relu = relu ? 1 : 0;
     base.rows = rows;
     base.nrows = nrows;
@@ -248,7 +257,7 @@ int oracle_gemm_strided_batched(int ta, int tb, int64_t M, int64_t N, int64_t K,
     for (b = 0; b < batch; ++b) {
         const int rc = oracle_gemm(ta, tb, M, N, K, alpha, A ? A + b * strideA : NULL, lda,
                                    B ? B + b * strideB : NULL, ldb, beta,
-                                   C0 ? C0 + b * strideC : NULL, ldc, NULL, 0, NULL, M,
+                                   C0 ? C0 + b * strideC : NULL, ldc, NULL, NULL, 0, NULL, M,
                                    out + b * M * N, mag ? mag + b * M * N : NULL, nthreads);
         if (rc != ORACLE_OK) return rc;
     }

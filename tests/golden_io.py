@@ -10,7 +10,7 @@ import os
 import numpy as np
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-_MATS = {"A", "B", "C0", "bias", "expect", "mag"}
+_MATS = {"A", "B", "C0", "bias", "row_bias", "expect", "mag"}
 
 
 def load(name):
@@ -46,6 +46,7 @@ def load(name):
         for k in _MATS:
             if k in c:
                 c[k] = np.array(c[k], dtype=np.float64)
-        if "bias" in c:
-            c["bias"] = c["bias"].reshape(-1)
+        for k in ("bias", "row_bias"):
+            if k in c:
+                c[k] = c[k].reshape(-1)
     return cases

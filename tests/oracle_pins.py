@@ -26,7 +26,7 @@ COMBOS = list(itertools.product((0, 1), (0, 1)))
 
 
 def _run(orc, A_log, B_log, ta, tb, alpha=1.0, beta=0.0, C0=None, bias=None, relu=False,
-         pad=(0, 0, 0), fill=np.nan, **kw):
+         pad=(0, 0, 0), fill=np.nan, row_bias=None, **kw):
     """Call the oracle on logical operands stored with transposes and padded ld."""
     M, K = A_log.shape
     N = B_log.shape[1]
@@ -38,7 +38,8 @@ def _run(orc, A_log, B_log, ta, tb, alpha=1.0, beta=0.0, C0=None, bias=None, rel
     B = store(B_log, tb, ldb, fill) if K * N else None
     C0s = store(C0, 0, ldc, fill) if C0 is not None else None
     return orc.gemm(ta, tb, M, N, K, alpha, A, lda, B, ldb, beta, C0s, ldc,
-                    bias=None if bias is None else np.asarray(bias, np.float32), relu=relu, **kw)
+                    bias=None if bias is None else np.asarray(bias, np.float32), relu=relu,
+                    row_bias=None if row_bias is None else np.asarray(row_bias, np.float32), **kw)
 
 
 def _exact(got, want, what):
@@ -56,7 +57,8 @@ def pin_golden(orc):
             for ta, tb in COMBOS:
                 for pad in ((0, 0, 0), (3, 1, 2)):
                     out, mag = _run(orc, case["A"], case["B"], ta, tb, case["alpha"], case["beta"],
-                                    case.get("C0"), case.get("bias"), case["relu"], pad=pad)
+                                    case.get("C0"), case.get("bias"), case["relu"], pad=pad,
+                                    row_bias=case.get("row_bias"))
                     tag = "%s %s ta=%d tb=%d pad=%s" % (fname, case["name"], ta, tb, pad)
                     _exact(out, case["expect"], tag)
                     _exact(mag, case["mag"], tag + " mag")
@@ -262,6 +264,23 @@ def pin_fused_consistency(orc):
         _exact(fused, np.maximum(biased, 0.0), "relu(bias)")
         _exact(relu_only, np.maximum(plain, 0.0), "relu only")
         assert (fused == 0).any() and (fused > 0).any()
+
+
+def pin_row_bias_is_column_bias_of_the_transpose(orc):
+    """A bias per row of C is a bias per column of C^T = B^T A^T (and ReLU commutes)."""
+    rng = np.random.default_rng(17)
+    M, N, K = 9, 7, 12
+    A = rng.uniform(-1, 1, (M, K)).astype(np.float32)
+    B = rng.uniform(-1, 1, (K, N)).astype(np.float32)
+    r = rng.uniform(-1, 1, M).astype(np.float32)
+    for relu in (False, True):
+        out, mag = orc.gemm(0, 0, M, N, K, 1.0, A.reshape(-1), K, B.reshape(-1), N, row_bias=r,
+                            relu=relu)
+        outT, magT = orc.gemm(1, 1, N, M, K, 1.0, B.reshape(-1), N, A.reshape(-1), K, bias=r,
+                              relu=relu)
+        _exact(outT, out.T, "row bias vs column bias of the transpose")
+        _exact(magT, mag.T, "row bias mag")
+        assert (out != _run(orc, A, B, 0, 0, relu=relu)[0]).any()
 
 
 def pin_magnitude(orc):

@@ -34,6 +34,8 @@ MUTANTS = [
     ("float accumulation (dot path)", "double s = 0.0, m = 0.0;", "float s = 0.0f; double m = 0.0;"),
     ("mag beta term dropped", "m += fabs(j->beta) * fabs(c0);", "m += 0.0;"),
     ("mag bias term dropped", "m += fabs((double)j->bias[c]);", "m += 0.0;"),
+    ("row bias dropped", "v += (double)j->row_bias[i];", "v += 0.0;"),
+    ("row bias by column", "v += (double)j->row_bias[i];", "v += (double)j->row_bias[c < j->M ? c : 0];"),
     ("mag alpha dropped", "fabs(j->alpha) * mrow[c]", "mrow[c]"),
     ("selected rows ignored", "const int64_t i = j->rows ? j->rows[r] : r;", "const int64_t i = r;"),
     ("batch stride of B ignored", "B ? B + b * strideB : NULL", "B"),
