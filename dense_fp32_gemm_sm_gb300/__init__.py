@@ -27,6 +27,7 @@ from ._binding import (  # noqa: F401
     select_config,
     sgemm,
     sgemm_bias_relu,
+    sgemm_row_bias_relu,
     NOALLOC_SCRATCH_BYTES,
     sgemm_splitk,
     sgemm_splitk_noalloc,

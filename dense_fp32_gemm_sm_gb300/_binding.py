@@ -46,6 +46,9 @@ def library() -> ctypes.CDLL:
                 "fgemm_sgemm_bias_relu": [_c_int, _c_int, _c_int, _c_int, _c_int, _c_float, _c_vp,
                                           _c_int, _c_vp, _c_int, _c_float, _c_vp, _c_int, _c_vp,
                                           _c_int, _c_vp],
+                "fgemm_sgemm_row_bias_relu": [_c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                              _c_vp, _c_int, _c_vp, _c_int, _c_float, _c_vp,
+                                              _c_int, _c_vp, _c_int, _c_vp],
                 "fgemm_sgemm_strided_batched": [_c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                                 _c_vp, _c_int, _c_ll, _c_vp, _c_int, _c_ll,
                                                 _c_float, _c_vp, _c_int, _c_ll, _c_int, _c_vp],
@@ -150,6 +153,17 @@ def sgemm_bias_relu(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc
                                          1 if apply_relu else 0, _stream(stream, C, A, B))
     if check:
         _check(st, "fgemm_sgemm_bias_relu")
+    return st
+
+
+def sgemm_row_bias_relu(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, row_bias,
+                        apply_relu, stream=None, check=True) -> int:
+    """``fgemm_sgemm_row_bias_relu``: C = relu?(alpha*op(A)*op(B) + beta*C + row_bias[row])."""
+    st = library().fgemm_sgemm_row_bias_relu(int(transa), int(transb), M, N, K, alpha, _ptr(A),
+                                             lda, _ptr(B), ldb, beta, _ptr(C), ldc, _ptr(row_bias),
+                                             1 if apply_relu else 0, _stream(stream, C, A, B))
+    if check:
+        _check(st, "fgemm_sgemm_row_bias_relu")
     return st
 
 

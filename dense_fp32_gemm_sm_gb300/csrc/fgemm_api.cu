@@ -40,6 +40,7 @@ struct Problem {
     const float *bias;
     int relu;
     cudaStream_t stream;
+    const float *row_bias = nullptr;
 };
 
 long long floor_div(long long a, long long b)
@@ -125,6 +126,7 @@ fgemm_status run(int config, const Problem &p)
     g.B = products ? p.B : nullptr;
     g.C = p.C;
     g.bias = p.bias;
+    g.row_bias = p.row_bias;
     g.lda = p.lda;
     g.ldb = p.ldb;
     g.ldc = p.ldc;
@@ -214,6 +216,7 @@ fgemm_status run_splitk(const Problem &p, int splits, float *W, size_t ws_bytes)
     q.alpha = 1.0f;
     q.beta = 0.0f;
     q.bias = nullptr;
+    q.row_bias = nullptr;
     q.relu = 0;
     q.C = W;
     q.ldc = p.N;
@@ -291,6 +294,17 @@ fgemm_status fgemm_sgemm_bias_relu(fgemm_op transa, fgemm_op transb, int M, int 
 {
     return run(-1, make_problem(transa, transb, M, N, K, alpha, A, lda, 0, B, ldb, 0, beta, C, ldc,
                                 0, 1, bias, apply_relu, stream));
+}
+
+fgemm_status fgemm_sgemm_row_bias_relu(fgemm_op transa, fgemm_op transb, int M, int N, int K,
+                                       float alpha, const float *A, int lda, const float *B,
+                                       int ldb, float beta, float *C, int ldc,
+                                       const float *row_bias, int apply_relu, cudaStream_t stream)
+{
+    fgemm::Problem p = make_problem(transa, transb, M, N, K, alpha, A, lda, 0, B, ldb, 0, beta, C,
+                                    ldc, 0, 1, nullptr, apply_relu, stream);
+    p.row_bias = row_bias;
+    return run(-1, p);
 }
 
 fgemm_status fgemm_sgemm_strided_batched(fgemm_op transa, fgemm_op transb, int M, int N, int K,

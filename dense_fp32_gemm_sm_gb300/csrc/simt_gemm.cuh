@@ -26,7 +26,8 @@
 //    loads.  Each a[i] is duplicated into a register pair once per k.
 //
 //  * Epilogue in registers (GEMM 优化详解, "Level 6: Kernel Fusion" and "Level 7:
-//    Vectorized Loads"): v = alpha*acc (+ beta*C) (+ bias[col]), ReLU, then float4
+//    Vectorized Loads"): v = alpha*acc (+ beta*C) (+ bias[col]) (+ row_bias[row]),
+//    ReLU, then float4
 //    stores when C is 16-byte aligned, scalar stores otherwise.
 //
 //  * Tiles are visited in groups of GROUP_M tile-rows so that concurrently
@@ -42,7 +43,8 @@ struct GemmParams {
     const float *A;
     const float *B;
     float *C;
-    const float *bias;
+    const float *bias;      // one value per column (length N), or null
+    const float *row_bias;  // one value per row (length M), or null
     long long lda, ldb, ldc;
     long long strideA, strideB, strideC;
     int M, N, K;  // K is 0 when no products are formed (K == 0 or alpha == 0)
@@ -409,6 +411,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
         const int gr = m0 + frag_row<Cfg>(wm0, lr, i);
         if (gr >= p.M) continue;
         float *const crow = C + (long long)gr * p.ldc;
+        const float rb = p.row_bias != nullptr ? __ldg(p.row_bias + gr) : 0.0f;
 #pragma unroll
         for (int g = 0; g < TN / 4; ++g) {
             const int gc = n0 + frag_col<Cfg>(wn0, lc, 4 * g);
@@ -428,6 +431,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     v[e] += bias_v[4 * g + e];
+                    v[e] += rb;
                     if (p.relu) v[e] = fmaxf(v[e], 0.0f);
                 }
                 *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
@@ -438,6 +442,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
                     float o = v[e];
                     if (p.beta != 0.0f) o = fmaf(p.beta, dst[e], o);
                     o += bias_v[4 * g + e];
+                    o += rb;
                     if (p.relu) o = fmaxf(o, 0.0f);
                     dst[e] = o;
                 }

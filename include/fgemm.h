@@ -78,6 +78,18 @@ fgemm_status fgemm_sgemm_bias_relu(fgemm_op transa, fgemm_op transb, int M, int 
                                    int apply_relu, cudaStream_t stream);
 
 /*
+ * The same fused epilogue with a bias per output ROW (row-broadcast bias):
+ *     C[i][j] = act( alpha * sum_k op(A)[i][k] op(B)[k][j] + beta * C[i][j] + row_bias[i] )
+ * (the per-column bias of GEMM 优化详解, "Level 6: Kernel Fusion", broadcast the other
+ * way, e.g. a per-query term added to attention scores).  row_bias: device vector of
+ * M floats, or NULL; apply_relu as above.  Runs on the CUDA cores.
+ */
+fgemm_status fgemm_sgemm_row_bias_relu(fgemm_op transa, fgemm_op transb, int M, int N, int K,
+                                       float alpha, const float *A, int lda, const float *B,
+                                       int ldb, float beta, float *C, int ldc,
+                                       const float *row_bias, int apply_relu, cudaStream_t stream);
+
+/*
  * Strided batch: for b in [0, batch), the plain GEMM on A + b*strideA,
  * B + b*strideB, C + b*strideC (strides in elements).  Used for batched
  * attention scores Q x K^T (GEMM 优化详解, "为什么 GEMM 重要？", and the

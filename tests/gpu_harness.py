@@ -9,7 +9,8 @@ Acceptance, per output element (fixed by the FP32 accuracy requirement of the
 method; the K in "1e-5 * K * sum|A||B| / K" cancels):
     integer-valued inputs:  bit-exact (every partial sum is an integer < 2^24)
     otherwise:              |C - C_ref| <= 1e-5 * mag + FLT_MIN
-with mag = |alpha| sum_k |a_ik||b_kj| + |beta||c_ij| + |bias_j| from the oracle.
+with mag = |alpha| sum_k |a_ik||b_kj| + |beta||c_ij| + |bias_j| + |row_bias_i| from the
+oracle.
 Elements of C outside the M x N region must come back unchanged.
 """
 
@@ -48,6 +49,7 @@ class Case:
     math: int = -1  # >= 0: call fgemm_gemm_math with this arithmetic instead of gemm_explicit
     c_nan: bool = False  # fill the initial C with NaN (only meaningful for beta == 0)
     a_nan: bool = False  # fill A with NaN (only meaningful for alpha == 0)
+    row_bias: bool = False  # call fgemm_sgemm_row_bias_relu with a per-row bias (single GEMM)
 
 
 def _draw(g, shape, ints):
@@ -97,13 +99,20 @@ def run(case: Case):
     if case.a_nan:
         A[:] = np.nan
     bias = _draw(g, (N,), True).astype(np.float32) if case.bias else None
+    row_bias = _draw(g, (M,), True).astype(np.float32) if case.row_bias else None
+    if row_bias is not None:
+        assert case.batch == 0 and case.math < 0 and case.config < 0 and bias is None
 
     dA, pA = _device(A, case.offset[0])
     dB, pB = _device(B, case.offset[1])
     dC, pC = _device(C0, case.offset[2])
     dbias, pbias = _device(bias, 0) if bias is not None else (None, None)
+    drow, prow = _device(row_bias, 0) if row_bias is not None else (None, None)
     stream = torch.cuda.current_stream().cuda_stream
-    if case.math >= 0:
+    if row_bias is not None:
+        fg.sgemm_row_bias_relu(case.ta, case.tb, M, N, K, case.alpha, pA, lda, pB, ldb, case.beta,
+                               pC, ldc, prow, case.relu, stream=stream)
+    elif case.math >= 0:
         fg.gemm_math(case.math, case.ta, case.tb, M, N, K, case.alpha, pA, lda, sA, pB, ldb, sB,
                      case.beta, pC, ldc, sC, nb, pbias, case.relu, stream=stream)
     else:
@@ -120,7 +129,7 @@ def run(case: Case):
     for b in range(nb):
         o, m = oracle.gemm(case.ta, case.tb, M, N, K, case.alpha, A[b * sA:], lda, B[b * sB:],
                            ldb, case.beta, C0[b * sC:] if case.beta != 0 else None, ldc,
-                           bias=bias, relu=case.relu)
+                           bias=bias, relu=case.relu, row_bias=row_bias)
         want[b], mag[b] = o, m
         for r in range(M):
             got[b, r] = Cout[b * sC + r * ldc: b * sC + r * ldc + N]

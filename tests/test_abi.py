@@ -157,3 +157,12 @@ def test_splitk_rejects_missing_workspace_before_launch():
     assert fg.sgemm_splitk(*args, 65, FAKE, need, check=False) == fg.ERR_INVALID_VALUE
     bad_ld = (0, 0, 64, 64, 256, 1.0, FAKE, 255, FAKE, 64, 0.0, FAKE, 64, None, 0)
     assert fg.sgemm_splitk(*bad_ld, 4, FAKE, need, check=False) == fg.ERR_INVALID_VALUE
+
+
+@pytest.mark.parametrize("kw", [dict(M=-1), dict(ldc=3), dict(transa=1, M=8, lda=7), dict(C=None)])
+def test_row_bias_entry_validates_before_launch(kw):
+    args = dict(transa=0, transb=0, M=4, N=4, K=4, alpha=1.0, A=FAKE, lda=4, B=FAKE, ldb=4,
+                beta=0.0, C=FAKE, ldc=4, row_bias=FAKE, apply_relu=True)
+    assert fg.sgemm_row_bias_relu(**dict(args, M=0), check=False) == fg.OK
+    args.update(kw)
+    assert fg.sgemm_row_bias_relu(**args, check=False) == fg.ERR_INVALID_VALUE
