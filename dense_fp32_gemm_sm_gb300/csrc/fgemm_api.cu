@@ -23,6 +23,7 @@ const ConfigInfo kConfigs[NUM_CONFIGS] = {
     {"simt_64x64x16_t4x4_s4", 64, 64, true},
     {"simt_64x64x16_t4x4_s4_scalar", 64, 64, false},
     {"simt_32x32x16_t4x4_s4", 32, 32, true},
+    {"simt_32x32x32_t4x4_s8_k4", 32, 32, true},
 };
 
 namespace {
@@ -142,6 +143,7 @@ fgemm_status run(int config, const Problem &p)
     g.c_vec = aligned16(p.C, p.ldc, p.sC, p.batch) ? 1 : 0;
 
     const LaunchFn *table = p.ta ? (p.tb ? kLaunchTT : kLaunchTN) : (p.tb ? kLaunchNT : kLaunchNN);
+    if (table[config] == nullptr) return FGEMM_ERR_NOT_SUPPORTED;
     return table[config](g, p.batch, p.stream);
 }
 

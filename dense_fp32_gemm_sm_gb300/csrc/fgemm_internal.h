@@ -21,7 +21,9 @@ enum ConfigId {
     CFG_64x64 = 2,          // 64x64x16, 4x4 per thread, 4 stages (small problems)
     CFG_64x64_SCALAR = 3,   // 64x64x16 with element-wise copies: any alignment
     CFG_32x32 = 4,          // 32x32x16, 4x4 per thread, 64 threads (tiny problems)
-    NUM_CONFIGS = 5,
+    CFG_32x32_K4 = 5,       // 32x32x32, 4x4 per thread, four k-groups of 2 warps, 8 stages
+                            // (the smallest grids: a quarter of the serial k-steps per thread)
+    NUM_CONFIGS = 6,
 };
 
 struct ConfigInfo {

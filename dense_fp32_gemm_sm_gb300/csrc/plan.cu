@@ -35,6 +35,10 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
     // Tiny problems are latency-bound: more, smaller CTAs finish sooner (256^3: 8.2 us
     // with 32 x 32 tiles against 12.4 us with 64 x 64).
     if (ceil_div(M, 64) * ceil_div(N, 64) * b >= num_sms) return CFG_64x64;
+    // Up to about two 32 x 32 tiles per SM, four k-groups per tile shorten the serial
+    // chain (512^3, 256 tiles: 14.4 us against 16.4 back to back); beyond that the
+    // one-group tile wins (768^3, 576 tiles: 35.5 us against 39.6).
+    if (ceil_div(M, 32) * ceil_div(N, 32) * b <= 2LL * num_sms) return CFG_32x32_K4;
     return CFG_32x32;
 }
 

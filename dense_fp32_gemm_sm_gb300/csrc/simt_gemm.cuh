@@ -107,6 +107,13 @@ __device__ __forceinline__ unsigned long long dup_pair(float a)
     return d;
 }
 
+__device__ __forceinline__ unsigned long long make_pair(float lo, float hi)
+{
+    unsigned long long d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
+    return d;
+}
+
 __device__ __forceinline__ float pair_lo(unsigned long long v) { return __uint_as_float((unsigned)v); }
 __device__ __forceinline__ float pair_hi(unsigned long long v)
 {
@@ -116,24 +123,35 @@ __device__ __forceinline__ float pair_hi(unsigned long long v)
 // ---- Configuration -------------------------------------------------------------
 
 template <int BM_, int BN_, int BK_, int WM_, int WN_, int TM_, int TN_, int STAGES_, int MINB_,
-          int TA_, int TB_, bool VEC_>
+          int TA_, int TB_, bool VEC_, int KS_ = 1>
 struct SimtCfg {
     static constexpr int BM = BM_, BN = BN_, BK = BK_;
     static constexpr int WM = WM_, WN = WN_, TM = TM_, TN = TN_;
     static constexpr int STAGES = STAGES_, MINB = MINB_;
     static constexpr int TA = TA_, TB = TB_;
     static constexpr bool VEC = VEC_;
+    // KS groups of warps share the CTA tile: group g multiplies k-columns
+    // [g*KB, (g+1)*KB) of every stage into its own accumulators, and the groups'
+    // sums are added through shared memory before the epilogue.  More warps per
+    // tile, fewer serial k-steps per thread: for problems with too few tiles to
+    // keep every SM busy.
+    static constexpr int KS = KS_;
+    static constexpr int KB = BK / KS;
     static constexpr int WARPS_M = BM / WM, WARPS_N = BN / WN;
-    static constexpr int THREADS = 32 * WARPS_M * WARPS_N;
+    static constexpr int GROUP_THREADS = 32 * WARPS_M * WARPS_N;
+    static constexpr int THREADS = GROUP_THREADS * KS;
     static constexpr int LR = WM / TM;  // lanes along M
     static constexpr int LC = WN / TN;  // lanes along N
     static constexpr int A_LD = BM + 4;  // sA[k][m]; +4 floats keeps transposed writes conflict-free
     static constexpr int B_LD = BN + 4;  // sB[k][n]
     static constexpr int A_STAGE = BK * A_LD;
     static constexpr int B_STAGE = BK * B_LD;
-    static constexpr int SMEM_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
+    static constexpr int STAGE_BYTES = STAGES * (A_STAGE + B_STAGE) * 4;
+    static constexpr int RED_BYTES = (KS - 1) * GROUP_THREADS * TM * TN * 4;
+    static constexpr int SMEM_BYTES = STAGE_BYTES > RED_BYTES ? STAGE_BYTES : RED_BYTES;
     static constexpr int GROUP_M = 8;
 
+    static_assert(BK % KS == 0 && KB % 2 == 0, "each k-group takes an even number of k per stage");
     static_assert(LR * LC == 32, "a warp is LR x LC lanes");
     static_assert(BM % WM == 0 && BN % WN == 0, "warp tiles must cover the CTA tile");
     static_assert(TM % 4 == 0 && TN % 4 == 0, "16-byte fragments");
@@ -300,8 +318,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    const int kg = warp / (Cfg::WARPS_M * Cfg::WARPS_N);  // k-group of this warp
+    const int wg = warp % (Cfg::WARPS_M * Cfg::WARPS_N);  // warp within its group
     const int lr = lane / Cfg::LC, lc = lane % Cfg::LC;
-    const int wm0 = (warp / Cfg::WARPS_N) * Cfg::WM, wn0 = (warp % Cfg::WARPS_N) * Cfg::WN;
+    const int wm0 = (wg / Cfg::WARPS_N) * Cfg::WM, wn0 = (wg % Cfg::WARPS_N) * Cfg::WN;
+    const int kb0 = kg * Cfg::KB;  // first k of a stage this group multiplies
 
     // Grouped tile order: GROUP_M consecutive tile-rows are swept column by column.
     int tile_m, tile_n;
@@ -355,22 +376,22 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
             for (int g = 0; g < TN / 4; ++g)
                 fb[buf][g] = *reinterpret_cast<const float4 *>(b + frag_col<Cfg>(wn0, lc, 4 * g));
         };
-        load_frag(0, 0, 0);
+        load_frag(0, 0, kb0);
 
         int slot = 0;
         for (int kt = 0; kt < KT; ++kt) {
 #pragma unroll
-            for (int k = 0; k < Cfg::BK; ++k) {
+            for (int k = 0; k < Cfg::KB; ++k) {
                 const int cur = k & 1;
-                if (k == Cfg::BK - 1) {
+                if (k == Cfg::KB - 1) {
                     // Stage kt+1 must have landed, and every thread must be done with
                     // the slot the next copy overwrites.
                     cp_async_wait<Cfg::STAGES - 2>();
                     __syncthreads();
                     slot = (slot + 1 == Cfg::STAGES) ? 0 : slot + 1;
-                    if (kt + 1 < KT) load_frag(cur ^ 1, slot, 0);
+                    if (kt + 1 < KT) load_frag(cur ^ 1, slot, kb0);
                 } else {
-                    load_frag(cur ^ 1, slot, k + 1);
+                    load_frag(cur ^ 1, slot, kb0 + k + 1);
                 }
                 if (k == 0) {
                     const int nk = kt + Cfg::STAGES - 1;
@@ -398,20 +419,55 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
         cp_async_wait<0>();
     }
 
+    // ---- K-groups: groups 1.. hand their sums to group 0 through shared memory
+    // (the stage buffers are free once every warp has passed the barrier), in
+    // group order, so the result does not depend on timing.
+    if constexpr (Cfg::KS > 1) {
+        if (KT > 0) {
+            constexpr int E = TM * TN / 2;  // accumulator pairs per thread
+            unsigned long long *const red = reinterpret_cast<unsigned long long *>(smem);
+            const int gt = tid - kg * Cfg::GROUP_THREADS;
+            __syncthreads();
+            if (kg > 0) {
+#pragma unroll
+                for (int i = 0; i < TM; ++i)
+#pragma unroll
+                    for (int j = 0; j < TN / 2; ++j)
+                        red[((kg - 1) * E + i * (TN / 2) + j) * Cfg::GROUP_THREADS + gt] = acc[i][j];
+            }
+            __syncthreads();
+            if (kg == 0) {
+#pragma unroll
+                for (int g = 1; g < Cfg::KS; ++g)
+#pragma unroll
+                    for (int i = 0; i < TM; ++i)
+#pragma unroll
+                        for (int j = 0; j < TN / 2; ++j) {
+                            const unsigned long long r =
+                                red[((g - 1) * E + i * (TN / 2) + j) * Cfg::GROUP_THREADS + gt];
+                            acc[i][j] = make_pair(pair_lo(acc[i][j]) + pair_lo(r),
+                                                  pair_hi(acc[i][j]) + pair_hi(r));
+                        }
+            }
+        }
+        if (kg != 0) return;
+    }
+
     // ---- Epilogue: alpha, beta, bias, ReLU in registers; vector stores where possible.
     const bool products = KT > 0;
+    const bool has_bias = p.bias != nullptr, has_row_bias = p.row_bias != nullptr;
     float bias_v[TN];
 #pragma unroll
     for (int j = 0; j < TN; ++j) {
         const int gc = n0 + frag_col<Cfg>(wn0, lc, j);
-        bias_v[j] = (p.bias != nullptr && gc < p.N) ? __ldg(p.bias + gc) : 0.0f;
+        bias_v[j] = (has_bias && gc < p.N) ? __ldg(p.bias + gc) : 0.0f;
     }
 #pragma unroll
     for (int i = 0; i < TM; ++i) {
         const int gr = m0 + frag_row<Cfg>(wm0, lr, i);
         if (gr >= p.M) continue;
         float *const crow = C + (long long)gr * p.ldc;
-        const float rb = p.row_bias != nullptr ? __ldg(p.row_bias + gr) : 0.0f;
+        const float rb = has_row_bias ? __ldg(p.row_bias + gr) : 0.0f;
 #pragma unroll
         for (int g = 0; g < TN / 4; ++g) {
             const int gc = n0 + frag_col<Cfg>(wn0, lc, 4 * g);
@@ -430,8 +486,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    v[e] += bias_v[4 * g + e];
-                    v[e] += rb;
+                    if (has_bias) v[e] += bias_v[4 * g + e];
+                    if (has_row_bias) v[e] += rb;
                     if (p.relu) v[e] = fmaxf(v[e], 0.0f);
                 }
                 *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
@@ -441,8 +497,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
                     if (gc + e >= p.N) break;
                     float o = v[e];
                     if (p.beta != 0.0f) o = fmaf(p.beta, dst[e], o);
-                    o += bias_v[4 * g + e];
-                    o += rb;
+                    if (has_bias) o += bias_v[4 * g + e];
+                    if (has_row_bias) o += rb;
                     if (p.relu) o = fmaxf(o, 0.0f);
                     dst[e] = o;
                 }

@@ -112,7 +112,8 @@ def test_selector():
     big = sel(0, 0, 4096, 4096, 4096, 1, 1, 152)
     assert fg.config_name(big).startswith("simt_128x128")
     small = sel(0, 0, 256, 256, 256, 1, 1, 152)
-    assert not fg.config_name(small).endswith("_scalar")
+    assert fg.config_name(small) == "simt_32x32x32_t4x4_s8_k4"
+    assert fg.config_name(sel(0, 0, 768, 768, 768, 1, 1, 152)) == "simt_32x32x16_t4x4_s4"
     # a batch of small problems fills the GPU with the large tile
     assert sel(0, 1, 2048, 2048, 128, 128, 1, 152) == big
     assert sel(0, 0, -1, 4, 4, 1, 1, 152) == -1

@@ -20,7 +20,8 @@ SHAPES = [
     (1600, 1600, 40, 0, "simt_128x128_t8x8"),
     (1024, 1000, 40, 0, "simt_128x64x16_t8x8_s4"),
     (832, 840, 36, 0, "simt_64x64x16_t4x4_s4"),
-    (100, 70, 33, 0, "simt_32x32x16_t4x4_s4"),
+    (640, 640, 24, 0, "simt_32x32x16_t4x4_s4"),
+    (100, 70, 33, 0, "simt_32x32x32_t4x4_s8_k4"),
     (130, 77, 45, 1, "simt_64x64x16_t4x4_s4_scalar"),
 ]
 
