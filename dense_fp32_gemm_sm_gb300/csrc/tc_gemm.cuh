@@ -52,7 +52,7 @@ constexpr int UMMA_K = 8;                   // K of one kind::tf32 MMA (32 bytes
 constexpr int TILE_A_BYTES = BM * BK * 4;   // 16 KB
 constexpr int TILE_B_BYTES = BN * BK * 4;   // 16 KB
 constexpr int THREADS = 320;               // 10 warps, see the kernel
-constexpr uint32_t TMEM_COLS = 2 * BN;      // two FP32 accumulators of 128 lanes x BN columns
+constexpr uint32_t ACC_COLS = 2 * BN;       // two FP32 accumulators of 128 lanes x BN columns
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // default: 4 s per wait
 
 // Error bits recorded in the device error word.
@@ -215,6 +215,21 @@ __device__ __forceinline__ void umma_tf32(uint32_t tmem_d, uint64_t adesc, uint6
         : "memory");
 }
 
+// The same MMA with the A operand read from tensor memory (128 lanes = rows of A,
+// one 32-bit column per element along K) instead of shared memory.
+__device__ __forceinline__ void umma_tf32_tmem_a(uint32_t tmem_d, uint32_t tmem_a, uint64_t bdesc,
+                                                 uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n"
+        "}\n" ::"r"(tmem_d),
+        "r"(tmem_a), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -239,6 +254,24 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&r)[32]
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
+
+// Store 32 consecutive columns of this thread's tensor-memory lane (warp-wide: lane i
+// of the warp writes lane base + i); complete before return.
+__device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // hi = x with the 13 low mantissa bits cleared (a TF32 value); lo = x - hi, exact.
 __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo)
@@ -317,6 +350,69 @@ __device__ __forceinline__ bool transpose_mnmajor(uint8_t *tile, uint8_t *lo, in
     return true;
 }
 
+// MN-major tile -> tensor memory, for the A operand of the MMA: tile row r (one m,
+// or one n) becomes tensor-memory lane r, k its column.  TMA wrote the tile as 32 rows
+// of k, 128 floats each; thread r (lane r of the tile, in the 32-lane quarter its warp
+// may access) reads column r of that -- a warp reads 128 consecutive bytes per k, no
+// bank conflict -- so the transpose happens in registers, and shared memory sees one
+// read of the tile instead of a read and a write.  3xTF32: hi and lo go to two
+// column ranges.
+template <bool SPLIT>
+__device__ __forceinline__ void mnmajor_to_tmem(const uint8_t *tile, int r, uint32_t t_hi,
+                                                uint32_t t_lo)
+{
+    const float *src = reinterpret_cast<const float *>(tile) + r;
+    uint32_t h[32];
+    if constexpr (SPLIT) {
+        uint32_t l[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            float hi, lo;
+            split_tf32(src[k * 128], hi, lo);
+            h[k] = __float_as_uint(hi);
+            l[k] = __float_as_uint(lo);
+        }
+        tmem_st_32cols(t_hi, h);
+        tmem_st_32cols(t_lo, l);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 32; ++k) h[k] = __float_as_uint(src[k * 128]);
+        tmem_st_32cols(t_hi, h);
+    }
+    tmem_st_wait();
+}
+
+// K-major tile (canonical 128-byte swizzled layout) -> tensor memory: thread r reads
+// row r (eight 16-byte chunks; a warp's loads of one chunk index cover all 32 banks)
+// into tensor-memory lane r, k as its column.  3xTF32: hi and lo go to two column
+// ranges.
+template <bool SPLIT>
+__device__ __forceinline__ void kmajor_to_tmem(const uint8_t *tile, int r, uint32_t t_hi,
+                                               uint32_t t_lo)
+{
+    uint32_t h[32];
+    uint32_t l[SPLIT ? 32 : 1];
+#pragma unroll
+    for (int kq = 0; kq < 8; ++kq) {
+        const float4 v = *reinterpret_cast<const float4 *>(tile + kmajor_offset(r, kq));
+        const float x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            if constexpr (SPLIT) {
+                float hi, lo;
+                split_tf32(x[e], hi, lo);
+                h[4 * kq + e] = __float_as_uint(hi);
+                l[4 * kq + e] = __float_as_uint(lo);
+            } else {
+                h[4 * kq + e] = __float_as_uint(x[e]);
+            }
+        }
+    }
+    tmem_st_32cols(t_hi, h);
+    if constexpr (SPLIT) tmem_st_32cols(t_lo, reinterpret_cast<const uint32_t (&)[32]>(l));
+    tmem_st_wait();
+}
+
 // ---- The kernel ------------------------------------------------------------------
 
 // MODE: MODE_TF32 or MODE_3XTF32.  TA = 0: A stored M x K (K-major), 1: K x M.
@@ -330,6 +426,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     constexpr bool A_K = TA == 0, B_K = TB == 1;
     constexpr bool THREE = MODE == MODE_3XTF32;
     constexpr bool CONVERT = THREE || !A_K || !B_K;  // warps 2-5 touch each stage
+    // One operand goes to tensor memory as the MMA's A operand, written there from
+    // registers by warps 2-5 (transposed on the way when it is stored MN-major, split
+    // into hi and lo in 3xTF32), so the tensor core reads only the other operand from
+    // shared memory:
+    //   A stored K x M (TA = 1), or any 3xTF32 layout but NN: A goes to tensor memory;
+    //   A stored M x K and B stored K x N (NN): B goes, the MMA's B operand is A and the
+    //   MMA computes the transposed tile D = C^T (lanes are columns of C);
+    //   TF32 with both operands K-major (NT): neither, the TMA tiles feed the MMA as is.
+    constexpr bool B_VIA_TMEM = A_K && !B_K;
+    constexpr bool A_VIA_TMEM = !B_VIA_TMEM && (THREE || !A_K);
+    constexpr bool TMEM_OP = A_VIA_TMEM || B_VIA_TMEM;
+    constexpr bool TRANS_OUT = B_VIA_TMEM;
+    // Tensor-memory columns: the two accumulators, then per stage 32 columns of the
+    // MMA's A operand (64 in 3xTF32: hi, lo).
+    constexpr uint32_t OP_COLS = THREE ? 64 : 32;
+    constexpr uint32_t TMEM_COLS = TMEM_OP ? 512 : ACC_COLS;
+    static_assert(!TMEM_OP || ACC_COLS + S * OP_COLS <= TMEM_COLS, "tensor-memory columns");
     // Without a split or transpose, warps 2-5 share the epilogue with warps 6-9.
     constexpr int EPI_WARPS = CONVERT ? 4 : 8;
     constexpr int EPI_COLS = BN * 4 / EPI_WARPS;  // columns of a tile per epilogue warp
@@ -456,20 +569,35 @@ __global__ void __launch_bounds__(THREADS, 1)
                                  : mbar_wait(full_bar(s), round & 1, err, ERR_MMA_WAIT, lim);
                     if (!ok) break;
                     tc_fence_after();
+                    if constexpr (TMEM_OP) {
+                        // A operand in tensor memory; B operand = the other (K-major) tile.
+                        const uint32_t at = tmem + ACC_COLS + (uint32_t)s * OP_COLS;
+                        const int kop = B_VIA_TMEM ? a_off(s) : b_off(s);
+                        const int kop_lo = B_VIA_TMEM ? alo_off(s) : blo_off(s);
+                        const uint64_t bd = kmajor_sw128_desc(sbase + kop);
+#pragma unroll
+                        for (int k = 0; k < BK / UMMA_K; ++k) {
+                            const uint64_t koff = (uint64_t)((k * UMMA_K * 4) >> 4);
+                            const uint32_t ak = at + (uint32_t)(k * UMMA_K);
+                            if constexpr (THREE) {
+                                const uint64_t bld = kmajor_sw128_desc(sbase + kop_lo);
+                                umma_tf32_tmem_a(d, ak + 32u, bd + koff, idesc, (kb | k) != 0);
+                                umma_tf32_tmem_a(d, ak, bld + koff, idesc, 1u);
+                                umma_tf32_tmem_a(d, ak, bd + koff, idesc, 1u);
+                            } else {
+                                umma_tf32_tmem_a(d, ak, bd + koff, idesc, (kb | k) != 0);
+                            }
+                        }
+                        umma_commit(empty_bar(s));
+                        continue;
+                    }
+                    // TF32 with both operands K-major: the TMA tiles feed the MMA.
                     const uint64_t ad = kmajor_sw128_desc(sbase + a_off(s));
                     const uint64_t bd = kmajor_sw128_desc(sbase + b_off(s));
 #pragma unroll
                     for (int k = 0; k < BK / UMMA_K; ++k) {
                         const uint64_t koff = (uint64_t)((k * UMMA_K * 4) >> 4);  // 32 bytes per step
-                        if constexpr (THREE) {
-                            const uint64_t ald = kmajor_sw128_desc(sbase + alo_off(s));
-                            const uint64_t bld = kmajor_sw128_desc(sbase + blo_off(s));
-                            umma_tf32(d, ald + koff, bd + koff, idesc, (kb | k) != 0);
-                            umma_tf32(d, ad + koff, bld + koff, idesc, 1u);
-                            umma_tf32(d, ad + koff, bd + koff, idesc, 1u);
-                        } else {
-                            umma_tf32(d, ad + koff, bd + koff, idesc, (kb | k) != 0);
-                        }
+                        umma_tf32(d, ad + koff, bd + koff, idesc, (kb | k) != 0);
                     }
                     umma_commit(empty_bar(s));  // the stage is free once these MMAs have read it
                 }
@@ -482,9 +610,12 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
         }
     } else if (CONVERT && warp < 6) {
-        // ---- warps 2..5: split / transpose every stage ----
+        // ---- warps 2..5: each stage's tensor-memory operand, and the split or
+        // transpose of the shared-memory operand ----
         if constexpr (CONVERT) {
+            static_assert(TMEM_OP, "every converted layout routes one operand through tensor memory");
             const int t = threadIdx.x - 64;  // 0..127
+            const int r = 32 * (warp & 3) + lane;  // the tensor-memory lane this thread writes
             int g = 0, transposes = 0;
             bool ok = true;
             for (long long tl = blockIdx.x; ok && tl < total_tiles; tl += gridDim.x) {
@@ -492,28 +623,36 @@ __global__ void __launch_bounds__(THREADS, 1)
                     const int s = g % S, round = g / S;
                     ok = mbar_wait(full_bar(s), round & 1, err, ERR_SPLIT_WAIT, lim);
                     if (!ok) break;
-                    if constexpr (A_K) {
+                    // The tensor-memory operand (this stage's columns are free: the copy
+                    // that just landed was issued only after the MMAs of the stage's
+                    // previous round had completed) ...
+                    const uint32_t t_hi = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + ACC_COLS +
+                                          (uint32_t)s * OP_COLS;
+                    if constexpr (B_VIA_TMEM)
+                        mnmajor_to_tmem<THREE>(smem + b_off(s), r, t_hi, t_hi + 32u);
+                    else if constexpr (A_K)
+                        kmajor_to_tmem<THREE>(smem + a_off(s), r, t_hi, t_hi + 32u);
+                    else
+                        mnmajor_to_tmem<THREE>(smem + a_off(s), r, t_hi, t_hi + 32u);
+                    // ... and the shared-memory operand: split, or transpose (and split).
+                    if constexpr (B_VIA_TMEM) {
                         if constexpr (THREE)
                             split_kmajor(reinterpret_cast<float4 *>(smem + a_off(s)),
                                          reinterpret_cast<float4 *>(smem + alo_off(s)), t);
-                    } else {
-                        ok = transpose_mnmajor<THREE>(smem + a_off(s), smem + alo_off(s), t,
-                                                      read_bar, transposes & 1, err, lim);
-                        ++transposes;
-                    }
-                    if (!ok) break;
-                    if constexpr (B_K) {
-                        if constexpr (THREE)
-                            split_kmajor(reinterpret_cast<float4 *>(smem + b_off(s)),
-                                         reinterpret_cast<float4 *>(smem + blo_off(s)), t);
-                    } else {
+                    } else if constexpr (!B_K) {
                         ok = transpose_mnmajor<THREE>(smem + b_off(s), smem + blo_off(s), t,
                                                       read_bar, transposes & 1, err, lim);
                         ++transposes;
+                        if (!ok) break;
+                    } else if constexpr (THREE) {
+                        split_kmajor(reinterpret_cast<float4 *>(smem + b_off(s)),
+                                     reinterpret_cast<float4 *>(smem + blo_off(s)), t);
                     }
-                    if (!ok) break;
-                    // Generic-proxy writes must be visible to the tensor core (async proxy).
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    // Generic-proxy writes must be visible to the tensor core (async
+                    // proxy); tensor-memory stores are ordered by the tcgen05 fence.
+                    if constexpr (THREE || !B_K)
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    tc_fence_before();
                     mbar_arrive(split_bar(s));
                 }
             }
@@ -535,84 +674,140 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!mbar_wait(acc_full_bar(acc), use & 1, err, ERR_EPILOGUE, lim)) break;
             tc_fence_after();
             const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-            const int row = m0 + q * 32 + lane;
-            if (p.c_tma) {
-                // beta == 0: alpha, bias, ReLU in registers; each 32 x 32 chunk is staged in
-                // shared memory (128-byte swizzle: lane = row, 16-byte chunk index XOR
-                // row % 8, conflict-free) and written by one TMA store, which clips the
-                // rows and columns outside C.  Two buffers per warp.
+            if constexpr (TRANS_OUT) {
+                // D = C^T: this thread holds column n of C, rows m0 + c0 + i.
+                const int n = n0 + q * 32 + lane;
+                const float bn = (p.bias && n < p.N) ? __ldg(p.bias + n) : 0.0f;
+                if (p.c_tma) {
+                    // Stage 32 rows x 32 columns of C (row i: 128 bytes, 16-byte chunk index
+                    // XOR i % 8; lane = column, so each row's stores hit 32 banks) and write
+                    // them with one TMA store, as in the untransposed case.
 #pragma unroll 1
-                for (int c0 = c_first; c0 < c_first + EPI_COLS; c0 += 32) {
-                    const int buf = EPI_BUFS == 2 ? (c0 >> 5) & 1 : 0;
-                    // the store that last read this buffer must have finished reading it
-                    if (lane == 0) {
-                        if constexpr (EPI_BUFS == 2)
-                            asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                        else
-                            asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                    }
-                    __syncwarp();
-                    uint32_t r[32];
-                    tmem_ld_32cols(src + (uint32_t)c0, r);
-                    uint8_t *const rowbuf = ebuf + buf * 4096 + lane * 128;
-#pragma unroll
-                    for (int g = 0; g < 8; ++g) {
-                        float v[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const int gc = n0 + c0 + 4 * g + e;
-                            float o = p.alpha * __uint_as_float(r[4 * g + e]);
-                            if (p.bias && gc < p.N) o += __ldg(p.bias + gc);
-                            if (p.relu) o = fmaxf(o, 0.0f);
-                            v[e] = o;
+                    for (int c0 = c_first; c0 < c_first + EPI_COLS; c0 += 32) {
+                        const int buf = EPI_BUFS == 2 ? (c0 >> 5) & 1 : 0;
+                        if (lane == 0) {
+                            if constexpr (EPI_BUFS == 2)
+                                asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                            else
+                                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
                         }
-                        *reinterpret_cast<float4 *>(rowbuf + ((g ^ (lane & 7)) << 4)) =
-                            make_float4(v[0], v[1], v[2], v[3]);
+                        __syncwarp();
+                        uint32_t r[32];
+                        tmem_ld_32cols(src + (uint32_t)c0, r);
+                        uint8_t *const cbuf = ebuf + buf * 4096;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            float o = p.alpha * __uint_as_float(r[i]) + bn;
+                            if (p.relu) o = fmaxf(o, 0.0f);
+                            *reinterpret_cast<float *>(cbuf + i * 128 +
+                                                       ((((lane >> 2) ^ (i & 7)) << 4) | ((lane & 3) << 2))) = o;
+                        }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
+                        if (lane == 0 && n0 + q * 32 < p.N && m0 + c0 < p.M)
+                            tma_store_3d(&p.tmC, stage0 + (uint32_t)buf * 4096u, n0 + q * 32, m0 + c0, bz);
                     }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                    // (a chunk entirely outside C is not stored at all)
-                    if (lane == 0 && n0 + c0 < p.N && m0 + q * 32 < p.M)
-                        tma_store_3d(&p.tmC, stage0 + (uint32_t)buf * 4096u, n0 + c0, m0 + q * 32, bz);
+                } else {
+                    float *const C = p.C + (long long)bz * p.strideC;
+#pragma unroll 1
+                    for (int c0 = c_first; c0 < c_first + EPI_COLS; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_ld_32cols(src + (uint32_t)c0, r);
+                        if (n < p.N) {
+#pragma unroll 4
+                            for (int i = 0; i < 32; ++i) {
+                                const int m = m0 + c0 + i;
+                                if (m >= p.M) break;
+                                float *const cp = C + (long long)m * p.ldc + n;
+                                float o = p.alpha * __uint_as_float(r[i]);
+                                if (p.beta != 0.0f) o = fmaf(p.beta, *cp, o);
+                                o += bn;
+                                if (p.relu) o = fmaxf(o, 0.0f);
+                                *cp = o;
+                            }
+                        }
+                    }
                 }
             } else {
-                float *const C = p.C + (long long)bz * p.strideC;
+                const int row = m0 + q * 32 + lane;
+                if (p.c_tma) {
+                    // beta == 0: alpha, bias, ReLU in registers; each 32 x 32 chunk is staged in
+                    // shared memory (128-byte swizzle: lane = row, 16-byte chunk index XOR
+                    // row % 8, conflict-free) and written by one TMA store, which clips the
+                    // rows and columns outside C.  Two buffers per warp.
 #pragma unroll 1
-                for (int c0 = c_first; c0 < c_first + EPI_COLS; c0 += 32) {
-                    uint32_t r[32];
-                    tmem_ld_32cols(src + (uint32_t)c0, r);
-                    if (row < p.M) {
-                        float *const crow = C + (long long)row * p.ldc;
+                    for (int c0 = c_first; c0 < c_first + EPI_COLS; c0 += 32) {
+                        const int buf = EPI_BUFS == 2 ? (c0 >> 5) & 1 : 0;
+                        // the store that last read this buffer must have finished reading it
+                        if (lane == 0) {
+                            if constexpr (EPI_BUFS == 2)
+                                asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                            else
+                                asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                        }
+                        __syncwarp();
+                        uint32_t r[32];
+                        tmem_ld_32cols(src + (uint32_t)c0, r);
+                        uint8_t *const rowbuf = ebuf + buf * 4096 + lane * 128;
 #pragma unroll
                         for (int g = 0; g < 8; ++g) {
-                            const int gc = n0 + c0 + 4 * g;
                             float v[4];
 #pragma unroll
-                            for (int e = 0; e < 4; ++e) v[e] = p.alpha * __uint_as_float(r[4 * g + e]);
-                            if (p.c_vec && gc + 3 < p.N) {
-                                if (p.beta != 0.0f) {
-                                    const float4 c = *reinterpret_cast<const float4 *>(crow + gc);
-                                    v[0] = fmaf(p.beta, c.x, v[0]);
-                                    v[1] = fmaf(p.beta, c.y, v[1]);
-                                    v[2] = fmaf(p.beta, c.z, v[2]);
-                                    v[3] = fmaf(p.beta, c.w, v[3]);
-                                }
+                            for (int e = 0; e < 4; ++e) {
+                                const int gc = n0 + c0 + 4 * g + e;
+                                float o = p.alpha * __uint_as_float(r[4 * g + e]);
+                                if (p.bias && gc < p.N) o += __ldg(p.bias + gc);
+                                if (p.relu) o = fmaxf(o, 0.0f);
+                                v[e] = o;
+                            }
+                            *reinterpret_cast<float4 *>(rowbuf + ((g ^ (lane & 7)) << 4)) =
+                                make_float4(v[0], v[1], v[2], v[3]);
+                        }
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        __syncwarp();
+                        // (a chunk entirely outside C is not stored at all)
+                        if (lane == 0 && n0 + c0 < p.N && m0 + q * 32 < p.M)
+                            tma_store_3d(&p.tmC, stage0 + (uint32_t)buf * 4096u, n0 + c0, m0 + q * 32, bz);
+                    }
+                } else {
+                    float *const C = p.C + (long long)bz * p.strideC;
+#pragma unroll 1
+                    for (int c0 = c_first; c0 < c_first + EPI_COLS; c0 += 32) {
+                        uint32_t r[32];
+                        tmem_ld_32cols(src + (uint32_t)c0, r);
+                        if (row < p.M) {
+                            float *const crow = C + (long long)row * p.ldc;
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    if (p.bias) v[e] += __ldg(p.bias + gc + e);
-                                    if (p.relu) v[e] = fmaxf(v[e], 0.0f);
-                                }
-                                *reinterpret_cast<float4 *>(crow + gc) =
-                                    make_float4(v[0], v[1], v[2], v[3]);
-                            } else {
+                            for (int g = 0; g < 8; ++g) {
+                                const int gc = n0 + c0 + 4 * g;
+                                float v[4];
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    if (gc + e >= p.N) break;
-                                    float o = v[e];
-                                    if (p.beta != 0.0f) o = fmaf(p.beta, crow[gc + e], o);
-                                    if (p.bias) o += __ldg(p.bias + gc + e);
-                                    if (p.relu) o = fmaxf(o, 0.0f);
-                                    crow[gc + e] = o;
+                                for (int e = 0; e < 4; ++e) v[e] = p.alpha * __uint_as_float(r[4 * g + e]);
+                                if (p.c_vec && gc + 3 < p.N) {
+                                    if (p.beta != 0.0f) {
+                                        const float4 c = *reinterpret_cast<const float4 *>(crow + gc);
+                                        v[0] = fmaf(p.beta, c.x, v[0]);
+                                        v[1] = fmaf(p.beta, c.y, v[1]);
+                                        v[2] = fmaf(p.beta, c.z, v[2]);
+                                        v[3] = fmaf(p.beta, c.w, v[3]);
+                                    }
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        if (p.bias) v[e] += __ldg(p.bias + gc + e);
+                                        if (p.relu) v[e] = fmaxf(v[e], 0.0f);
+                                    }
+                                    *reinterpret_cast<float4 *>(crow + gc) =
+                                        make_float4(v[0], v[1], v[2], v[3]);
+                                } else {
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        if (gc + e >= p.N) break;
+                                        float o = v[e];
+                                        if (p.beta != 0.0f) o = fmaf(p.beta, crow[gc + e], o);
+                                        if (p.bias) o += __ldg(p.bias + gc + e);
+                                        if (p.relu) o = fmaxf(o, 0.0f);
+                                        crow[gc + e] = o;
+                                    }
                                 }
                             }
                         }
