@@ -63,10 +63,11 @@ enum Mode { MODE_TF32 = 1, MODE_3XTF32 = 3 };
 
 template <int MODE>
 struct Layout {
-    static constexpr int STAGES = MODE == MODE_3XTF32 ? 3 : 6;
-    // Per stage: A, B (raw, or hi after the split), then A_lo, B_lo in 3xTF32.
+    static constexpr int STAGES = MODE == MODE_3XTF32 ? 4 : 6;
+    // Per stage: A, B (raw, or hi after the split), then in 3xTF32 the lo part of the
+    // one operand that stays in shared memory (the other goes to tensor memory).
     static constexpr int STAGE_BYTES =
-        (TILE_A_BYTES + TILE_B_BYTES) * (MODE == MODE_3XTF32 ? 2 : 1);
+        TILE_A_BYTES + TILE_B_BYTES + (MODE == MODE_3XTF32 ? TILE_A_BYTES : 0);
     // Epilogue staging: 32 KB, two 4 KB chunk buffers per epilogue warp (four warps),
     // or one per warp when eight warps share the epilogue.
     static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;
@@ -464,8 +465,7 @@ __global__ void __launch_bounds__(THREADS, 1)
 
     auto a_off = [&](int s) { return s * L::STAGE_BYTES; };
     auto b_off = [&](int s) { return s * L::STAGE_BYTES + TILE_A_BYTES; };
-    auto alo_off = [&](int s) { return s * L::STAGE_BYTES + TILE_A_BYTES + TILE_B_BYTES; };
-    auto blo_off = [&](int s) { return s * L::STAGE_BYTES + 2 * TILE_A_BYTES + TILE_B_BYTES; };
+    auto lo_off = [&](int s) { return s * L::STAGE_BYTES + TILE_A_BYTES + TILE_B_BYTES; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KT = (p.K + BK - 1) / BK;
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         // A operand in tensor memory; B operand = the other (K-major) tile.
                         const uint32_t at = tmem + ACC_COLS + (uint32_t)s * OP_COLS;
                         const int kop = B_VIA_TMEM ? a_off(s) : b_off(s);
-                        const int kop_lo = B_VIA_TMEM ? alo_off(s) : blo_off(s);
+                        const int kop_lo = lo_off(s);
                         const uint64_t bd = kmajor_sw128_desc(sbase + kop);
 #pragma unroll
                         for (int k = 0; k < BK / UMMA_K; ++k) {
@@ -638,15 +638,15 @@ __global__ void __launch_bounds__(THREADS, 1)
                     if constexpr (B_VIA_TMEM) {
                         if constexpr (THREE)
                             split_kmajor(reinterpret_cast<float4 *>(smem + a_off(s)),
-                                         reinterpret_cast<float4 *>(smem + alo_off(s)), t);
+                                         reinterpret_cast<float4 *>(smem + lo_off(s)), t);
                     } else if constexpr (!B_K) {
-                        ok = transpose_mnmajor<THREE>(smem + b_off(s), smem + blo_off(s), t,
+                        ok = transpose_mnmajor<THREE>(smem + b_off(s), smem + lo_off(s), t,
                                                       read_bar, transposes & 1, err, lim);
                         ++transposes;
                         if (!ok) break;
                     } else if constexpr (THREE) {
                         split_kmajor(reinterpret_cast<float4 *>(smem + b_off(s)),
-                                     reinterpret_cast<float4 *>(smem + blo_off(s)), t);
+                                     reinterpret_cast<float4 *>(smem + lo_off(s)), t);
                     }
                     // Generic-proxy writes must be visible to the tensor core (async
                     // proxy); tensor-memory stores are ordered by the tcgen05 fence.
