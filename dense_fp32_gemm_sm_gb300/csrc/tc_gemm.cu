@@ -41,11 +41,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
 
 // One operand as a 3-D tensor map (inner, outer, batch), `batch` problems `stride`
 // elements apart.  K-major storage (rows x K, K contiguous): inner = K, boxes of
-// 32 x 128 with the 128-byte swizzle (the canonical UMMA layout).  MN-major storage
-// (K x rows, rows contiguous): inner = rows, plain 128 x 32 boxes that the kernel
-// transposes on chip.
+// 32 x box_rows with the 128-byte swizzle (the canonical UMMA layout).  MN-major
+// storage (K x rows, rows contiguous): inner = rows, plain box_rows x 32 boxes that
+// the kernel transposes on chip.
 bool make_operand_map(CUtensorMap *map, const float *base, bool kmajor, long long rows, long long K,
-                      long long ld, long long batch, long long stride)
+                      long long ld, long long batch, long long stride, int box_rows)
 {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;
@@ -54,8 +54,8 @@ bool make_operand_map(CUtensorMap *map, const float *base, bool kmajor, long lon
     const cuuint64_t dims[3] = {(cuuint64_t)(kmajor ? K : rows), (cuuint64_t)outer,
                                 (cuuint64_t)batch};
     const cuuint64_t strides[2] = {(cuuint64_t)ld * 4, (cuuint64_t)stride * 4};
-    const cuuint32_t box[3] = {kmajor ? (cuuint32_t)tc::BK : 128u, kmajor ? 128u : (cuuint32_t)tc::BK,
-                               1};
+    const cuuint32_t box[3] = {kmajor ? (cuuint32_t)tc::BK : (cuuint32_t)box_rows,
+                               kmajor ? (cuuint32_t)box_rows : (cuuint32_t)tc::BK, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     const CUresult r =
         enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(base), dims, strides, box,
@@ -110,15 +110,22 @@ cudaError_t prepare_tc()
     const unsigned long long bit = 1ull << (dev & 63);
     if (ready.load(std::memory_order_acquire) & bit) return cudaSuccess;
     e = cudaFuncSetAttribute(tc::tc_gemm_kernel<MODE, TA, TB>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, tc::Layout<MODE>::SMEM_BYTES);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             tc::TcShape<MODE, TA, TB>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     ready.fetch_or(bit, std::memory_order_acq_rel);
     return cudaSuccess;
 }
 
 template <int MODE, int TA, int TB>
-fgemm_status launch_tc_mode(tc::TcParams &p, cudaStream_t stream)
+fgemm_status launch_tc_mode(const TcProblem &q, tc::TcParams &p, cudaStream_t stream)
 {
+    using Shape = tc::TcShape<MODE, TA, TB>;
+    if (!make_operand_map(&p.tmA, q.A, TA == 0, q.M, q.K, q.lda, q.batch, q.sA, Shape::TILE_M) ||
+        !make_operand_map(&p.tmB, q.B, TB == 1, q.N, q.K, q.ldb, q.batch, q.sB, Shape::TILE_N))
+        return FGEMM_ERR_NOT_SUPPORTED;
+    p.tiles_m = (q.M + Shape::TILE_M - 1) / Shape::TILE_M;
+    p.tiles_n = (q.N + Shape::TILE_N - 1) / Shape::TILE_N;
     unsigned *err = error_word();
     int sms = 0;
     if (!err || prepare_tc<MODE, TA, TB>() != cudaSuccess || device_sm_count(&sms) != 0) {
@@ -128,8 +135,7 @@ fgemm_status launch_tc_mode(tc::TcParams &p, cudaStream_t stream)
     // Persistent: one CTA per SM (or per tile, if there are fewer tiles).
     const long long tiles = (long long)p.tiles_m * p.tiles_n * p.batch;
     const long long grid = tiles < sms ? tiles : sms;
-    tc::tc_gemm_kernel<MODE, TA, TB><<<(unsigned)grid, tc::THREADS, tc::Layout<MODE>::SMEM_BYTES,
-                                       stream>>>(p, err);
+    tc::tc_gemm_kernel<MODE, TA, TB><<<(unsigned)grid, tc::THREADS, Shape::SMEM_BYTES, stream>>>(p, err);
     return cudaGetLastError() == cudaSuccess ? FGEMM_OK : FGEMM_ERR_LAUNCH;
 }
 
@@ -144,7 +150,8 @@ bool tc_supported(const TcProblem &q)
     if (q.batch > 1 && (q.sA % 4 || q.sB % 4)) return false;
     const long long lim = 1ll << 38;  // tensor-map strides are below 2^40 bytes
     if (q.lda >= lim || q.ldb >= lim || q.sA >= lim || q.sB >= lim) return false;
-    if ((long long)((q.M + tc::BM - 1) / tc::BM) * ((q.N + tc::BN - 1) / tc::BN) > INT_MAX) return false;
+    // (the smallest tile of any instance is 128 x 128)
+    if ((long long)((q.M + 127) / 128) * ((q.N + 127) / 128) > INT_MAX) return false;
     return encode_fn() != nullptr;
 }
 
@@ -152,9 +159,6 @@ fgemm_status launch_tc(int mode, const TcProblem &q, cudaStream_t stream)
 {
     tc::TcParams p;
     std::memset(&p, 0, sizeof(p));
-    if (!make_operand_map(&p.tmA, q.A, q.ta == 0, q.M, q.K, q.lda, q.batch, q.sA) ||
-        !make_operand_map(&p.tmB, q.B, q.tb == 1, q.N, q.K, q.ldb, q.batch, q.sB))
-        return FGEMM_ERR_NOT_SUPPORTED;
     p.C = q.C;
     p.bias = q.bias;
     p.ldc = q.ldc;
@@ -173,25 +177,23 @@ fgemm_status launch_tc(int mode, const TcProblem &q, cudaStream_t stream)
                make_output_map(&p.tmC, q.C, q.M, q.N, q.ldc, q.batch, q.sC))
                   ? 1
                   : 0;
-    p.tiles_m = (q.M + tc::BM - 1) / tc::BM;
-    p.tiles_n = (q.N + tc::BN - 1) / tc::BN;
     p.batch = q.batch;
     p.withhold_kb = g_withhold_kb.load(std::memory_order_relaxed);
     p.wait_limit_ns = g_wait_limit_ns.load(std::memory_order_relaxed);
     const int layout = q.ta * 2 + q.tb;  // 0: NN, 1: NT, 2: TN, 3: TT
     if (mode == tc::MODE_3XTF32) {
         switch (layout) {
-        case 0: return launch_tc_mode<tc::MODE_3XTF32, 0, 0>(p, stream);
-        case 1: return launch_tc_mode<tc::MODE_3XTF32, 0, 1>(p, stream);
-        case 2: return launch_tc_mode<tc::MODE_3XTF32, 1, 0>(p, stream);
-        default: return launch_tc_mode<tc::MODE_3XTF32, 1, 1>(p, stream);
+        case 0: return launch_tc_mode<tc::MODE_3XTF32, 0, 0>(q, p, stream);
+        case 1: return launch_tc_mode<tc::MODE_3XTF32, 0, 1>(q, p, stream);
+        case 2: return launch_tc_mode<tc::MODE_3XTF32, 1, 0>(q, p, stream);
+        default: return launch_tc_mode<tc::MODE_3XTF32, 1, 1>(q, p, stream);
         }
     }
     switch (layout) {
-    case 0: return launch_tc_mode<tc::MODE_TF32, 0, 0>(p, stream);
-    case 1: return launch_tc_mode<tc::MODE_TF32, 0, 1>(p, stream);
-    case 2: return launch_tc_mode<tc::MODE_TF32, 1, 0>(p, stream);
-    default: return launch_tc_mode<tc::MODE_TF32, 1, 1>(p, stream);
+    case 0: return launch_tc_mode<tc::MODE_TF32, 0, 0>(q, p, stream);
+    case 1: return launch_tc_mode<tc::MODE_TF32, 0, 1>(q, p, stream);
+    case 2: return launch_tc_mode<tc::MODE_TF32, 1, 0>(q, p, stream);
+    default: return launch_tc_mode<tc::MODE_TF32, 1, 1>(q, p, stream);
     }
 }
 

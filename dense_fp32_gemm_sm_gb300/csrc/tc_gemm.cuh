@@ -47,12 +47,10 @@
 namespace fgemm {
 namespace tc {
 
-constexpr int BM = 128, BN = 128, BK = 32;  // BK FP32 values = one 128-byte swizzle row
-constexpr int UMMA_K = 8;                   // K of one kind::tf32 MMA (32 bytes)
-constexpr int TILE_A_BYTES = BM * BK * 4;   // 16 KB
-constexpr int TILE_B_BYTES = BN * BK * 4;   // 16 KB
-constexpr int THREADS = 320;               // 10 warps, see the kernel
-constexpr uint32_t ACC_COLS = 2 * BN;       // two FP32 accumulators of 128 lanes x BN columns
+constexpr int MMA_M = 128;  // rows of the MMA = tensor-memory lanes
+constexpr int BK = 32;      // k per stage: 32 FP32 values = one 128-byte swizzle row
+constexpr int UMMA_K = 8;   // K of one kind::tf32 MMA (32 bytes)
+constexpr int THREADS = 320;  // 10 warps, see the kernel
 constexpr unsigned long long kWaitLimitNs = 4000000000ull;  // default: 4 s per wait
 
 // Error bits recorded in the device error word.
@@ -61,13 +59,43 @@ constexpr unsigned ERR_PRODUCER = 1u, ERR_MMA_WAIT = 2u, ERR_SPLIT_WAIT = 4u, ER
 
 enum Mode { MODE_TF32 = 1, MODE_3XTF32 = 3 };
 
-template <int MODE>
-struct Layout {
-    static constexpr int STAGES = MODE == MODE_3XTF32 ? 4 : 6;
-    // Per stage: A, B (raw, or hi after the split), then in 3xTF32 the lo part of the
-    // one operand that stays in shared memory (the other goes to tensor memory).
-    static constexpr int STAGE_BYTES =
-        TILE_A_BYTES + TILE_B_BYTES + (MODE == MODE_3XTF32 ? TILE_A_BYTES : 0);
+// Shapes of one kernel instance.  The MMA is 128 x MMA_N x 8; MMA_N = 256 halves the
+// MMA instructions and the operand traffic per FLOP against 128 (measured, TF32 NT:
+// 549 -> 659 TFLOP/s at 4096^3, 599 -> 820 at 8192^3), and is used in TF32 whenever one
+// operand is K-major.  3xTF32 keeps MMA_N = 128: its extra lo tile would leave only two
+// stages of shared memory.  The operand that goes through tensor memory (see the
+// kernel) is always the 128-row side; with MMA_N = 256 there is room in tensor memory
+// for it or for a second accumulator, not both, so those layouts use one accumulator.
+template <int MODE, int TA, int TB>
+struct TcShape {
+    static constexpr bool A_K = TA == 0, B_K = TB == 1;  // operand stored K-major
+    static constexpr bool THREE = MODE == MODE_3XTF32;
+    // Which operand reaches the MMA through tensor memory (as its A operand):
+    // B when A is K-major and B is not (NN: the MMA then computes C^T), else A in
+    // 3xTF32 or when A is stored K x M; TF32 NT uses none.
+    static constexpr bool B_VIA_TMEM = A_K && !B_K;
+    static constexpr bool A_VIA_TMEM = !B_VIA_TMEM && (THREE || !A_K);
+    static constexpr bool TMEM_OP = A_VIA_TMEM || B_VIA_TMEM;
+    static constexpr bool TRANS_OUT = B_VIA_TMEM;
+    static constexpr bool WIDE = !THREE && (A_K || B_K);
+    static constexpr int MMA_N = WIDE ? 256 : 128;
+    static constexpr int NACC = (TMEM_OP && WIDE) ? 1 : 2;  // accumulators in tensor memory
+    // The C tile of one MMA sequence: MMA rows are C rows, or C columns when TRANS_OUT.
+    static constexpr int TILE_M = TRANS_OUT ? MMA_N : MMA_M;
+    static constexpr int TILE_N = TRANS_OUT ? MMA_M : MMA_N;
+    static constexpr int A_BYTES = TILE_M * BK * 4;
+    static constexpr int B_BYTES = TILE_N * BK * 4;
+    // 3xTF32: the lo part of the operand that stays in shared memory (128 rows).
+    static constexpr int LO_BYTES = THREE ? MMA_M * BK * 4 : 0;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + LO_BYTES;
+    static constexpr int STAGES = STAGE_BYTES > 32768 ? 4 : 6;
+    // Tensor-memory columns: the accumulators, then per stage 32 columns of the MMA's
+    // A operand (64 in 3xTF32: hi, lo).
+    static constexpr uint32_t ACC_COLS = NACC * MMA_N;
+    static constexpr uint32_t OP_COLS = THREE ? 64 : 32;
+    static constexpr uint32_t TMEM_COLS = TMEM_OP ? 512 : ACC_COLS;
+    static_assert(!TMEM_OP || ACC_COLS + STAGES * OP_COLS <= TMEM_COLS, "tensor-memory columns");
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "allocation: a power of two");
     // Epilogue staging: 32 KB, two 4 KB chunk buffers per epilogue warp (four warps),
     // or one per warp when eight warps share the epilogue.
     static constexpr int EPI_OFFSET = STAGES * STAGE_BYTES;
@@ -80,7 +108,7 @@ struct Layout {
 };
 
 struct TcParams {
-    // K-major operand: dims (K, rows, batch), box (32, 128, 1), 128-byte swizzle.
+    // K-major operand: dims (K, rows, batch), box (32, tile rows, 1), 128-byte swizzle.
     // MN-major operand: dims (rows, K, batch), box (128, 32, 1), no swizzle.
     CUtensorMap tmA;
     CUtensorMap tmB;
@@ -288,7 +316,7 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo)
 __device__ __forceinline__ void split_kmajor(float4 *tile, float4 *lo, int t)
 {
 #pragma unroll 4
-    for (int c = t; c < TILE_A_BYTES / 16; c += 128) {
+    for (int c = t; c < MMA_M * BK * 4 / 16; c += 128) {
         const float4 v = tile[c];
         float4 h, l;
         split_tf32(v.x, h.x, l.x);
@@ -422,31 +450,21 @@ template <int MODE, int TA, int TB>
 __global__ void __launch_bounds__(THREADS, 1)
     tc_gemm_kernel(const __grid_constant__ TcParams p, unsigned *err)
 {
-    using L = Layout<MODE>;
+    using L = TcShape<MODE, TA, TB>;
     constexpr int S = L::STAGES;
-    constexpr bool A_K = TA == 0, B_K = TB == 1;
-    constexpr bool THREE = MODE == MODE_3XTF32;
+    constexpr bool A_K = L::A_K, B_K = L::B_K, THREE = L::THREE;
     constexpr bool CONVERT = THREE || !A_K || !B_K;  // warps 2-5 touch each stage
     // One operand goes to tensor memory as the MMA's A operand, written there from
     // registers by warps 2-5 (transposed on the way when it is stored MN-major, split
     // into hi and lo in 3xTF32), so the tensor core reads only the other operand from
-    // shared memory:
-    //   A stored K x M (TA = 1), or any 3xTF32 layout but NN: A goes to tensor memory;
-    //   A stored M x K and B stored K x N (NN): B goes, the MMA's B operand is A and the
-    //   MMA computes the transposed tile D = C^T (lanes are columns of C);
-    //   TF32 with both operands K-major (NT): neither, the TMA tiles feed the MMA as is.
-    constexpr bool B_VIA_TMEM = A_K && !B_K;
-    constexpr bool A_VIA_TMEM = !B_VIA_TMEM && (THREE || !A_K);
-    constexpr bool TMEM_OP = A_VIA_TMEM || B_VIA_TMEM;
-    constexpr bool TRANS_OUT = B_VIA_TMEM;
-    // Tensor-memory columns: the two accumulators, then per stage 32 columns of the
-    // MMA's A operand (64 in 3xTF32: hi, lo).
-    constexpr uint32_t OP_COLS = THREE ? 64 : 32;
-    constexpr uint32_t TMEM_COLS = TMEM_OP ? 512 : ACC_COLS;
-    static_assert(!TMEM_OP || ACC_COLS + S * OP_COLS <= TMEM_COLS, "tensor-memory columns");
+    // shared memory; in NN that is A, and the MMA computes the transposed tile D = C^T
+    // (tensor-memory lanes are columns of C).  See TcShape for which goes where.
+    constexpr bool B_VIA_TMEM = L::B_VIA_TMEM, TMEM_OP = L::TMEM_OP, TRANS_OUT = L::TRANS_OUT;
+    constexpr int MMA_N = L::MMA_N, NACC = L::NACC;
+    constexpr uint32_t ACC_COLS = L::ACC_COLS, OP_COLS = L::OP_COLS, TMEM_COLS = L::TMEM_COLS;
     // Without a split or transpose, warps 2-5 share the epilogue with warps 6-9.
     constexpr int EPI_WARPS = CONVERT ? 4 : 8;
-    constexpr int EPI_COLS = BN * 4 / EPI_WARPS;  // columns of a tile per epilogue warp
+    constexpr int EPI_COLS = MMA_N * 4 / EPI_WARPS;  // accumulator columns per epilogue warp
     constexpr int EPI_BUFS = 8 / (EPI_WARPS / 4) / 4;  // 4 KB buffers per epilogue warp
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment of the operand tiles (the swizzle atom).
@@ -464,8 +482,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + L::BAR_OFFSET + 8 * (3 * S + 6));
 
     auto a_off = [&](int s) { return s * L::STAGE_BYTES; };
-    auto b_off = [&](int s) { return s * L::STAGE_BYTES + TILE_A_BYTES; };
-    auto lo_off = [&](int s) { return s * L::STAGE_BYTES + TILE_A_BYTES + TILE_B_BYTES; };
+    auto b_off = [&](int s) { return s * L::STAGE_BYTES + L::A_BYTES; };
+    auto lo_off = [&](int s) { return s * L::STAGE_BYTES + L::A_BYTES + L::B_BYTES; };
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KT = (p.K + BK - 1) / BK;
@@ -482,8 +500,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int first_m = group * 8;
         const int rows_in_group = min(p.tiles_m - first_m, 8);
         const int in_group = r - group * per_group;
-        m0 = (first_m + in_group % rows_in_group) * BM;
-        n0 = (in_group / rows_in_group) * BN;
+        m0 = (first_m + in_group % rows_in_group) * L::TILE_M;
+        n0 = (in_group / rows_in_group) * L::TILE_N;
     };
 
     if (warp == 0 && lane == 0) {
@@ -531,7 +549,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(s), TILE_A_BYTES + TILE_B_BYTES);
+                    mbar_arrive_expect_tx(full_bar(s), L::A_BYTES + L::B_BYTES);
                     if constexpr (A_K)
                         tma_load_3d(sbase + a_off(s), &p.tmA, full_bar(s), kb * BK, m0, bz);
                     else
@@ -548,21 +566,21 @@ __global__ void __launch_bounds__(THREADS, 1)
                 mbar_wait(full_bar(k % S), (k / S) & 1, err, ERR_DRAIN, lim, false);
         }
     } else if (warp == 1) {
-        // ---- MMA issuer: accumulator j & 1 for this CTA's j-th tile ----
+        // ---- MMA issuer: accumulator j % NACC for this CTA's j-th tile ----
         if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc(BM, BN);
+            constexpr uint32_t idesc = make_idesc(MMA_M, MMA_N);
             int g = 0;
             bool ok = true;
             int j = 0;
             for (long long t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++j) {
-                const int acc = j & 1, use = j >> 1;
-                // The epilogue must have drained this accumulator (tile j - 2).
+                const int acc = j % NACC, use = j / NACC;
+                // The epilogue must have drained this accumulator (tile j - NACC).
                 if (use > 0 && !mbar_wait(acc_empty_bar(acc), (use - 1) & 1, err, ERR_MMA_WAIT, lim)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)(acc * BN);
+                const uint32_t d = tmem + (uint32_t)(acc * MMA_N);
                 for (int kb = 0; kb < KT; ++kb, ++g) {
                     const int s = g % S, round = g / S;
                     ok = CONVERT ? mbar_wait(split_bar(s), round & 1, err, ERR_MMA_WAIT, lim)
@@ -670,10 +688,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (long long t = blockIdx.x; t < total_tiles; t += gridDim.x, ++j) {
             int m0, n0, bz;
             tile_coords(t, m0, n0, bz);
-            const int acc = j & 1, use = j >> 1;
+            const int acc = j % NACC, use = j / NACC;
             if (!mbar_wait(acc_full_bar(acc), use & 1, err, ERR_EPILOGUE, lim)) break;
             tc_fence_after();
-            const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            const uint32_t src = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * MMA_N);
             if constexpr (TRANS_OUT) {
                 // D = C^T: this thread holds column n of C, rows m0 + c0 + i.
                 const int n = n0 + q * 32 + lane;
