@@ -62,8 +62,8 @@ enum Mode { MODE_TF32 = 1, MODE_3XTF32 = 3 };
 // Shapes of one kernel instance.  The MMA is 128 x MMA_N x 8; MMA_N = 256 halves the
 // MMA instructions and the operand traffic per FLOP against 128 (measured, TF32 NT:
 // 549 -> 659 TFLOP/s at 4096^3, 599 -> 820 at 8192^3), and is used in TF32 whenever one
-// operand is K-major.  3xTF32 keeps MMA_N = 128: its extra lo tile would leave only two
-// stages of shared memory.  The operand that goes through tensor memory (see the
+// operand is K-major.  3xTF32 keeps MMA_N = 128: its extra lo tile leaves room for only
+// two stages at 256 (measured 190 against 240 TFLOP/s at 4096^3).  The operand that goes through tensor memory (see the
 // kernel) is always the 128-row side; with MMA_N = 256 there is room in tensor memory
 // for it or for a second accumulator, not both, so those layouts use one accumulator.
 template <int MODE, int TA, int TB>
