@@ -403,10 +403,12 @@ def run_fgemm(args, rank, world, local_rank):
     kernel_name = fg.config_name(chosen)
     if splitk is not None:
         kernel_name = "%s_splitk%d" % (kernel_name, args.splitk)
-    # The tensor-core kernels take every layout of these (16-byte aligned) workloads.
+    # The tensor-core kernels take every layout of these (16-byte aligned) workloads;
+    # TF32 runs 128 x 256 MMAs when one operand is stored K-major, 3xTF32 128 x 128.
     tensor_path = args.math != "fp32"
     if tensor_path:
-        kernel_name = "tcgen05_%s_128x128" % args.math
+        wide = args.math == "tf32" and (w.ta == 0 or w.tb == 1)
+        kernel_name = "tcgen05_%s_mma128x%d" % (args.math, 256 if wide else 128)
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(max_s * 1e3 /
