@@ -173,8 +173,11 @@ fgemm_status launch_tc(int mode, const TcProblem &q, cudaStream_t stream)
                (q.batch <= 1 || q.sC % 4 == 0))
                   ? 1
                   : 0;
-    p.c_tma = (q.beta == 0.0f && p.c_vec && q.ldc < (1ll << 38) && q.sC < (1ll << 38) &&
-               make_output_map(&p.tmC, q.C, q.M, q.N, q.ldc, q.batch, q.sC))
+    // TMA stores clip a box at the tensor's edge in whole 16-byte chunks (measured: with
+    // N = 31 the store wrote column 31 of a padded C), so they are used only when the
+    // last column ends a chunk.
+    p.c_tma = (q.beta == 0.0f && p.c_vec && q.N % 4 == 0 && q.ldc < (1ll << 38) &&
+               q.sC < (1ll << 38) && make_output_map(&p.tmC, q.C, q.M, q.N, q.ldc, q.batch, q.sC))
                   ? 1
                   : 0;
     p.batch = q.batch;

@@ -109,3 +109,21 @@ def test_bad_math_value():
 def test_device_status_clean():
     torch.cuda.synchronize()
     assert fg.device_status(clear=False) == fg.OK
+
+
+@pytest.mark.parametrize("math", MODES, ids=["tf32", "3xtf32"])
+@pytest.mark.parametrize("ta,tb", COMBOS)
+@pytest.mark.parametrize("shape", [(300, 200, 130), (257, 31, 515), (129, 257, 33), (520, 600, 96),
+                                   (64, 36, 40)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_beta_zero_epilogue(math, ta, tb, shape):
+    # beta = 0 with an aligned C and N a multiple of 4 takes the epilogue that stages
+    # tiles in shared memory and writes them with TMA stores (clipped at the edges;
+    # transposed tiles in NN); other N store directly.  C starts as NaN (any read of it
+    # would show) and its padding columns hold a sentinel that must survive.
+    M, N, K = shape
+    check(Case(ta=ta, tb=tb, M=M, N=N, K=K, alpha=1.5, beta=0.0, bias=True, relu=True,
+               c_nan=True, pad=(4, 8, 4), math=math, seed=M + 3 * N + K))
+    check(Case(ta=ta, tb=tb, M=M, N=N, K=K, alpha=1.0, beta=0.0, c_nan=True, pad=(0, 0, 8),
+               math=math, ints=False, seed=M + N),
+          rel_tol=TF32_TOL if math == fg.MATH_TF32 else 1e-5)
