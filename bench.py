@@ -76,6 +76,9 @@ def parse_args(argv=None):
                     help="S > 1: split-K GEMM into S slices with a workspace (single problems)")
     ap.add_argument("--epilogue", choices=("workload", "none"), default="workload",
                     help="'none' drops the workload's bias/ReLU (plain sgemm at the same shape)")
+    ap.add_argument("--cpu-baseline-table", action="store_true",
+                    help="no GPU: time the FP64 oracle on every workload on one host core and on "
+                         "all of them (bounded samples), one JSON line each")
     return ap.parse_args(argv)
 
 
@@ -260,10 +263,11 @@ def _launch(fg, w, cfg, dA, dB, dC, dbias, stream, math="fp32", splitk=None):
                  stream=stream)
 
 
-def cpu_baseline(w, seconds: float):
-    """FP64 oracle on whole rows of C (all columns), sized to take about `seconds`."""
+def cpu_baseline(w, seconds: float, threads=None):
+    """FP64 oracle on whole rows of C (all columns), sized to take about `seconds`, on
+    `threads` host threads (default: all)."""
     import oracle
-    threads = oracle.default_threads()
+    threads = threads or oracle.default_threads()
     A = w.A.numpy().reshape(-1) if not w.batch else w.A[0].numpy().reshape(-1)
     B = w.B.numpy().reshape(-1) if not w.batch else w.B[0].numpy().reshape(-1)
     C0 = None if w.C0 is None else w.C0.numpy().reshape(-1)
@@ -508,8 +512,21 @@ def run_reference(args, rank, world):
     }
 
 
+def cpu_baseline_table(args):
+    """The oracle beside the GPU numbers, per workload: one core and every core."""
+    import oracle
+    for name in workloads.WORKLOADS:
+        w = workloads.make(name)
+        for threads in (1, oracle.default_threads()):
+            r = cpu_baseline(w, args.cpu_seconds, threads)
+            print(json.dumps({"workload": describe(w), "cpu_baseline": r}), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
+    if args.cpu_baseline_table:
+        cpu_baseline_table(args)
+        return
     rank, world, local_rank = dist_env()
     if args.gpus != world and world > 1:
         print("bench.py: --gpus %d but WORLD_SIZE %d" % (args.gpus, world), file=sys.stderr)

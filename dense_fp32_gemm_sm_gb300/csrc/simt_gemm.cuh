@@ -93,32 +93,9 @@ __device__ __forceinline__ int clamp_bytes(long long remaining_elems)
     return remaining_elems >= 4 ? 16 : (remaining_elems > 0 ? int(remaining_elems) * 4 : 0);
 }
 
-// d += a * b on two packed FP32 lanes (fma.rn.f32x2: round-to-nearest, no flush).
-__device__ __forceinline__ void ffma2(unsigned long long &d, unsigned long long a,
-                                      unsigned long long b)
-{
-    asm volatile("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(d) : "l"(a), "l"(b));
-}
-
-__device__ __forceinline__ unsigned long long dup_pair(float a)
-{
-    unsigned long long d;
-    asm("mov.b64 %0, {%1, %1};" : "=l"(d) : "f"(a));
-    return d;
-}
-
-__device__ __forceinline__ unsigned long long make_pair(float lo, float hi)
-{
-    unsigned long long d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "f"(lo), "f"(hi));
-    return d;
-}
-
-__device__ __forceinline__ float pair_lo(unsigned long long v) { return __uint_as_float((unsigned)v); }
-__device__ __forceinline__ float pair_hi(unsigned long long v)
-{
-    return __uint_as_float((unsigned)(v >> 32));
-}
+// d += a * b on two packed FP32 lanes: the sm_100+ packed FMA (round-to-nearest, no
+// flush), through the compiler's builtin so that it schedules the packed FMAs itself.
+__device__ __forceinline__ void ffma2(float2 &d, float2 a, float2 b) { d = __ffma2_rn(a, b, d); }
 
 // ---- Configuration -------------------------------------------------------------
 
@@ -153,6 +130,7 @@ struct SimtCfg {
 
     static_assert(BK % KS == 0 && KB % 2 == 0, "each k-group takes an even number of k per stage");
     static_assert(LR * LC == 32, "a warp is LR x LC lanes");
+    static_assert(LR % 2 == 0 && LC % 2 == 0, "lane quads are 2 x 2");
     static_assert(BM % WM == 0 && BN % WN == 0, "warp tiles must cover the CTA tile");
     static_assert(TM % 4 == 0 && TN % 4 == 0, "16-byte fragments");
     static_assert(BK % 8 == 0, "transposing copies move 8 k per warp row");
@@ -294,6 +272,22 @@ struct StageCopy {
 // Row (within the CTA tile) of the thread's i-th accumulator row, and column of
 // its j-th accumulator column: groups of 4 consecutive rows/columns, one 16-byte
 // fragment load each.
+// Lane -> (lr, lc) position in the warp's LR x LC lane grid.  Every 4 consecutive
+// lanes form a 2 x 2 block (bit 0 picks the column, bit 1 the row).  Measured on
+// GB300: a warp-wide 16-byte shared load costs 2 wavefronts when each group of 4
+// consecutive lanes reads at most 2 distinct 16-byte chunks, and 4 otherwise.  The A
+// fragment address depends on lr only and the B fragment address on lc only, so with
+// 2 x 2 quads both loads take 2 wavefronts (8 per k-step for 8 x 8 per thread); a
+// row-major lane order (quads along one row) makes the B loads take 4 (12 per k).
+template <class Cfg>
+__device__ __forceinline__ void lane_coords(int lane, int &lr, int &lc)
+{
+    constexpr int HC = Cfg::LC / 2;  // 2 x 2 quads across the lane grid's columns
+    const int quad = lane >> 2;
+    lc = (lane & 1) + 2 * (quad % HC);
+    lr = ((lane >> 1) & 1) + 2 * (quad / HC);
+}
+
 template <class Cfg>
 __device__ __forceinline__ int frag_row(int wm0, int lr, int i)
 {
@@ -320,7 +314,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
     const int warp = tid >> 5, lane = tid & 31;
     const int kg = warp / (Cfg::WARPS_M * Cfg::WARPS_N);  // k-group of this warp
     const int wg = warp % (Cfg::WARPS_M * Cfg::WARPS_N);  // warp within its group
-    const int lr = lane / Cfg::LC, lc = lane % Cfg::LC;
+    int lr, lc;
+    lane_coords<Cfg>(lane, lr, lc);
     const int wm0 = (wg / Cfg::WARPS_N) * Cfg::WM, wn0 = (wg % Cfg::WARPS_N) * Cfg::WN;
     const int kb0 = kg * Cfg::KB;  // first k of a stage this group multiplies
 
@@ -342,11 +337,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
     const float *const B = p.B + bz * p.strideB;
     float *const C = p.C + bz * p.strideC;
 
-    unsigned long long acc[TM][TN / 2];  // acc[i][j] = (c[i][2j], c[i][2j+1])
+    float2 acc[TM][TN / 2];  // acc[i][j] = (c[i][2j], c[i][2j+1])
 #pragma unroll
     for (int i = 0; i < TM; ++i)
 #pragma unroll
-        for (int j = 0; j < TN / 2; ++j) acc[i][j] = 0ull;
+        for (int j = 0; j < TN / 2; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
 
     const uint32_t sA_base = smem_addr(sA_all), sB_base = smem_addr(sB_all);
     const int KT = (p.K + Cfg::BK - 1) / Cfg::BK;
@@ -406,10 +401,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
                 // Duplicate all of a[] first, then sweep the b pairs: each duplicate is
                 // produced well before its first use.
                 const float *a = reinterpret_cast<const float *>(&fa[cur][0]);
-                const unsigned long long *b2 = reinterpret_cast<const unsigned long long *>(&fb[cur][0]);
-                unsigned long long ad[TM];
+                const float2 *b2 = reinterpret_cast<const float2 *>(&fb[cur][0]);
+                float2 ad[TM];
 #pragma unroll
-                for (int i = 0; i < TM; ++i) ad[i] = dup_pair(a[i]);
+                for (int i = 0; i < TM; ++i) ad[i] = make_float2(a[i], a[i]);
 #pragma unroll
                 for (int j = 0; j < TN / 2; ++j)
 #pragma unroll
@@ -425,7 +420,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
     if constexpr (Cfg::KS > 1) {
         if (KT > 0) {
             constexpr int E = TM * TN / 2;  // accumulator pairs per thread
-            unsigned long long *const red = reinterpret_cast<unsigned long long *>(smem);
+            float2 *const red = reinterpret_cast<float2 *>(smem);
             const int gt = tid - kg * Cfg::GROUP_THREADS;
             __syncthreads();
             if (kg > 0) {
@@ -443,10 +438,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
                     for (int i = 0; i < TM; ++i)
 #pragma unroll
                         for (int j = 0; j < TN / 2; ++j) {
-                            const unsigned long long r =
+                            const float2 r =
                                 red[((g - 1) * E + i * (TN / 2) + j) * Cfg::GROUP_THREADS + gt];
-                            acc[i][j] = make_pair(pair_lo(acc[i][j]) + pair_lo(r),
-                                                  pair_hi(acc[i][j]) + pair_hi(r));
+                            acc[i][j] = make_float2(acc[i][j].x + r.x, acc[i][j].y + r.y);
                         }
             }
         }
@@ -471,8 +465,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
 #pragma unroll
         for (int g = 0; g < TN / 4; ++g) {
             const int gc = n0 + frag_col<Cfg>(wn0, lc, 4 * g);
-            float v[4] = {pair_lo(acc[i][2 * g]), pair_hi(acc[i][2 * g]), pair_lo(acc[i][2 * g + 1]),
-                          pair_hi(acc[i][2 * g + 1])};
+            float v[4] = {acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x, acc[i][2 * g + 1].y};
 #pragma unroll
             for (int e = 0; e < 4; ++e) v[e] = products ? p.alpha * v[e] : 0.0f;
             float *const dst = crow + gc;
