@@ -92,8 +92,8 @@ fgemm_status fgemm_sgemm_row_bias_relu(fgemm_op transa, fgemm_op transb, int M, 
 /*
  * Strided batch: for b in [0, batch), the plain GEMM on A + b*strideA,
  * B + b*strideB, C + b*strideC (strides in elements).  Used for batched
- * attention scores Q x K^T (GEMM 优化详解, "为什么 GEMM 重要？", and the
- * "考虑 batched GEMM" advice of "矩阵大小选择策略").
+ * attention scores Q x K^T (GEMM 优化详解, "为什么 GEMM 重要？"; batching small
+ * problems is the page's advice for small matrices in "矩阵大小选择策略").
  * strideA, strideB >= 0 (0 reuses one operand for every problem).
  * strideC >= 0, and no element of C may belong to two problems (checked
  * exactly, so interleaved layouts such as ldc = batch*N, strideC = N are
