@@ -135,6 +135,15 @@ fgemm_status launch_tc_mode(const TcProblem &q, tc::TcParams &p, cudaStream_t st
     // Persistent: one CTA per SM (or per tile, if there are fewer tiles).
     const long long tiles = (long long)p.tiles_m * p.tiles_n * p.batch;
     const long long grid = tiles < sms ? tiles : sms;
+    // With 256-wide MMAs, a last partial wave of at most half the grid is run as twice
+    // as many 128-wide half tiles, so it takes half as long.
+    const long long rem = tiles % grid;
+    p.full_items = tiles;
+    p.total_items = tiles;
+    if (Shape::MMA_N == 2 * tc::MMA_M && rem > 0 && 2 * rem <= grid) {
+        p.full_items = tiles - rem;
+        p.total_items = tiles + rem;
+    }
     tc::tc_gemm_kernel<MODE, TA, TB><<<(unsigned)grid, tc::THREADS, Shape::SMEM_BYTES, stream>>>(p, err);
     return cudaGetLastError() == cudaSuccess ? FGEMM_OK : FGEMM_ERR_LAUNCH;
 }

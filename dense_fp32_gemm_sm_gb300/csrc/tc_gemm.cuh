@@ -123,6 +123,10 @@ struct TcParams {
     int c_tma;  // beta == 0 and C allows TMA stores: stage rows in shared memory
     int tiles_m, tiles_n;
     int batch;   // problems in the strided batch; tiles run over (batch, tile-row, tile-col)
+    // Work items: items [0, full_items) are whole tiles; items from full_items on split
+    // each remaining tile into two halves of 128 along the MMA's N (the last partial
+    // wave then takes half as long).  total_items = full_items when nothing is split.
+    long long full_items, total_items;
     unsigned long long wait_limit_ns;  // bound of every mbarrier wait
     int withhold_kb;  // testing: the producer never issues this k-block (-1: none)
 };
@@ -488,7 +492,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KT = (p.K + BK - 1) / BK;
     const int tiles_per_problem = p.tiles_m * p.tiles_n;
-    const long long total_tiles = (long long)tiles_per_problem * p.batch;
+    const long long total_items = p.total_items;
     const unsigned long long lim = p.wait_limit_ns;
     // The j-th tile of this CTA: problem bz, rows m0.., columns n0.. (grouped order:
     // 8 tile-rows swept column by column, so resident CTAs share panels in L2).
@@ -502,6 +506,19 @@ __global__ void __launch_bounds__(THREADS, 1)
         const int in_group = r - group * per_group;
         m0 = (first_m + in_group % rows_in_group) * L::TILE_M;
         n0 = (in_group / rows_in_group) * L::TILE_N;
+    };
+    // Work item w: its tile's origin, moved to the second half for the odd half-item;
+    // `narrow` items multiply 128 instead of MMA_N columns of the accumulator.
+    auto item_coords = [&](long long w, int &m0, int &n0, int &bz, bool &narrow) {
+        narrow = w >= p.full_items;
+        const long long h = w - p.full_items;
+        tile_coords(narrow ? p.full_items + h / 2 : w, m0, n0, bz);
+        if (narrow && (h & 1)) {
+            if constexpr (TRANS_OUT)
+                m0 += MMA_M;
+            else
+                n0 += MMA_M;
+        }
     };
 
     if (warp == 0 && lane == 0) {
@@ -536,9 +553,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (lane == 0) {
             int g = 0;  // k-blocks issued so far (runs across tiles)
             bool ok = true;
-            for (long long t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+            for (long long t = blockIdx.x; ok && t < total_items; t += gridDim.x) {
                 int m0, n0, bz;
-                tile_coords(t, m0, n0, bz);
+                bool narrow;
+                item_coords(t, m0, n0, bz, narrow);
                 for (int kb = 0; kb < KT; ++kb) {
                     const int s = g % S, round = g / S;
                     if (round > 0 && !mbar_wait(empty_bar(s), (round - 1) & 1, err, ERR_PRODUCER, lim)) {
@@ -568,11 +586,13 @@ __global__ void __launch_bounds__(THREADS, 1)
     } else if (warp == 1) {
         // ---- MMA issuer: accumulator j % NACC for this CTA's j-th tile ----
         if (lane == 0) {
-            constexpr uint32_t idesc = make_idesc(MMA_M, MMA_N);
+            constexpr uint32_t idesc_full = make_idesc(MMA_M, MMA_N);
+            constexpr uint32_t idesc_narrow = make_idesc(MMA_M, MMA_M);
             int g = 0;
             bool ok = true;
             int j = 0;
-            for (long long t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++j) {
+            for (long long t = blockIdx.x; ok && t < total_items; t += gridDim.x, ++j) {
+                const uint32_t idesc = t >= p.full_items ? idesc_narrow : idesc_full;
                 const int acc = j % NACC, use = j / NACC;
                 // The epilogue must have drained this accumulator (tile j - NACC).
                 if (use > 0 && !mbar_wait(acc_empty_bar(acc), (use - 1) & 1, err, ERR_MMA_WAIT, lim)) {
@@ -636,7 +656,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int r = 32 * (warp & 3) + lane;  // the tensor-memory lane this thread writes
             int g = 0, transposes = 0;
             bool ok = true;
-            for (long long tl = blockIdx.x; ok && tl < total_tiles; tl += gridDim.x) {
+            for (long long tl = blockIdx.x; ok && tl < total_items; tl += gridDim.x) {
                 for (int kb = 0; kb < KT; ++kb, ++g) {
                     const int s = g % S, round = g / S;
                     ok = mbar_wait(full_bar(s), round & 1, err, ERR_SPLIT_WAIT, lim);
@@ -685,9 +705,11 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t stage0 = sbase + (uint32_t)(L::EPI_OFFSET + ew * EPI_BUFS * 4096);
         uint8_t *const ebuf = smem + L::EPI_OFFSET + ew * EPI_BUFS * 4096;
         int j = 0;
-        for (long long t = blockIdx.x; t < total_tiles; t += gridDim.x, ++j) {
+        for (long long t = blockIdx.x; t < total_items; t += gridDim.x, ++j) {
             int m0, n0, bz;
-            tile_coords(t, m0, n0, bz);
+            bool narrow;
+            item_coords(t, m0, n0, bz, narrow);
+            const int c_end = narrow ? MMA_M : MMA_N;  // accumulator columns of this item
             const int acc = j % NACC, use = j / NACC;
             if (!mbar_wait(acc_full_bar(acc), use & 1, err, ERR_EPILOGUE, lim)) break;
             tc_fence_after();
@@ -701,7 +723,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // XOR i % 8; lane = column, so each row's stores hit 32 banks) and write
                     // them with one TMA store, as in the untransposed case.
 #pragma unroll 1
-                    for (int c0 = c_first; c0 < c_first + EPI_COLS; c0 += 32) {
+                    for (int c0 = c_first; c0 < c_first + EPI_COLS && c0 < c_end; c0 += 32) {
                         const int buf = EPI_BUFS == 2 ? (c0 >> 5) & 1 : 0;
                         if (lane == 0) {
                             if constexpr (EPI_BUFS == 2)
@@ -728,7 +750,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 } else {
                     float *const C = p.C + (long long)bz * p.strideC;
 #pragma unroll 1
-                    for (int c0 = c_first; c0 < c_first + EPI_COLS; c0 += 32) {
+                    for (int c0 = c_first; c0 < c_first + EPI_COLS && c0 < c_end; c0 += 32) {
                         uint32_t r[32];
                         tmem_ld_32cols(src + (uint32_t)c0, r);
                         if (n < p.N) {
@@ -754,7 +776,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                     // row % 8, conflict-free) and written by one TMA store, which clips the
                     // rows and columns outside C.  Two buffers per warp.
 #pragma unroll 1
-                    for (int c0 = c_first; c0 < c_first + EPI_COLS; c0 += 32) {
+                    for (int c0 = c_first; c0 < c_first + EPI_COLS && c0 < c_end; c0 += 32) {
                         const int buf = EPI_BUFS == 2 ? (c0 >> 5) & 1 : 0;
                         // the store that last read this buffer must have finished reading it
                         if (lane == 0) {
@@ -790,7 +812,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                 } else {
                     float *const C = p.C + (long long)bz * p.strideC;
 #pragma unroll 1
-                    for (int c0 = c_first; c0 < c_first + EPI_COLS; c0 += 32) {
+                    for (int c0 = c_first; c0 < c_first + EPI_COLS && c0 < c_end; c0 += 32) {
                         uint32_t r[32];
                         tmem_ld_32cols(src + (uint32_t)c0, r);
                         if (row < p.M) {

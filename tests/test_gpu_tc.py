@@ -127,3 +127,16 @@ def test_beta_zero_epilogue(math, ta, tb, shape):
     check(Case(ta=ta, tb=tb, M=M, N=N, K=K, alpha=1.0, beta=0.0, c_nan=True, pad=(0, 0, 8),
                math=math, ints=False, seed=M + N),
           rel_tol=TF32_TOL if math == fg.MATH_TF32 else 1e-5)
+
+
+@pytest.mark.parametrize("math", MODES, ids=["tf32", "3xtf32"])
+@pytest.mark.parametrize("ta,tb", COMBOS)
+@pytest.mark.parametrize("shape", [(2560, 2048, 64), (2048, 2560, 40)],
+                         ids=lambda s: "x".join(map(str, s)))
+def test_last_wave_split_into_half_tiles(math, ta, tb, shape):
+    # 160 tiles of 128 x 256 (or 256 x 128) on a ~150-SM GPU: the last partial wave runs
+    # as half tiles of 128 x 128.  Exact on integer data, every element checked.
+    M, N, K = shape
+    check(Case(ta=ta, tb=tb, M=M, N=N, K=K, alpha=1.0, beta=0.0, math=math, seed=M + N + K))
+    check(Case(ta=ta, tb=tb, M=M, N=N, K=K, alpha=0.5, beta=1.0, bias=True, relu=True, math=math,
+               pad=(4, 0, 4), seed=K))
