@@ -76,6 +76,10 @@ def parse_args(argv=None):
                     help="S > 1: split-K GEMM into S slices with a workspace (single problems)")
     ap.add_argument("--epilogue", choices=("workload", "none"), default="workload",
                     help="'none' drops the workload's bias/ReLU (plain sgemm at the same shape)")
+    ap.add_argument("--graph-calls", type=int, default=0,
+                    help="N > 0: also time N back-to-back library calls captured in one CUDA "
+                         "graph (warm L2, no host launch cost): the per-call latency of small "
+                         "shapes")
     ap.add_argument("--cpu-baseline-table", action="store_true",
                     help="no GPU: time the FP64 oracle on every workload on one host core and on "
                          "all of them (bounded samples), one JSON line each")
@@ -400,6 +404,30 @@ def run_fgemm(args, rank, world, local_rank):
     e2e_s = e_start.elapsed_time(e_end) / 1e3 / args.e2e_steps
     e2e_flops, e2e_max = aggregate(w.flops, e2e_s, world, dev if world > 1 else None)
 
+    back_to_back = None
+    if args.graph_calls > 0:
+        # N calls back to back in one CUDA graph: no host launch cost and no L2 flush in
+        # between, so this is the device time per call of a user's captured sequence.
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            step()  # every one-time setup happens before the capture
+        torch.cuda.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            for _ in range(args.graph_calls):
+                _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math, splitk)
+        g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):  # replay() launches on the current stream
+            graph.replay()
+            torch.cuda.synchronize()
+            g0.record(stream)
+            graph.replay()
+            g1.record(stream)
+        torch.cuda.synchronize()
+        per_call = g0.elapsed_time(g1) / 1e3 / args.graph_calls
+        back_to_back = {"calls": args.graph_calls, "us_per_call": round(per_call * 1e6, 3),
+                        "value": round(w.flops / per_call / 1e12, 4), "unit": UNIT,
+                        "l2": "warm (calls back to back in one CUDA graph)"}
+
     chosen = args.config
     if chosen < 0:
         aligned = True
@@ -436,6 +464,8 @@ def run_fgemm(args, rank, world, local_rank):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "wall_s_timed_region": round(wall, 3),
     }
+    if back_to_back is not None:
+        line["back_to_back"] = back_to_back
     if tensor_path:
         tpeak, tsrc = tensor_peak_tflops(args.math)
         line["roofline"] = {"bound": "tensor", "achieved": round(achieved, 4),
