@@ -27,6 +27,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -93,14 +94,22 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source without comments and with whitespace collapsed (the sources'
+    string literals hold no comment markers)."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_hash(family: str) -> str:
-    """Short hash of one kernel family's CUDA sources; profile summaries record the
-    hash of the sources they measured."""
+    """Short hash of one kernel family's CUDA code (comments and layout ignored);
+    profile summaries record the hash of the code they measured."""
     m = hashlib.sha256()
     for name in KERNEL_SOURCES[family]:
         m.update(name.encode())
-        with open(os.path.join(ROOT, "dense_fp32_gemm_sm_gb300", "csrc", name), "rb") as fh:
-            m.update(fh.read())
+        with open(os.path.join(ROOT, "dense_fp32_gemm_sm_gb300", "csrc", name), encoding="utf-8") as fh:
+            m.update(_code_only(fh.read()).encode())
     return m.hexdigest()[:16]
 
 

@@ -15,28 +15,31 @@
 //            precision accuracy from Tensor Cores while surpassing the FP32 theoretical
 //            peak performance", 2022).
 //
-// Structure: a persistent kernel, one CTA per SM, each CTA walking 128 x 128 tiles
-// of C (tile = blockIdx.x, + gridDim.x, ...), ten warps:
-//   warp 0     TMA producer: one lane streams 128 x 32 tiles of A and B (128-byte
-//              swizzled, the canonical K-major operand layout) into a ring of stages,
-//              running ahead across tile boundaries.
-//   warp 1     allocates two 128 x 128 FP32 accumulators in tensor memory; one lane
-//              issues tcgen05.mma (M=128, N=128, K=8) into them alternately and
-//              commits each stage back to the producer through an mbarrier.
-//   warps 2-5  3xTF32: split each stage into hi/lo in place; both modes: transpose
-//              MN-major operands on chip (idle otherwise).
-//   warps 6-9  epilogue of the previous tile while the next one is being multiplied
-//              (warps 2-5 join them when there is nothing to split or transpose):
-//              tcgen05.ld of their 32 accumulator lanes, alpha, beta*C, bias, ReLU;
-//              with beta == 0 the rows are staged in shared memory and written by
+// Structure: a persistent kernel, one CTA per SM, each CTA walking work items (C
+// tiles, item = blockIdx.x, + gridDim.x, ...; a last partial wave of 256-wide tiles
+// runs as 128-wide halves), ten warps:
+//   warp 0     TMA producer: one lane streams the operand tiles of every k-block (32
+//              deep; 128-byte swizzled boxes for K-major operands, plain boxes for
+//              MN-major ones) into a ring of stages, running ahead across items.
+//   warp 1     allocates tensor memory; one lane issues tcgen05.mma (M=128, N=MMA_N,
+//              K=8) into one or two FP32 accumulators and commits each stage back to
+//              the producer through an mbarrier.
+//   warps 2-5  (every layout but TF32 NT) move one operand of each stage from shared
+//              memory through registers into tensor memory, where the MMA reads it as
+//              its A operand -- transposed on the way when stored MN-major, split into
+//              hi and lo in 3xTF32 -- and split (3xTF32) or transpose (both operands
+//              MN-major) the other operand in shared memory.
+//   warps 6-9  epilogue of the previous item while the next one is being multiplied
+//              (warps 2-5 join them when there is nothing to convert): tcgen05.ld of
+//              their 32 accumulator lanes, alpha, beta*C, bias, ReLU; with beta == 0
+//              (and N a multiple of 4) the tile is staged in shared memory and written by
 //              TMA stores, otherwise stored directly; then the accumulator is handed
 //              back to the MMA warp.
-// Operands stored K-major (A as M x K, B as N x K) arrive by TMA already in the
-// canonical layout.  An operand stored MN-major (A as K x M, B as K x N) arrives as a
-// plain 32 x 128 tile and warps 2-5 transpose it in place into the canonical K-major
-// layout (splitting it too in 3xTF32), so every MMA reads K-major descriptors.
-// Every mbarrier wait is bounded by a
-// wall-clock limit: on expiry the kernel records the failure in a device error word,
+// TcShape below fixes, per layout and mode, which operand goes through tensor memory,
+// the MMA's N (256 in TF32 when one operand is K-major, else 128) and the number of
+// accumulators.  In NN the tensor-memory operand is B, so the MMA computes C^T and the
+// epilogue reads accumulator lanes as columns of C.  Every mbarrier wait is bounded by
+// a wall-clock limit: on expiry the kernel records the failure in a device error word,
 // drains its own copies and MMAs, frees its tensor memory and returns.
 #pragma once
 
