@@ -18,17 +18,21 @@
 //    16-byte loads along m and n (the transposed-A idea of the same page, and the
 //    row padding of GEMM 优化详解, "Level 3" / 第5章-基础Kernel, "Shared + Padding").
 //    Fragments for k+1 are loaded while k is computed (register double buffer).
+//    The lanes of a warp form 2 x 2 quads of the warp's lane grid, so both
+//    fragment loads take 2 shared-memory wavefronts (see lane_coords).
 //
 //  * Register blocking (GEMM 优化详解, "Level 5: Register Blocking"): each thread
 //    owns TM x TN accumulators (8 x 8), held as pairs along n and updated with the
-//    packed FP32 FMA of sm_100+ (fma.rn.f32x2): one instruction does two FMAs, so
+//    packed FP32 FMA of sm_100+ (__ffma2_rn): one instruction does two FMAs, so
 //    the FMA pipe stays busy while the issue slots left over carry the shared
-//    loads.  Each a[i] is duplicated into a register pair once per k.
+//    loads.  Each a[i] is paired with itself once per k.
 //
 //  * Epilogue in registers (GEMM 优化详解, "Level 6: Kernel Fusion" and "Level 7:
 //    Vectorized Loads"): v = alpha*acc (+ beta*C) (+ bias[col]) (+ row_bias[row]),
-//    ReLU, then float4
-//    stores when C is 16-byte aligned, scalar stores otherwise.
+//    ReLU, then float4 stores when C is 16-byte aligned, scalar stores otherwise.
+//
+//  * K-groups (KS > 1, for the smallest grids): several warp groups split each
+//    stage's k and add their sums through shared memory before the epilogue.
 //
 //  * Tiles are visited in groups of GROUP_M tile-rows so that concurrently
 //    resident CTAs share panels of A and B in L2.
