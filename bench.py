@@ -113,6 +113,20 @@ def kernel_source_hash(family: str) -> str:
     return m.hexdigest()[:16]
 
 
+def build_info():
+    """nvcc version and the flags the library was compiled with."""
+    from dense_fp32_gemm_sm_gb300 import _build
+    try:
+        out = subprocess.run([_build.nvcc(), "--version"], capture_output=True, text=True,
+                             timeout=30).stdout
+        lines = [l for l in out.splitlines() if "release" in l]
+        version = lines[0].strip() if lines else "unknown"
+    except (OSError, subprocess.SubprocessError):
+        version = "unknown"
+    flags = [f for f in _build.ARCH + _build.NVCC_FLAGS if not f.startswith("-I")]
+    return {"nvcc": version, "flags": " ".join(flags)}
+
+
 def recorded_traffic(config_name: str, workload: str):
     """DRAM bytes per launch from profiles/<config>_<workload>.md, if measured on these sources."""
     path = os.path.join(ROOT, "profiles", "%s_%s.md" % (config_name, workload))
@@ -472,6 +486,9 @@ def run_fgemm(args, rank, world, local_rank):
         "e2e": {"value": round(e2e_flops / e2e_max / 1e12, 4), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "wall_s_timed_region": round(wall, 3),
+        "step_ms": {"median": round(statistics.median(step_ms), 5), "min": round(min(step_ms), 5),
+                    "max": round(max(step_ms), 5)},
+        "build": build_info(),
     }
     if back_to_back is not None:
         line["back_to_back"] = back_to_back
