@@ -104,8 +104,10 @@ __device__ __forceinline__ void ffma2(float2 &d, float2 a, float2 b) { d = __ffm
 // ---- Configuration -------------------------------------------------------------
 
 template <int BM_, int BN_, int BK_, int WM_, int WN_, int TM_, int TN_, int STAGES_, int MINB_,
-          int TA_, int TB_, bool VEC_, int KS_ = 1>
+          int TA_, int TB_, bool VEC_, int KS_ = 1, bool FASTCOPY_ = true>
 struct SimtCfg {
+    // Interior stages issue their copies without per-copy bounds predicates.
+    static constexpr bool FASTCOPY = FASTCOPY_;
     static constexpr int BM = BM_, BN = BN_, BK = BK_;
     static constexpr int WM = WM_, WN = WN_, TM = TM_, TN = TN_;
     static constexpr int STAGES = STAGES_, MINB = MINB_;
@@ -156,7 +158,7 @@ struct SimtCfg {
 // Stored block whose rows run along k (K x MN storage, MN contiguous): rows
 // [k0, k0+BK) x columns [c0, c0+COLS) -> s[k][c] with row stride S_LD.  Thread t
 // always copies the same column chunk, in rows r_base + it * RSTEP.
-template <int BK, int COLS, int S_LD, int THREADS, bool VEC>
+template <int BK, int COLS, int S_LD, int THREADS, bool VEC, bool FAST>
 struct KRowsCopy {
     static constexpr int W = VEC ? 4 : 1;          // elements per copy
     static constexpr int CPR = COLS / W;           // copies per row
@@ -180,6 +182,18 @@ struct KRowsCopy {
                                           int K, int tid)
     {
         const uint32_t s0 = s_tile + (r_base * S_LD + (tid % CPR) * W) * 4;
+        if (FAST && k0 + BK <= K && bytes_c == 4 * W) {
+            // Every copy of this stage is inside the matrix: no per-copy predicates.
+#pragma unroll
+            for (int it = 0; it < ITERS; ++it) {
+                if constexpr (VEC)
+                    cp_async_16(s0 + it * RSTEP * S_LD * 4, p + (long long)(it * RSTEP) * ld, 16);
+                else
+                    cp_async_4(s0 + it * RSTEP * S_LD * 4, p + (long long)(it * RSTEP) * ld, 4);
+            }
+            p += (long long)BK * ld;
+            return;
+        }
 #pragma unroll
         for (int it = 0; it < ITERS; ++it) {
             const bool ok = k0 + r_base + it * RSTEP < K && bytes_c > 0;
@@ -198,7 +212,7 @@ struct KRowsCopy {
 // 8 (k) x 4 (rows) patches: lane&7 picks k, lane>>3 picks the row, so a warp reads
 // four full 32-byte sectors and writes 32 distinct banks.  A thread keeps one k and
 // copies rows r_base + it * RSTEP.
-template <int BK, int ROWS, int S_LD, int THREADS>
+template <int BK, int ROWS, int S_LD, int THREADS, bool FAST>
 struct KColsCopy {
     static constexpr int WARPS = THREADS / 32;
     static constexpr int PATCHES_K = BK / 8;
@@ -207,6 +221,7 @@ struct KColsCopy {
     static_assert(WARPS % PATCHES_K == 0 && ROWS % RSTEP == 0 && ITERS <= 32,
                   "patches divide evenly over the warps");
 
+    static constexpr unsigned kFullMask = ITERS == 32 ? 0xFFFFFFFFu : (1u << ITERS) - 1u;
     const float *p;  // this thread's element (row r0 + r_base, column k_local) of the next stage
     unsigned rmask;  // bit it: row r0 + r_base + it * RSTEP is inside the matrix
 
@@ -230,6 +245,14 @@ struct KColsCopy {
                                           int K, int tid)
     {
         const uint32_t s0 = s_tile + (k_local(tid) * S_LD + r_base(tid)) * 4;
+        if (FAST && k0 + BK <= K && rmask == kFullMask) {
+            // Every copy of this stage is inside the matrix: no per-copy predicates.
+#pragma unroll
+            for (int it = 0; it < ITERS; ++it)
+                cp_async_4(s0 + it * RSTEP * 4, p + (long long)(it * RSTEP) * ld, 4);
+            p += BK;
+            return;
+        }
         const bool kok = k0 + k_local(tid) < K;
 #pragma unroll
         for (int it = 0; it < ITERS; ++it) {
@@ -243,12 +266,12 @@ struct KColsCopy {
 // The two loaders of a configuration: A into sA[k][m], B into sB[k][n].
 template <class Cfg>
 struct StageCopy {
-    using ACopy = typename std::conditional<Cfg::TA == 1,
-                                            KRowsCopy<Cfg::BK, Cfg::BM, Cfg::A_LD, Cfg::THREADS, Cfg::VEC>,
-                                            KColsCopy<Cfg::BK, Cfg::BM, Cfg::A_LD, Cfg::THREADS>>::type;
-    using BCopy = typename std::conditional<Cfg::TB == 0,
-                                            KRowsCopy<Cfg::BK, Cfg::BN, Cfg::B_LD, Cfg::THREADS, Cfg::VEC>,
-                                            KColsCopy<Cfg::BK, Cfg::BN, Cfg::B_LD, Cfg::THREADS>>::type;
+    using ACopy = typename std::conditional<
+        Cfg::TA == 1, KRowsCopy<Cfg::BK, Cfg::BM, Cfg::A_LD, Cfg::THREADS, Cfg::VEC, Cfg::FASTCOPY>,
+        KColsCopy<Cfg::BK, Cfg::BM, Cfg::A_LD, Cfg::THREADS, Cfg::FASTCOPY>>::type;
+    using BCopy = typename std::conditional<
+        Cfg::TB == 0, KRowsCopy<Cfg::BK, Cfg::BN, Cfg::B_LD, Cfg::THREADS, Cfg::VEC, Cfg::FASTCOPY>,
+        KColsCopy<Cfg::BK, Cfg::BN, Cfg::B_LD, Cfg::THREADS, Cfg::FASTCOPY>>::type;
     ACopy a;
     BCopy b;
 
