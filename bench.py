@@ -355,10 +355,6 @@ def run_fgemm(args, rank, world, local_rank):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    n_batch_launches = (max(1, w.batch) + 65534) // 65535
-    if splitk is not None:  # partial GEMMs (one or two launches) + the reduction
-        Ks = -(-(-(-w.K // args.splitk)) // 32) * 32
-        n_batch_launches = (1 if w.K % Ks == 0 else 2) + 1
     sampler = ClockSampler(local_rank, enabled=not args.no_clocks)
     barrier(world)
     torch.cuda.synchronize()
@@ -456,6 +452,14 @@ def run_fgemm(args, rank, world, local_rank):
         aligned = True
         chosen = fg.select_config(w.ta, w.tb, w.M, w.N, w.K, max(1, w.batch), aligned, sms)
     kernel_name = fg.config_name(chosen)
+    n_batch_launches = (max(1, w.batch) + 65534) // 65535
+    if kernel_name.endswith("_split"):
+        # whole 128 x 128 tiles, then the last (tiles mod SMs) as quarter tiles
+        total = -(-w.M // 128) * -(-w.N // 128) * max(1, w.batch)
+        n_batch_launches = int(total - total % sms > 0) + int(total % sms > 0)
+    if splitk is not None:  # partial GEMMs (one or two launches) + the reduction
+        Ks = -(-(-(-w.K // args.splitk)) // 32) * 32
+        n_batch_launches = (1 if w.K % Ks == 0 else 2) + 1
     if splitk is not None:
         kernel_name = "%s_splitk%d" % (kernel_name, args.splitk)
     # The tensor-core kernels take every layout of these (16-byte aligned) workloads;
@@ -490,6 +494,9 @@ def run_fgemm(args, rank, world, local_rank):
                     "max": round(max(step_ms), 5)},
         "build": build_info(),
     }
+    if kernel_name.endswith("_split") and not tensor_path:
+        line["roofline"]["kernels"] = ("two launches of simt_gemm_kernel (whole tiles, then the "
+                                       "quarter tiles of the last wave), timed together as one call")
     if back_to_back is not None:
         line["back_to_back"] = back_to_back
     if tensor_path:

@@ -10,7 +10,7 @@ namespace fgemm {
 
 struct GemmParams;
 
-// A launcher runs one configuration over `batch` problems (blockIdx.z) on a stream.
+// A launcher runs one configuration over `batch` problems on a stream.
 using LaunchFn = fgemm_status (*)(const GemmParams &p, int batch, cudaStream_t stream);
 
 // Kernel configurations.  Ids are part of the test/bench interface.
@@ -23,7 +23,9 @@ enum ConfigId {
     CFG_32x32 = 4,          // 32x32x16, 4x4 per thread, 64 threads (tiny problems)
     CFG_32x32_K4 = 5,       // 32x32x32, 4x4 per thread, four k-groups of 2 warps, 8 stages
                             // (the smallest grids: a quarter of the serial k-steps per thread)
-    NUM_CONFIGS = 6,
+    CFG_128x128_SPLIT = 6,  // CFG_128x128 for all but the last (tiles mod SMs) tiles, which
+                            // then run as 64x64 quarters with four k-groups (second launch)
+    NUM_CONFIGS = 7,
 };
 
 struct ConfigInfo {

@@ -27,7 +27,16 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
     if (!aligned) return CFG_64x64_SCALAR;
     if (num_sms < 1) num_sms = 1;
     const long long b = batch > 0 ? batch : 1;
-    if (ceil_div(M, 128) * ceil_div(N, 128) * b >= num_sms) return CFG_128x128;
+    const long long tiles = ceil_div(M, 128) * ceil_div(N, 128) * b;
+    if (tiles >= num_sms) {
+        // Two CTAs per SM retire tile-pairs at the rate of lone tiles, so the last
+        // r = tiles mod SMs tiles cost a whole lone-tile period.  As quarter tiles
+        // they cost ceil(4r / SMs) quarter periods at about 0.7 of the whole-tile
+        // rate (measured): a gain while that is at most 2 quarters per SM.
+        const long long r = tiles % num_sms;
+        if (r > 0 && 2 * r <= num_sms) return CFG_128x128_SPLIT;
+        return CFG_128x128;
+    }
     // 128 x 64 tiles (8 x 8 per thread) beat twice as many 64 x 64 tiles (4 x 4 per
     // thread) as long as they still occupy most SMs (measured: 1024^2, 128 tiles on
     // 152 SMs, 34.8 vs 28.3 TFLOP/s).

@@ -36,6 +36,13 @@
 //
 //  * Tiles are visited in groups of GROUP_M tile-rows so that concurrently
 //    resident CTAs share panels of A and B in L2.
+//
+//  * Last-wave split (TILE_QUARTER launches): with two CTAs per SM an SM retires
+//    tile-pairs at the same rate as lone tiles, so a grid whose tile count leaves a
+//    remainder r = tiles mod SMs spends a whole extra lone-tile period on those r
+//    tiles while the other SMs idle.  A split launch runs the first tiles whole and
+//    then cuts each of the last r into four quarter tiles with four k-groups each,
+//    so the remainder's work spreads over the SMs in quarter-tile steps.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -56,6 +63,9 @@ struct GemmParams {
     int relu;
     int tiles_m, tiles_n;
     int c_vec;  // C pointer, ldc and strideC allow 16-byte accesses
+    // Last-wave split: the tiles of the linear tile order (all problems of the
+    // batch, problem-major) before full_units run whole, the rest as quarter tiles.
+    int full_units;
 };
 
 // ---- PTX helpers ---------------------------------------------------------------
@@ -329,7 +339,23 @@ __device__ __forceinline__ int frag_col(int wn0, int lc, int j)
 
 // ---- The kernel ----------------------------------------------------------------
 
-template <class Cfg>
+// How a CTA finds its tile.
+enum TileMap {
+    // blockIdx.x walks the grouped tile order of problem blockIdx.z.
+    TILE_GRID = 0,
+    // One-dimensional grid: CTA t takes tile t of the linear tile order (problem-
+    // major, each problem in grouped order); the whole tiles of a split batch.
+    TILE_LINEAR = 1,
+    // One-dimensional grid: CTA 4 t' + q takes quarter q (row half q / 2, column
+    // half q % 2) of Parent-sized tile full_units + t' of the linear tile order;
+    // quarters wholly outside C do nothing.
+    TILE_QUARTER = 2,
+};
+
+// MAP and Parent select the tile of each CTA; the body is the same for every map.
+// (Moving the body into a function called from three kernels measured 1 % slower
+// at 4096^3, so the maps live here as compile-time branches.)
+template <class Cfg, int MAP = TILE_GRID, class Parent = Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(const GemmParams p)
 {
     extern __shared__ __align__(128) float smem[];
@@ -348,7 +374,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
 
     // Grouped tile order: GROUP_M consecutive tile-rows are swept column by column.
     int tile_m, tile_n;
-    {
+    int m0, n0;
+    long long bz;
+    if constexpr (MAP == TILE_GRID) {
         const int pid = blockIdx.x;
         const int per_group = Cfg::GROUP_M * p.tiles_n;
         const int group = pid / per_group;
@@ -357,9 +385,33 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
         const int in_group = pid - group * per_group;
         tile_m = first_m + in_group % rows_in_group;
         tile_n = in_group / rows_in_group;
+        m0 = tile_m * Cfg::BM;
+        n0 = tile_n * Cfg::BN;
+        bz = blockIdx.z;
+    } else {
+        static_assert(MAP != TILE_QUARTER || (Parent::BM == 2 * Cfg::BM && Parent::BN == 2 * Cfg::BN),
+                      "a quarter CTA computes one quarter of a parent tile");
+        const long long tiles = (long long)p.tiles_m * p.tiles_n;
+        const long long t = MAP == TILE_LINEAR ? (long long)blockIdx.x
+                                               : (long long)p.full_units + (blockIdx.x >> 2);
+        bz = t / tiles;
+        const int pid = (int)(t - bz * tiles);
+        const int per_group = Parent::GROUP_M * p.tiles_n;
+        const int group = pid / per_group;
+        const int first_m = group * Parent::GROUP_M;
+        const int rows_in_group = min(p.tiles_m - first_m, Parent::GROUP_M);
+        const int in_group = pid - group * per_group;
+        tile_m = first_m + in_group % rows_in_group;
+        tile_n = in_group / rows_in_group;
+        m0 = tile_m * Parent::BM;
+        n0 = tile_n * Parent::BN;
+        if constexpr (MAP == TILE_QUARTER) {
+            const int q = blockIdx.x & 3;
+            m0 += (q >> 1) * Cfg::BM;
+            n0 += (q & 1) * Cfg::BN;
+            if (m0 >= p.M || n0 >= p.N) return;  // the same for the whole CTA
+        }
     }
-    const int m0 = tile_m * Cfg::BM, n0 = tile_n * Cfg::BN;
-    const long long bz = blockIdx.z;
     const float *const A = p.A + bz * p.strideA;
     const float *const B = p.B + bz * p.strideB;
     float *const C = p.C + bz * p.strideC;

@@ -55,9 +55,21 @@ struct ConfigOf<CFG_32x32_K4, TA, TB> {
     using type = SimtCfg<32, 32, 32, 32, 16, 4, 4, 8, 2, TA, TB, true, 4>;
 };
 
-// Opt the kernel in to its dynamic shared memory once per device.
-template <class Cfg>
-static cudaError_t prepare_kernel()
+// The quarter tiles of the last-wave split: 64 x 64 with four k-groups of two
+// warps (8 x 8 per thread), so a quarter tile has the CTA size, register budget and
+// per-thread tile of a 128 x 128 tile and a quarter of its serial k-steps.  64-deep
+// stages give each k-group 16 k per stage; when both operands are transposed on
+// copy, 32-deep stages keep the element copies per thread at 16.
+template <int TA, int TB>
+struct SplitTailOf {
+    static constexpr bool BOTH_T = (TA == 0 && TB == 1);
+    using type = SimtCfg<64, 64, BOTH_T ? 32 : 64, 64, 32, 8, 8, BOTH_T ? 4 : 3, 2, TA, TB, true, 4>;
+};
+
+// Opt a kernel in to its dynamic shared memory once per device.  Tag makes the
+// once-per-device flag distinct per kernel.
+template <class Tag, class KernelFn>
+static cudaError_t prepare_kernel_fn(KernelFn kernel, int smem_bytes)
 {
     static std::atomic<unsigned long long> ready{0};
     int dev = 0;
@@ -65,14 +77,18 @@ static cudaError_t prepare_kernel()
     if (e != cudaSuccess) return e;
     const unsigned long long bit = 1ull << (dev & 63);
     if (ready.load(std::memory_order_acquire) & bit) return cudaSuccess;
-    e = cudaFuncSetAttribute(simt_gemm_kernel<Cfg>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Cfg::SMEM_BYTES);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(simt_gemm_kernel<Cfg>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                             100);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     ready.fetch_or(bit, std::memory_order_acq_rel);
     return cudaSuccess;
+}
+
+template <class Cfg>
+static cudaError_t prepare_kernel()
+{
+    return prepare_kernel_fn<Cfg>(simt_gemm_kernel<Cfg>, Cfg::SMEM_BYTES);
 }
 
 template <class Cfg>
@@ -103,6 +119,54 @@ static fgemm_status launch_simt(const GemmParams &p0, int batch, cudaStream_t st
     return FGEMM_OK;
 }
 
+// Last-wave split: the first (tiles - r) tiles of all problems whole, then the
+// last r = tiles mod SMs as quarter tiles (TILE_QUARTER), two launches on
+// the stream.
+template <class Main, class Tail>
+static fgemm_status launch_simt_split(const GemmParams &p0, int batch, cudaStream_t stream)
+{
+    struct TailTag {};
+    static_assert(Tail::THREADS == Main::THREADS, "tail CTAs fill the slots of main CTAs");
+    GemmParams p = p0;
+    p.tiles_m = (p.M + Main::BM - 1) / Main::BM;
+    p.tiles_n = (p.N + Main::BN - 1) / Main::BN;
+    const long long total = (long long)p.tiles_m * p.tiles_n * batch;
+    int sms = 0;
+    if (device_sm_count(&sms) != 0 || sms < 1) {
+        (void)cudaGetLastError();
+        return FGEMM_ERR_LAUNCH;
+    }
+    const long long rem = total % sms;
+    if (total - rem > INT_MAX || 4 * rem > INT_MAX) return FGEMM_ERR_NOT_SUPPORTED;
+    p.full_units = (int)(total - rem);
+    struct LinearTag {};
+    if (prepare_kernel<Main>() != cudaSuccess ||
+        prepare_kernel_fn<LinearTag>(simt_gemm_kernel<Main, TILE_LINEAR>, Main::SMEM_BYTES) !=
+            cudaSuccess ||
+        prepare_kernel_fn<TailTag>(simt_gemm_kernel<Tail, TILE_QUARTER, Main>, Tail::SMEM_BYTES) !=
+            cudaSuccess) {
+        (void)cudaGetLastError();
+        return FGEMM_ERR_LAUNCH;
+    }
+    if (p.full_units > 0) {
+        // One problem: the per-problem kernel over the first full_units tiles.
+        // A batch: the linear-order kernel, whose whole tiles may end inside a problem.
+        if (batch == 1)
+            simt_gemm_kernel<Main><<<(unsigned)p.full_units, Main::THREADS, Main::SMEM_BYTES,
+                                     stream>>>(p);
+        else
+            simt_gemm_kernel<Main, TILE_LINEAR><<<(unsigned)p.full_units, Main::THREADS,
+                                                 Main::SMEM_BYTES, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return FGEMM_ERR_LAUNCH;
+    }
+    if (rem > 0) {
+        simt_gemm_kernel<Tail, TILE_QUARTER, Main><<<(unsigned)(4 * rem), Tail::THREADS,
+                                                     Tail::SMEM_BYTES, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return FGEMM_ERR_LAUNCH;
+    }
+    return FGEMM_OK;
+}
+
 #define FGEMM_LAUNCH_TABLE(NAME, TA, TB)                                   \
     const LaunchFn NAME[NUM_CONFIGS] = {                                   \
         &launch_simt<ConfigOf<CFG_128x128, TA, TB>::type>,                 \
@@ -111,7 +175,9 @@ static fgemm_status launch_simt(const GemmParams &p0, int batch, cudaStream_t st
         &launch_simt<ConfigOf<CFG_64x64_SCALAR, TA, TB>::type>,            \
         &launch_simt<ConfigOf<CFG_32x32, TA, TB>::type>,                   \
         &launch_simt<ConfigOf<CFG_32x32_K4, TA, TB>::type>,                \
+        &launch_simt_split<ConfigOf<CFG_128x128, TA, TB>::type,            \
+                           SplitTailOf<TA, TB>::type>,                     \
     };                                                                     \
-    static_assert(NUM_CONFIGS == 6, "one launcher per configuration");
+    static_assert(NUM_CONFIGS == 7, "one launcher per configuration");
 
 }  // namespace fgemm

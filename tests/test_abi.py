@@ -110,7 +110,16 @@ def test_selector():
     scalar = [i for i in range(fg.num_configs()) if fg.config_name(i).endswith("_scalar")]
     assert sel(0, 0, 4096, 4096, 4096, 1, 0, 152) in scalar
     big = sel(0, 0, 4096, 4096, 4096, 1, 1, 152)
-    assert fg.config_name(big).startswith("simt_128x128")
+    # 1024 tiles on 152 SMs leave r = 112 > 152 / 2: whole tiles only
+    assert fg.config_name(big) == "simt_128x128_t8x8"
+    # 928 tiles leave r = 16 <= 76: the last-wave split; 1216 = 8 * 152 tiles: none left
+    assert fg.config_name(sel(0, 0, 4096, 3648, 4096, 1, 1, 152)) == "simt_128x128_t8x8_split"
+    assert fg.config_name(sel(0, 0, 4096, 4864, 4096, 1, 1, 152)) == "simt_128x128_t8x8"
+    # 128 problems of 16 tiles: r = 2048 mod 152 = 72 <= 76
+    assert fg.config_name(sel(0, 0, 2048, 128, 2048, 128, 1, 152)) == "simt_128x128_t8x8_split"
+    # with 148 SMs the 928 tiles leave r = 40: still split; 1024 tiles leave r = 136
+    assert fg.config_name(sel(0, 0, 4096, 3648, 4096, 1, 1, 148)) == "simt_128x128_t8x8_split"
+    assert fg.config_name(sel(0, 0, 4096, 4096, 4096, 1, 1, 148)) == "simt_128x128_t8x8"
     small = sel(0, 0, 256, 256, 256, 1, 1, 152)
     assert fg.config_name(small) == "simt_32x32x32_t4x4_s8_k4"
     assert fg.config_name(sel(0, 0, 768, 768, 768, 1, 1, 152)) == "simt_32x32x16_t4x4_s4"

@@ -17,7 +17,8 @@ pytestmark = pytest.mark.gpu
 # (M, N, K, offset of A) chosen so the selector lands on each configuration on a GPU
 # with about 150 SMs (asserted below for the GPU at hand).
 SHAPES = [
-    (1600, 1600, 40, 0, "simt_128x128_t8x8"),
+    (1600, 1600, 40, 0, "simt_128x128_t8x8_split"),
+    (2000, 2100, 40, 0, "simt_128x128_t8x8"),
     (1024, 1000, 40, 0, "simt_128x64x16_t8x8_s4"),
     (832, 840, 36, 0, "simt_64x64x16_t4x4_s4"),
     (640, 640, 24, 0, "simt_32x32x16_t4x4_s4"),
@@ -39,6 +40,10 @@ def test_row_bias_parity(M, N, K, offA, name, ta, tb, relu):
         if not 140 <= sms <= 160:
             pytest.skip("shape table assumes about 150 SMs")
         cfg = fg.select_config(ta, tb, M, N, K, 1, True, sms)
+        if name.startswith("simt_128x128"):
+            # whole tiles, or the last-wave split when tiles mod SMs is at most half the SMs
+            r = (-(-M // 128) * -(-N // 128)) % sms
+            name = "simt_128x128_t8x8" + ("_split" if 0 < r and 2 * r <= sms else "")
         assert fg.config_name(cfg) == name
     check(Case(ta=ta, tb=tb, M=M, N=N, K=K, alpha=1.0, beta=0.0, relu=relu, row_bias=True,
                offset=(offA, 0, 0), align_ld=offA == 0, seed=M + N + K))
