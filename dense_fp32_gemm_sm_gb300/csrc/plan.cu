@@ -23,7 +23,6 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
 {
     (void)ta;
     (void)tb;
-    (void)K;
     if (!aligned) return CFG_64x64_SCALAR;
     if (num_sms < 1) num_sms = 1;
     const long long b = batch > 0 ? batch : 1;
@@ -32,9 +31,13 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
         // Two CTAs per SM retire tile-pairs at the rate of lone tiles, so the last
         // r = tiles mod SMs tiles cost a whole lone-tile period.  As quarter tiles
         // they cost ceil(4r / SMs) quarter periods at about 0.7 of the whole-tile
-        // rate (measured): a gain while that is at most 2 quarters per SM.
+        // rate.  Measured on 152 SMs: a gain for r <= SMs / 2 (FC 8192x4096x11008,
+        // r = 32: +1.4 %; 4096x2560x4096, r = 32: +14 %), and for r <= 3/4 SMs when
+        // K >= 4096 (4096^3, r = 112: +0.8 %); a loss above 3/4 (3072^3, r = 120:
+        // -5.7 %) and at r = 104 with K = 2048 (2048^3: -1.2 %).
         const long long r = tiles % num_sms;
-        if (r > 0 && 2 * r <= num_sms) return CFG_128x128_SPLIT;
+        if (r > 0 && (2 * r <= num_sms || (4 * r <= 3LL * num_sms && K >= 4096)))
+            return CFG_128x128_SPLIT;
         return CFG_128x128;
     }
     // 128 x 64 tiles (8 x 8 per thread) beat twice as many 64 x 64 tiles (4 x 4 per

@@ -110,8 +110,11 @@ def test_selector():
     scalar = [i for i in range(fg.num_configs()) if fg.config_name(i).endswith("_scalar")]
     assert sel(0, 0, 4096, 4096, 4096, 1, 0, 152) in scalar
     big = sel(0, 0, 4096, 4096, 4096, 1, 1, 152)
-    # 1024 tiles on 152 SMs leave r = 112 > 152 / 2: whole tiles only
-    assert fg.config_name(big) == "simt_128x128_t8x8"
+    # 1024 tiles on 152 SMs leave r = 112: above 152 / 2 but within 3/4 with K >= 4096
+    assert fg.config_name(big) == "simt_128x128_t8x8_split"
+    assert fg.config_name(sel(0, 0, 4096, 4096, 2048, 1, 1, 152)) == "simt_128x128_t8x8"
+    # 576 tiles leave r = 120 > 114: whole tiles only, whatever K
+    assert fg.config_name(sel(0, 0, 3072, 3072, 8192, 1, 1, 152)) == "simt_128x128_t8x8"
     # 928 tiles leave r = 16 <= 76: the last-wave split; 1216 = 8 * 152 tiles: none left
     assert fg.config_name(sel(0, 0, 4096, 3648, 4096, 1, 1, 152)) == "simt_128x128_t8x8_split"
     assert fg.config_name(sel(0, 0, 4096, 4864, 4096, 1, 1, 152)) == "simt_128x128_t8x8"
@@ -123,8 +126,9 @@ def test_selector():
     small = sel(0, 0, 256, 256, 256, 1, 1, 152)
     assert fg.config_name(small) == "simt_32x32x32_t4x4_s8_k4"
     assert fg.config_name(sel(0, 0, 768, 768, 768, 1, 1, 152)) == "simt_32x32x16_t4x4_s4"
-    # a batch of small problems fills the GPU with the large tile
-    assert sel(0, 1, 2048, 2048, 128, 128, 1, 152) == big
+    # a batch of small problems fills the GPU with the large tile (32768 tiles, r = 88,
+    # K = 128: whole tiles)
+    assert fg.config_name(sel(0, 1, 2048, 2048, 128, 128, 1, 152)) == "simt_128x128_t8x8"
     assert sel(0, 0, -1, 4, 4, 1, 1, 152) == -1
     for ta in (0, 1):
         for tb in (0, 1):

@@ -83,8 +83,10 @@ def test_no_remainder_runs_whole_tiles_only():
 
 def test_selector_splits_when_the_remainder_is_small():
     sms = _sms()
-    for M, N, batch in ((4096, 4096, 1), (1700, 1650, 1), (2048, 2048, 128), (1000, 990, 5)):
+    for M, N, K, batch in ((4096, 4096, 4096, 1), (4096, 4096, 64, 1), (1700, 1650, 64, 1),
+                           (2048, 2048, 128, 128), (1000, 990, 64, 5), (3072, 3072, 8192, 1)):
         tiles = _tiles(M, N, batch)
         r = tiles % sms
-        want = "simt_128x128_t8x8_split" if (r > 0 and 2 * r <= sms) else "simt_128x128_t8x8"
-        assert fg.config_name(fg.select_config(0, 0, M, N, 64, batch, True, sms)) == want
+        split = r > 0 and (2 * r <= sms or (4 * r <= 3 * sms and K >= 4096))
+        want = "simt_128x128_t8x8_split" if split else "simt_128x128_t8x8"
+        assert fg.config_name(fg.select_config(0, 0, M, N, K, batch, True, sms)) == want
