@@ -3,7 +3,8 @@
 //
 // Size classes follow GEMM 优化详解, "矩阵大小选择策略" (small matrices get small
 // blocks, large ones large blocks), re-derived for a GPU whose SM count is read at
-// run time: the largest tile that still gives every SM a CTA is used.
+// run time: each configuration's launch time is estimated from its CTA count per SM
+// and K with a fitted model, and the fastest is used.
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -16,42 +17,99 @@ namespace {
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
+// Time model of one launch, fitted to CUDA-event times (L2 flushed) of every
+// configuration in each transpose layout on 31 shapes (M = N from 256 to 2048 and
+// rectangular ones, K from 256 to 4096) on a 152-SM GB300 at 2070 MHz:
+//
+//     t(us) = a + aK * K + K * max(n * b, L),   n = ceil(CTAs / SMs)
+//
+// n is the number of CTAs the busiest SM runs (the hardware spreads a grid over
+// the SMs breadth-first); b is the time per k of one CTA's share of a busy SM and L
+// the per-k latency floor of a CTA that has an SM to itself.  Chosen by the model,
+// the fitted shapes lose 0.25 % on average (4.5 % at most) against the fastest
+// configuration, and 32 random shapes not used in the fit (all layouts, batches of
+// 1 and 3, K from 64 to 6000) 1.4 % on average (27 % at most, one NT shape).  The
+// model also predicts 4096^3 (2188 us whole tiles, 2185 us split; measured 2201 and
+// 2183), 3072^3, 2048^3 and the FC and PV workloads to within 2 %.
+struct LaunchModel {
+    double a, aK, b, L;
+};
+enum ModelSlot { M_128x128, M_128x64, M_64x64, M_32x32, M_32x32_K4, M_QUARTER, NUM_SLOTS };
+constexpr LaunchModel kModel[4][NUM_SLOTS] = {
+    {  // op(A) N, op(B) N
+        {9.26, 0.00815, 0.07485, 0.0000},  // 128x128
+        {9.78, -0.00270, 0.04241, 0.0475},  // 128x64
+        {7.39, -0.00198, 0.02840, 0.0310},  // 64x64
+        {7.30, 0.00285, 0.00781, 0.0140},  // 32x32
+        {7.59, -0.00037, 0.00961, 0.0000},  // 32x32 k4
+        {10.91, -0.00391, 0.02504, 0.0290},  // quarter
+    },
+    {  // op(A) N, op(B) T
+        {9.31, 0.02485, 0.07644, 0.0000},  // 128x128
+        {9.88, 0.00193, 0.04351, 0.0465},  // 128x64
+        {6.80, -0.00429, 0.03358, 0.0380},  // 64x64
+        {7.15, -0.00007, 0.01026, 0.0185},  // 32x32
+        {8.87, -0.00377, 0.01162, 0.0145},  // 32x32 k4
+        {10.34, -0.00607, 0.03031, 0.0360},  // quarter
+    },
+    {  // op(A) T, op(B) N
+        {9.35, 0.00555, 0.07214, 0.0000},  // 128x128
+        {9.94, -0.02056, 0.04543, 0.0605},  // 128x64
+        {7.33, 0.00335, 0.02171, 0.0000},  // 64x64
+        {7.57, 0.00052, 0.00588, 0.0170},  // 32x32
+        {8.28, -0.00109, 0.00749, 0.0085},  // 32x32 k4
+        {10.38, -0.00499, 0.02380, 0.0285},  // quarter
+    },
+    {  // op(A) T, op(B) T
+        {8.99, 0.00259, 0.07926, 0.0000},  // 128x128
+        {10.03, 0.00503, 0.03817, 0.0000},  // 128x64
+        {7.51, -0.00213, 0.02800, 0.0320},  // 64x64
+        {7.52, 0.00109, 0.00790, 0.0150},  // 32x32
+        {8.39, -0.00052, 0.00910, 0.0000},  // 32x32 k4
+        {10.74, -0.00425, 0.02599, 0.0305},  // quarter
+    },
+};
+
+double model_us(const LaunchModel &m, long long ctas, long long K, int num_sms)
+{
+    const double n = (double)ceil_div(ctas, num_sms);
+    const double per_k = n * m.b > m.L ? n * m.b : m.L;
+    return m.a + m.aK * (double)K + (double)K * per_k;
+}
+
 }  // namespace
 
 int select_config(int ta, int tb, long long M, long long N, long long K, long long batch,
                   bool aligned, int num_sms)
 {
-    (void)ta;
-    (void)tb;
     if (!aligned) return CFG_64x64_SCALAR;
     if (num_sms < 1) num_sms = 1;
     const long long b = batch > 0 ? batch : 1;
-    const long long tiles = ceil_div(M, 128) * ceil_div(N, 128) * b;
-    if (tiles >= num_sms) {
-        // Two CTAs per SM retire tile-pairs at the rate of lone tiles, so the last
-        // r = tiles mod SMs tiles cost a whole lone-tile period.  As quarter tiles
-        // they cost ceil(4r / SMs) quarter periods at about 0.7 of the whole-tile
-        // rate.  Measured on 152 SMs: a gain for r <= SMs / 2 (FC 8192x4096x11008,
-        // r = 32: +1.4 %; 4096x2560x4096, r = 32: +14 %), and for r <= 3/4 SMs when
-        // K >= 4096 (4096^3, r = 112: +0.8 %); a loss above 3/4 (3072^3, r = 120:
-        // -5.7 %) and at r = 104 with K = 2048 (2048^3: -1.2 %).
-        const long long r = tiles % num_sms;
-        if (r > 0 && (2 * r <= num_sms || (4 * r <= 3LL * num_sms && K >= 4096)))
-            return CFG_128x128_SPLIT;
-        return CFG_128x128;
-    }
-    // 128 x 64 tiles (8 x 8 per thread) beat twice as many 64 x 64 tiles (4 x 4 per
-    // thread) as long as they still occupy most SMs (measured: 1024^2, 128 tiles on
-    // 152 SMs, 34.8 vs 28.3 TFLOP/s).
-    if (ceil_div(M, 128) * ceil_div(N, 64) * b * 5 >= (long long)num_sms * 4) return CFG_128x64;
-    // Tiny problems are latency-bound: more, smaller CTAs finish sooner (256^3: 8.2 us
-    // with 32 x 32 tiles against 12.4 us with 64 x 64).
-    if (ceil_div(M, 64) * ceil_div(N, 64) * b >= num_sms) return CFG_64x64;
-    // Up to about two 32 x 32 tiles per SM, four k-groups per tile shorten the serial
-    // chain (512^3, 256 tiles: 14.4 us against 16.4 back to back); beyond that the
-    // one-group tile wins (768^3, 576 tiles: 35.5 us against 39.6).
-    if (ceil_div(M, 32) * ceil_div(N, 32) * b <= 2LL * num_sms) return CFG_32x32_K4;
-    return CFG_32x32;
+    const long long k = K > 0 ? K : 0;
+    const long long tiles128 = ceil_div(M, 128) * ceil_div(N, 128) * b;
+    // The last-wave split: whole 128 x 128 tiles for all but r = tiles mod SMs,
+    // then those r as 4r quarter tiles (a second launch; none when r = 0).
+    const long long r = tiles128 % num_sms, whole = tiles128 - r;
+    const LaunchModel *const mm = kModel[(ta ? 2 : 0) + (tb ? 1 : 0)];
+    double split = 0.0;
+    if (whole > 0) split += model_us(mm[M_128x128], whole, k, num_sms);
+    if (r > 0) split += model_us(mm[M_QUARTER], 4 * r, k, num_sms);
+    struct Option {
+        int config;
+        double us;
+    };
+    const Option options[] = {
+        {CFG_128x128, model_us(mm[M_128x128], tiles128, k, num_sms)},
+        {CFG_128x128_SPLIT, r > 0 ? split : 1e300},
+        {CFG_128x64, model_us(mm[M_128x64], ceil_div(M, 128) * ceil_div(N, 64) * b, k, num_sms)},
+        {CFG_64x64, model_us(mm[M_64x64], ceil_div(M, 64) * ceil_div(N, 64) * b, k, num_sms)},
+        {CFG_32x32, model_us(mm[M_32x32], ceil_div(M, 32) * ceil_div(N, 32) * b, k, num_sms)},
+        {CFG_32x32_K4, model_us(mm[M_32x32_K4], ceil_div(M, 32) * ceil_div(N, 32) * b, k, num_sms)},
+    };
+    Option best = options[0];
+    for (const Option &o : options)
+        if (o.us < best.us) best = o;
+    return best.config;
 }
 
 int device_sm_count(int *out)

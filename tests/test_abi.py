@@ -107,35 +107,36 @@ def test_explicit_vector_config_refuses_unaligned():
 
 def test_selector():
     sel = fg.select_config
+    name = lambda *a: fg.config_name(sel(*a))
     scalar = [i for i in range(fg.num_configs()) if fg.config_name(i).endswith("_scalar")]
     assert sel(0, 0, 4096, 4096, 4096, 1, 0, 152) in scalar
-    big = sel(0, 0, 4096, 4096, 4096, 1, 1, 152)
-    # 1024 tiles on 152 SMs leave r = 112: above 152 / 2 but within 3/4 with K >= 4096
-    assert fg.config_name(big) == "simt_128x128_t8x8_split"
-    assert fg.config_name(sel(0, 0, 4096, 4096, 2048, 1, 1, 152)) == "simt_128x128_t8x8"
-    # 576 tiles leave r = 120 > 114: whole tiles only, whatever K
-    assert fg.config_name(sel(0, 0, 3072, 3072, 8192, 1, 1, 152)) == "simt_128x128_t8x8"
-    # 928 tiles leave r = 16 <= 76: the last-wave split; 1216 = 8 * 152 tiles: none left
-    assert fg.config_name(sel(0, 0, 4096, 3648, 4096, 1, 1, 152)) == "simt_128x128_t8x8_split"
-    assert fg.config_name(sel(0, 0, 4096, 4864, 4096, 1, 1, 152)) == "simt_128x128_t8x8"
-    # 128 problems of 16 tiles: r = 2048 mod 152 = 72 <= 76
-    assert fg.config_name(sel(0, 0, 2048, 128, 2048, 128, 1, 152)) == "simt_128x128_t8x8_split"
-    # with 148 SMs the 928 tiles leave r = 40: still split; 1024 tiles leave r = 136
-    assert fg.config_name(sel(0, 0, 4096, 3648, 4096, 1, 1, 148)) == "simt_128x128_t8x8_split"
-    assert fg.config_name(sel(0, 0, 4096, 4096, 4096, 1, 1, 148)) == "simt_128x128_t8x8"
-    small = sel(0, 0, 256, 256, 256, 1, 1, 152)
-    assert fg.config_name(small) == "simt_32x32x32_t4x4_s8_k4"
-    assert fg.config_name(sel(0, 0, 768, 768, 768, 1, 1, 152)) == "simt_32x32x16_t4x4_s4"
-    # a batch of small problems fills the GPU with the large tile (32768 tiles, r = 88,
-    # K = 128: whole tiles)
-    assert fg.config_name(sel(0, 1, 2048, 2048, 128, 128, 1, 152)) == "simt_128x128_t8x8"
+    # Choices of the fitted launch-time model on 152 SMs (each measured fastest, or
+    # within 1 %, on a GB300):
+    assert name(0, 0, 4096, 4096, 4096, 1, 1, 152) == "simt_128x128_t8x8_split"  # r = 112
+    assert name(0, 0, 4096, 4864, 4096, 1, 1, 152) == "simt_128x128_t8x8"  # 8 x 152 tiles
+    assert name(0, 0, 4096, 3648, 4096, 1, 1, 152) == "simt_128x128_t8x8_split"  # r = 16
+    assert name(0, 0, 3072, 3072, 3072, 1, 1, 152) == "simt_128x128_t8x8"  # r = 120
+    assert name(0, 0, 2048, 2048, 2048, 1, 1, 152) == "simt_128x128_t8x8"
+    assert name(0, 0, 1792, 1792, 1024, 1, 1, 152) == "simt_128x64x16_t8x8_s4"
+    assert name(0, 0, 1280, 1280, 4096, 1, 1, 152) == "simt_128x128_t8x8_split"  # all quarters
+    assert name(0, 0, 1024, 1024, 1024, 1, 1, 152) == "simt_128x64x16_t8x8_s4"
+    assert name(0, 0, 896, 896, 4096, 1, 1, 152) == "simt_128x64x16_t8x8_s4"
+    assert name(0, 0, 768, 768, 768, 1, 1, 152) == "simt_64x64x16_t4x4_s4"
+    assert name(0, 0, 640, 640, 640, 1, 1, 152) == "simt_32x32x16_t4x4_s4"
+    assert name(0, 0, 256, 256, 256, 1, 1, 152) == "simt_32x32x32_t4x4_s8_k4"
+    # batches: QK^T (32768 tiles, r = 88, K = 128) whole; Score x V (2048 tiles, r = 72)
+    assert name(0, 1, 2048, 2048, 128, 128, 1, 152) == "simt_128x128_t8x8"
+    assert name(0, 0, 2048, 128, 2048, 128, 1, 152) == "simt_128x128_t8x8_split"
+    # the SM count enters: 1024 tiles on 148 SMs leave r = 136
+    assert name(0, 0, 4096, 4096, 4096, 1, 1, 148) == "simt_128x128_t8x8"
     assert sel(0, 0, -1, 4, 4, 1, 1, 152) == -1
     for ta in (0, 1):
         for tb in (0, 1):
             for n in (1, 7, 64, 255, 1000, 5000):
-                c = sel(ta, tb, n, n, n, 1, 1, 152)
-                assert 0 <= c < fg.num_configs()
-
+                for k in (0, 1, 100, 5000):
+                    for sms in (1, 16, 152, 1000):
+                        c = sel(ta, tb, n, n, k, 1, 1, sms)
+                        assert 0 <= c < fg.num_configs() and c not in scalar
 
 
 def test_gemm_math_validates_before_launch():

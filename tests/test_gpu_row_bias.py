@@ -14,39 +14,44 @@ from gpu_harness import Case, check
 
 pytestmark = pytest.mark.gpu
 
-# (M, N, K, offset of A) chosen so the selector lands on each configuration on a GPU
-# with about 150 SMs (asserted below for the GPU at hand).
-SHAPES = [
-    (1600, 1600, 40, 0, "simt_128x128_t8x8_split"),
-    (2000, 2100, 40, 0, "simt_128x128_t8x8"),
-    (1024, 1000, 40, 0, "simt_128x64x16_t8x8_s4"),
-    (832, 840, 36, 0, "simt_64x64x16_t4x4_s4"),
-    (640, 640, 24, 0, "simt_32x32x16_t4x4_s4"),
-    (100, 70, 33, 0, "simt_32x32x32_t4x4_s8_k4"),
-    (130, 77, 45, 1, "simt_64x64x16_t4x4_s4_scalar"),
-]
+# The row-bias entry point has no configuration argument: the selector picks one.
+# For each configuration and layout the test takes the smallest shape of this list
+# on which the selector, at this GPU's SM count, picks that configuration.
+CANDIDATES = sorted(
+    ((M, N, K) for K in (40, 64, 100, 256, 512) for M in range(96, 2500, 100)
+     for N in (M, M + 36, 2 * M + 10)),
+    key=lambda s: s[0] * s[1] * s[2])
+TARGETS = ["simt_128x128_t8x8", "simt_128x128_t8x8_split", "simt_128x64x16_t8x8_s4",
+           "simt_64x64x16_t4x4_s4", "simt_32x32x16_t4x4_s4", "simt_32x32x32_t4x4_s8_k4"]
 
 
 def _sms():
     return torch.cuda.get_device_properties(0).multi_processor_count
 
 
-@pytest.mark.parametrize("M,N,K,offA,name", SHAPES)
+def _shape_for(name, ta, tb):
+    sms = _sms()
+    for M, N, K in CANDIDATES:
+        if fg.config_name(fg.select_config(ta, tb, M, N, K, 1, True, sms)) == name:
+            return M, N, K
+    raise AssertionError("the selector never picks %s for layout %d%d" % (name, ta, tb))
+
+
+@pytest.mark.parametrize("name", TARGETS)
 @pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1), (1, 0), (1, 1)])
 @pytest.mark.parametrize("relu", [False, True])
-def test_row_bias_parity(M, N, K, offA, name, ta, tb, relu):
-    if offA == 0:
-        sms = _sms()
-        if not 140 <= sms <= 160:
-            pytest.skip("shape table assumes about 150 SMs")
-        cfg = fg.select_config(ta, tb, M, N, K, 1, True, sms)
-        if name.startswith("simt_128x128"):
-            # whole tiles, or the last-wave split when tiles mod SMs is at most half the SMs
-            r = (-(-M // 128) * -(-N // 128)) % sms
-            name = "simt_128x128_t8x8" + ("_split" if 0 < r and 2 * r <= sms else "")
-        assert fg.config_name(cfg) == name
+def test_row_bias_parity(name, ta, tb, relu):
+    M, N, K = _shape_for(name, ta, tb)
     check(Case(ta=ta, tb=tb, M=M, N=N, K=K, alpha=1.0, beta=0.0, relu=relu, row_bias=True,
-               offset=(offA, 0, 0), align_ld=offA == 0, seed=M + N + K))
+               seed=M + N + K))
+
+
+@pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1), (1, 0), (1, 1)])
+def test_row_bias_unaligned_takes_the_scalar_config(ta, tb):
+    assert fg.config_name(fg.select_config(ta, tb, 130, 77, 45, 1, False, _sms())).endswith(
+        "_scalar")
+    check(Case(ta=ta, tb=tb, M=130, N=77, K=45, relu=True, row_bias=True, offset=(1, 0, 0),
+               align_ld=False, seed=252))
 
 
 @pytest.mark.parametrize("alpha,beta", [(2.0, 1.0), (0.0, -1.0), (-1.0, 0.5)])
