@@ -453,8 +453,8 @@ def run_fgemm(args, rank, world, local_rank):
         chosen = fg.select_config(w.ta, w.tb, w.M, w.N, w.K, max(1, w.batch), aligned, sms)
     kernel_name = fg.config_name(chosen)
     n_batch_launches = (max(1, w.batch) + 65534) // 65535
-    if kernel_name.endswith("_split"):
-        # whole 128 x 128 tiles, then the last (tiles mod SMs) as quarter tiles
+    if kernel_name.endswith(("_split", "_ksplit")):
+        # whole 128 x 128 tiles, then the last (tiles mod SMs) as quarter tiles or k-slices
         total = -(-w.M // 128) * -(-w.N // 128) * max(1, w.batch)
         n_batch_launches = int(total - total % sms > 0) + int(total % sms > 0)
     if splitk is not None:  # partial GEMMs (one or two launches) + the reduction
@@ -494,9 +494,11 @@ def run_fgemm(args, rank, world, local_rank):
                     "max": round(max(step_ms), 5)},
         "build": build_info(),
     }
-    if kernel_name.endswith("_split") and not tensor_path:
+    if kernel_name.endswith(("_split", "_ksplit")) and not tensor_path:
         line["roofline"]["kernels"] = ("two launches of simt_gemm_kernel (whole tiles, then the "
-                                       "quarter tiles of the last wave), timed together as one call")
+                                       "last wave's tiles as %s), timed together as one call" % (
+                                           "k-slice clusters" if kernel_name.endswith("_ksplit")
+                                           else "quarter tiles"))
     if back_to_back is not None:
         line["back_to_back"] = back_to_back
     if tensor_path:

@@ -25,7 +25,9 @@ enum ConfigId {
                             // (the smallest grids: a quarter of the serial k-steps per thread)
     CFG_128x128_SPLIT = 6,  // CFG_128x128 for all but the last (tiles mod SMs) tiles, which
                             // then run as 64x64 quarters with four k-groups (second launch)
-    NUM_CONFIGS = 7,
+    CFG_128x128_KSPLIT = 7, // CFG_128x128 for all but the last (tiles mod SMs) tiles, which
+                            // then run as clusters of four k-slices of whole tiles (second launch)
+    NUM_CONFIGS = 8,
 };
 
 struct ConfigInfo {

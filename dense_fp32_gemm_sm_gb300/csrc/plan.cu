@@ -70,11 +70,25 @@ constexpr LaunchModel kModel[4][NUM_SLOTS] = {
     },
 };
 
+double model_n_us(const LaunchModel &m, long long n, double K)
+{
+    const double per_k = (double)n * m.b > m.L ? (double)n * m.b : m.L;
+    return m.a + m.aK * K + K * per_k;
+}
+
 double model_us(const LaunchModel &m, long long ctas, long long K, int num_sms)
 {
-    const double n = (double)ceil_div(ctas, num_sms);
-    const double per_k = n * m.b > m.L ? n * m.b : m.L;
-    return m.a + m.aK * (double)K + (double)K * per_k;
+    return model_n_us(m, ceil_div(ctas, num_sms), (double)K);
+}
+
+// Clusters of four k-slice CTAs that run at once with one CTA per SM.  Measured on
+// 152 SMs: 74 clusters of four are resident at two CTAs per SM (296 CTAs, not 304:
+// a cluster stays inside one GPC), and the k-split tail of r tiles takes
+// ceil(r / 37) rounds of a quarter of a whole-tile period.
+long long ksplit_clusters_per_round(int num_sms)
+{
+    const long long c = num_sms / 4 - 1;
+    return c > 0 ? c : 1;
 }
 
 }  // namespace
@@ -91,9 +105,13 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
     // then those r as 4r quarter tiles (a second launch; none when r = 0).
     const long long r = tiles128 % num_sms, whole = tiles128 - r;
     const LaunchModel *const mm = kModel[(ta ? 2 : 0) + (tb ? 1 : 0)];
-    double split = 0.0;
-    if (whole > 0) split += model_us(mm[M_128x128], whole, k, num_sms);
-    if (r > 0) split += model_us(mm[M_QUARTER], 4 * r, k, num_sms);
+    const double main_us = whole > 0 ? model_us(mm[M_128x128], whole, k, num_sms) : 0.0;
+    // quarter tiles: 4r CTAs of the quarter model
+    const double split = main_us + (r > 0 ? model_us(mm[M_QUARTER], 4 * r, k, num_sms) : 0.0);
+    // k-split tiles: whole-tile CTAs over K / 4 each, in rounds of clusters (measured
+    // within 2-7 % of the whole-tile model at K / 4 on 152 SMs)
+    const long long rounds = ceil_div(r, ksplit_clusters_per_round(num_sms));
+    const double ksplit = main_us + (r > 0 ? model_n_us(mm[M_128x128], rounds, (double)k / 4.0) : 0.0);
     struct Option {
         int config;
         double us;
@@ -101,6 +119,7 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
     const Option options[] = {
         {CFG_128x128, model_us(mm[M_128x128], tiles128, k, num_sms)},
         {CFG_128x128_SPLIT, r > 0 ? split : 1e300},
+        {CFG_128x128_KSPLIT, r > 0 ? ksplit : 1e300},
         {CFG_128x64, model_us(mm[M_128x64], ceil_div(M, 128) * ceil_div(N, 64) * b, k, num_sms)},
         {CFG_64x64, model_us(mm[M_64x64], ceil_div(M, 64) * ceil_div(N, 64) * b, k, num_sms)},
         {CFG_32x32, model_us(mm[M_32x32], ceil_div(M, 32) * ceil_div(N, 32) * b, k, num_sms)},

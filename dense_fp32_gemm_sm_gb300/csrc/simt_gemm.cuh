@@ -96,6 +96,34 @@ __device__ __forceinline__ void cp_async_commit()
     asm volatile("cp.async.commit_group;\n" ::: "memory");
 }
 
+// Thread-block cluster helpers (sm_90+): this CTA's rank, a cluster-wide barrier
+// with release/acquire ordering of shared-memory writes, and a 16-byte load from
+// the shared memory of CTA `rank` at the address a local variable has there.
+__device__ __forceinline__ unsigned cluster_rank()
+{
+    unsigned r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n"
+                 "barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ float4 ld_cluster_f4(uint32_t local_addr, unsigned rank)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local_addr), "r"(rank));
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(remote)
+                 : "memory");
+    return v;
+}
+
 template <int N>
 __device__ __forceinline__ void cp_async_wait()
 {
@@ -299,10 +327,10 @@ struct StageCopy {
     }
 
     __device__ __forceinline__ void issue(uint32_t sA, uint32_t sB, const GemmParams &p,
-                                          const float *A, const float *B, int k0, int tid)
+                                          const float *A, const float *B, int k0, int K, int tid)
     {
-        a.issue(sA, A, p.lda, k0, p.K, tid);
-        b.issue(sB, B, p.ldb, k0, p.K, tid);
+        a.issue(sA, A, p.lda, k0, K, tid);
+        b.issue(sB, B, p.ldb, k0, K, tid);
     }
 };
 
@@ -350,7 +378,13 @@ enum TileMap {
     // half q % 2) of Parent-sized tile full_units + t' of the linear tile order;
     // quarters wholly outside C do nothing.
     TILE_QUARTER = 2,
+    // One-dimensional grid in clusters of KSPLIT CTAs: the CTAs of cluster t' each
+    // multiply one k-slice of tile full_units + t' of the linear tile order, then
+    // add their partial sums through distributed shared memory in slice order and
+    // write the tile, a 1/KSPLIT band of rows each.
+    TILE_KSPLIT = 3,
 };
+constexpr int KSPLIT = 4;
 
 // MAP and Parent select the tile of each CTA; the body is the same for every map.
 // (Moving the body into a function called from three kernels measured 1 % slower
@@ -394,6 +428,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
         const long long tiles = (long long)p.tiles_m * p.tiles_n;
         const long long t = MAP == TILE_LINEAR ? (long long)blockIdx.x
                                                : (long long)p.full_units + (blockIdx.x >> 2);
+        static_assert(MAP != TILE_KSPLIT || KSPLIT == 4, "k-slice CTAs are numbered 4 t' + slice");
         bz = t / tiles;
         const int pid = (int)(t - bz * tiles);
         const int per_group = Parent::GROUP_M * p.tiles_n;
@@ -412,8 +447,19 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
             if (m0 >= p.M || n0 >= p.N) return;  // the same for the whole CTA
         }
     }
-    const float *const A = p.A + bz * p.strideA;
-    const float *const B = p.B + bz * p.strideB;
+    // k range of this CTA: all of K, or one k-slice (whole stages) of a k-split tile.
+    int k_len = p.K;
+    long long a_koff = 0, b_koff = 0;
+    if constexpr (MAP == TILE_KSPLIT) {
+        const int slice = (int)cluster_rank();
+        const int per = ((p.K + KSPLIT - 1) / KSPLIT + Cfg::BK - 1) / Cfg::BK * Cfg::BK;
+        const int kb = min(p.K, slice * per);
+        k_len = min(p.K - kb, per);
+        a_koff = Cfg::TA ? (long long)kb * p.lda : kb;
+        b_koff = Cfg::TB ? kb : (long long)kb * p.ldb;
+    }
+    const float *const A = p.A + bz * p.strideA + a_koff;
+    const float *const B = p.B + bz * p.strideB + b_koff;
     float *const C = p.C + bz * p.strideC;
 
     float2 acc[TM][TN / 2];  // acc[i][j] = (c[i][2j], c[i][2j+1])
@@ -423,7 +469,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
         for (int j = 0; j < TN / 2; ++j) acc[i][j] = make_float2(0.0f, 0.0f);
 
     const uint32_t sA_base = smem_addr(sA_all), sB_base = smem_addr(sB_all);
-    const int KT = (p.K + Cfg::BK - 1) / Cfg::BK;
+    const int KT = (k_len + Cfg::BK - 1) / Cfg::BK;
 
     if (KT > 0) {
         StageCopy<Cfg> copy;
@@ -433,7 +479,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
         for (int s = 0; s < Cfg::STAGES - 1; ++s) {
             if (s < KT)
                 copy.issue(sA_base + s * Cfg::A_STAGE * 4, sB_base + s * Cfg::B_STAGE * 4, p, A, B,
-                           s * Cfg::BK, tid);
+                           s * Cfg::BK, k_len, tid);
             cp_async_commit();
         }
         cp_async_wait<Cfg::STAGES - 2>();
@@ -473,7 +519,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
                         int ws = slot + Cfg::STAGES - 1;
                         if (ws >= Cfg::STAGES) ws -= Cfg::STAGES;
                         copy.issue(sA_base + ws * Cfg::A_STAGE * 4, sB_base + ws * Cfg::B_STAGE * 4,
-                                   p, A, B, nk * Cfg::BK, tid);
+                                   p, A, B, nk * Cfg::BK, k_len, tid);
                     }
                     cp_async_commit();
                 }
@@ -524,6 +570,88 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
             }
         }
         if (kg != 0) return;
+    }
+
+    // ---- k-split tiles: partial sums through distributed shared memory.  Every CTA
+    // of the cluster stores its slice's sums in its own shared memory (the stage
+    // buffers are free once every warp is past the barrier); after a cluster barrier
+    // CTA `slice` adds the four partials of its band of rows in slice order, so the
+    // result does not depend on timing, and applies the epilogue of the whole tile.
+    if constexpr (MAP == TILE_KSPLIT) {
+        constexpr int P_LD = Cfg::BN + 4;
+        constexpr int BAND = Cfg::BM / KSPLIT;  // rows each CTA reduces and writes
+        constexpr int C4 = Cfg::BN / 4;         // 16-byte chunks per row
+        constexpr int ITER = BAND * C4 / Cfg::THREADS;
+        static_assert(Cfg::KS == 1, "one k-group per slice");
+        static_assert(Cfg::BM * P_LD * 4 <= Cfg::SMEM_BYTES, "the partial tile fits the stages");
+        static_assert(Cfg::BM % KSPLIT == 0 && (BAND * C4) % Cfg::THREADS == 0,
+                      "the bands divide over the threads");
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int r = frag_row<Cfg>(wm0, lr, i);
+#pragma unroll
+            for (int g = 0; g < TN / 4; ++g)
+                *reinterpret_cast<float4 *>(smem + r * P_LD + frag_col<Cfg>(wn0, lc, 4 * g)) =
+                    make_float4(acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
+                                acc[i][2 * g + 1].y);
+        }
+        cluster_sync();
+        const int band0 = (int)cluster_rank() * BAND;
+        const bool products = p.K > 0;
+        const bool has_bias = p.bias != nullptr, has_row_bias = p.row_bias != nullptr;
+        const uint32_t base = smem_addr(smem);
+#pragma unroll
+        for (int it = 0; it < ITER; ++it) {
+            const int e = it * Cfg::THREADS + tid;
+            const int r = band0 + e / C4, c = (e % C4) * 4;
+            const uint32_t la = base + (uint32_t)(r * P_LD + c) * 4u;
+            float4 sum = ld_cluster_f4(la, 0);
+#pragma unroll
+            for (unsigned q = 1; q < (unsigned)KSPLIT; ++q) {
+                const float4 w = ld_cluster_f4(la, q);
+                sum.x += w.x;
+                sum.y += w.y;
+                sum.z += w.z;
+                sum.w += w.w;
+            }
+            const int gr = m0 + r, gc = n0 + c;
+            if (gr >= p.M || gc >= p.N) continue;
+            float v[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) v[q] = products ? p.alpha * v[q] : 0.0f;
+            float *const dst = C + (long long)gr * p.ldc + gc;
+            const float rb = has_row_bias ? __ldg(p.row_bias + gr) : 0.0f;
+            if (p.c_vec && gc + 3 < p.N) {
+                if (p.beta != 0.0f) {
+                    const float4 c0 = *reinterpret_cast<const float4 *>(dst);
+                    v[0] = fmaf(p.beta, c0.x, v[0]);
+                    v[1] = fmaf(p.beta, c0.y, v[1]);
+                    v[2] = fmaf(p.beta, c0.z, v[2]);
+                    v[3] = fmaf(p.beta, c0.w, v[3]);
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (has_bias) v[q] += __ldg(p.bias + gc + q);
+                    if (has_row_bias) v[q] += rb;
+                    if (p.relu) v[q] = fmaxf(v[q], 0.0f);
+                }
+                *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+            } else {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    if (gc + q >= p.N) break;
+                    float o = v[q];
+                    if (p.beta != 0.0f) o = fmaf(p.beta, dst[q], o);
+                    if (has_bias) o += __ldg(p.bias + gc + q);
+                    if (has_row_bias) o += rb;
+                    if (p.relu) o = fmaxf(o, 0.0f);
+                    dst[q] = o;
+                }
+            }
+        }
+        cluster_sync();  // no CTA leaves while another still reads its shared memory
+        return;
     }
 
     // ---- Epilogue: alpha, beta, bias, ReLU in registers; vector stores where possible.

@@ -167,6 +167,64 @@ static fgemm_status launch_simt_split(const GemmParams &p0, int batch, cudaStrea
     return FGEMM_OK;
 }
 
+// Last-wave k-split: the first (tiles - r) tiles whole, then each of the last
+// r = tiles mod SMs tiles as a cluster of KSPLIT CTAs, one k-slice each, reduced
+// through distributed shared memory (TILE_KSPLIT); two launches on the stream.
+template <class Main>
+static fgemm_status launch_simt_ksplit(const GemmParams &p0, int batch, cudaStream_t stream)
+{
+    struct LinearTag {};
+    struct KsplitTag {};
+    GemmParams p = p0;
+    p.tiles_m = (p.M + Main::BM - 1) / Main::BM;
+    p.tiles_n = (p.N + Main::BN - 1) / Main::BN;
+    const long long total = (long long)p.tiles_m * p.tiles_n * batch;
+    int sms = 0;
+    if (device_sm_count(&sms) != 0 || sms < 1) {
+        (void)cudaGetLastError();
+        return FGEMM_ERR_LAUNCH;
+    }
+    const long long rem = total % sms;
+    if (total - rem > INT_MAX || KSPLIT * rem > INT_MAX) return FGEMM_ERR_NOT_SUPPORTED;
+    p.full_units = (int)(total - rem);
+    if (prepare_kernel<Main>() != cudaSuccess ||
+        prepare_kernel_fn<LinearTag>(simt_gemm_kernel<Main, TILE_LINEAR>, Main::SMEM_BYTES) !=
+            cudaSuccess ||
+        prepare_kernel_fn<KsplitTag>(simt_gemm_kernel<Main, TILE_KSPLIT>, Main::SMEM_BYTES) !=
+            cudaSuccess) {
+        (void)cudaGetLastError();
+        return FGEMM_ERR_LAUNCH;
+    }
+    if (p.full_units > 0) {
+        if (batch == 1)
+            simt_gemm_kernel<Main><<<(unsigned)p.full_units, Main::THREADS, Main::SMEM_BYTES,
+                                     stream>>>(p);
+        else
+            simt_gemm_kernel<Main, TILE_LINEAR><<<(unsigned)p.full_units, Main::THREADS,
+                                                 Main::SMEM_BYTES, stream>>>(p);
+        if (cudaGetLastError() != cudaSuccess) return FGEMM_ERR_LAUNCH;
+    }
+    if (rem > 0) {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = KSPLIT;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(KSPLIT * rem), 1, 1);
+        cfg.blockDim = dim3(Main::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = Main::SMEM_BYTES;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, simt_gemm_kernel<Main, TILE_KSPLIT>, p) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return FGEMM_ERR_LAUNCH;
+        }
+    }
+    return FGEMM_OK;
+}
+
 #define FGEMM_LAUNCH_TABLE(NAME, TA, TB)                                   \
     const LaunchFn NAME[NUM_CONFIGS] = {                                   \
         &launch_simt<ConfigOf<CFG_128x128, TA, TB>::type>,                 \
@@ -177,7 +235,8 @@ static fgemm_status launch_simt_split(const GemmParams &p0, int batch, cudaStrea
         &launch_simt<ConfigOf<CFG_32x32_K4, TA, TB>::type>,                \
         &launch_simt_split<ConfigOf<CFG_128x128, TA, TB>::type,            \
                            SplitTailOf<TA, TB>::type>,                     \
+        &launch_simt_ksplit<ConfigOf<CFG_128x128, TA, TB>::type>,          \
     };                                                                     \
-    static_assert(NUM_CONFIGS == 7, "one launcher per configuration");
+    static_assert(NUM_CONFIGS == 8, "one launcher per configuration");
 
 }  // namespace fgemm

@@ -1,11 +1,14 @@
-"""The last-wave split launch (simt_128x128_t8x8_split) against the FP64 oracle.
+"""The last-wave split launches against the FP64 oracle.
 
-The split launch computes the first (tiles - r) 128 x 128 tiles whole and the
-last r = tiles mod SMs as 64 x 64 quarter tiles with four k-groups.  These cases
-put whole and quarter tiles in one launch, with the quarter tiles on the ragged
-bottom and right edges (quarters wholly outside the matrix are skipped), on the
-last problem of a strided batch, and in all four transpose layouts; integer data
-must come back bit-exact, uniform data within 1e-5 * mag.
+Both compute the first (tiles - r) 128 x 128 tiles whole and then the last
+r = tiles mod SMs another way: simt_128x128_t8x8_split as 64 x 64 quarter tiles
+with four k-groups, simt_128x128_t8x8_ksplit as clusters of four CTAs that each
+multiply one k-slice of a whole tile and add the partial sums through distributed
+shared memory.  These cases put whole and split tiles in one call, with split
+tiles on the ragged bottom and right edges (quarters wholly outside the matrix are
+skipped), on the last problem of a strided batch, with k-slices that are short or
+empty, and in all four transpose layouts; integer data must come back bit-exact,
+uniform data within 1e-5 * mag.
 """
 
 import itertools
@@ -21,8 +24,11 @@ pytestmark = pytest.mark.gpu
 COMBOS = list(itertools.product((0, 1), (0, 1)))
 
 
-def _split_config():
-    ids = [i for i in range(fg.num_configs()) if fg.config_name(i) == "simt_128x128_t8x8_split"]
+SPLITS = ["simt_128x128_t8x8_split", "simt_128x128_t8x8_ksplit"]
+
+
+def _config(name):
+    ids = [i for i in range(fg.num_configs()) if fg.config_name(i) == name]
     assert len(ids) == 1
     return ids[0]
 
@@ -42,43 +48,56 @@ def _tiles(M, N, batch=1):
     return -(-M // 128) * -(-N // 128) * batch
 
 
+@pytest.mark.parametrize("split", SPLITS)
 @pytest.mark.parametrize("ta,tb", COMBOS)
-def test_whole_and_quarter_tiles_integer_exact(ta, tb):
+def test_whole_and_split_tiles_integer_exact(split, ta, tb):
     # 1700 x 1650: 14 x 13 = 182 tiles; the last ones include the bottom-right
     # corner tile (rows 1664..1699, columns 1536..1649).
     M, N, K = 1700, 1650, 70
     assert _tiles(M, N) % _sms() != 0
-    check(Case(ta=ta, tb=tb, M=M, N=N, K=K, alpha=2.0, beta=-0.5, config=_split_config(),
+    check(Case(ta=ta, tb=tb, M=M, N=N, K=K, alpha=2.0, beta=-0.5, config=_config(split),
                pad=(4, 8, 4), seed=M + K + 2 * ta + tb))
 
 
+@pytest.mark.parametrize("split", SPLITS)
 @pytest.mark.parametrize("ta,tb", COMBOS)
-def test_whole_and_quarter_tiles_uniform(ta, tb):
+def test_whole_and_split_tiles_uniform(split, ta, tb):
     M, N, K = 1500, 1800, 333
     check(Case(ta=ta, tb=tb, M=M, N=N, K=K, alpha=1.5, beta=0.5, ints=False, bias=True,
-               relu=True, config=_split_config(), seed=21 + 2 * ta + tb))
+               relu=True, config=_config(split), seed=21 + 2 * ta + tb))
 
 
+@pytest.mark.parametrize("split", SPLITS)
 @pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1)])
-def test_quarter_tiles_on_the_last_problem_of_a_batch(ta, tb):
+def test_split_tiles_on_the_last_problem_of_a_batch(split, ta, tb):
     # 5 problems of 8 x 8 tiles = 320 tiles: with about 150 SMs the quarter tiles
     # all come from the last problem.
     check(Case(ta=ta, tb=tb, M=1000, N=990, K=37, alpha=1.0, beta=1.0, batch=5,
-               config=_split_config(), seed=33 + tb))
+               config=_config(split), seed=33 + tb))
 
 
-def test_all_tiles_quartered_when_fewer_tiles_than_sms():
+@pytest.mark.parametrize("split", SPLITS)
+def test_every_tile_split_when_fewer_tiles_than_sms(split):
     M, N = 700, 500
     assert _tiles(M, N) < _sms()
     for ta, tb in COMBOS:
         check(Case(ta=ta, tb=tb, M=M, N=N, K=150, alpha=-0.5, beta=2.0, bias=True,
-                   config=_split_config(), seed=40 + 2 * ta + tb))
+                   config=_config(split), seed=40 + 2 * ta + tb))
 
 
-def test_no_remainder_runs_whole_tiles_only():
+@pytest.mark.parametrize("K", [0, 1, 31, 32, 33, 97, 128, 129])
+def test_k_slices_short_and_empty(K):
+    # K slices are whole 32-deep stages: K <= 96 leaves the last slices empty.
+    for ta, tb in COMBOS:
+        check(Case(ta=ta, tb=tb, M=300, N=260, K=K, alpha=1.0, beta=0.5, bias=True, relu=True,
+                   config=_config("simt_128x128_t8x8_ksplit"), seed=60 + K + 2 * ta + tb))
+
+
+@pytest.mark.parametrize("split", SPLITS)
+def test_no_remainder_runs_whole_tiles_only(split):
     sms = _sms()
     M, N = 128 * sms, 256  # exactly 2 * SMs tiles
-    check(Case(M=M, N=N, K=24, alpha=1.0, beta=0.0, config=_split_config(), seed=50))
+    check(Case(M=M, N=N, K=24, alpha=1.0, beta=0.0, config=_config(split), seed=50))
 
 
 def test_selector_on_this_gpu():
@@ -89,7 +108,7 @@ def test_selector_on_this_gpu():
         pytest.skip("expectations measured on 152 SMs")
     name = lambda *a: fg.config_name(fg.select_config(*a, True, sms))
     assert name(0, 0, 4096, 4096, 4096, 1) == "simt_128x128_t8x8_split"
-    assert name(0, 0, 8192, 11008, 4096, 1) == "simt_128x128_t8x8_split"
-    assert name(0, 0, 2048, 128, 2048, 128) == "simt_128x128_t8x8_split"
+    assert name(0, 0, 8192, 11008, 4096, 1) == "simt_128x128_t8x8_ksplit"
+    assert name(0, 0, 2048, 128, 2048, 128) == "simt_128x128_t8x8_ksplit"
     assert name(0, 1, 2048, 2048, 128, 128) == "simt_128x128_t8x8"
     assert name(0, 0, 3072, 3072, 3072, 1) == "simt_128x128_t8x8"
