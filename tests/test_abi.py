@@ -122,7 +122,7 @@ def test_selector():
     assert name(0, 0, 1280, 1280, 4096, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # all split
     assert name(0, 0, 768, 768, 768, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # 36 tiles
     assert name(0, 0, 768, 768, 128, 1, 1, 152) == "simt_64x64x16_t4x4_s4"
-    assert name(0, 0, 640, 640, 640, 1, 1, 152) == "simt_32x32x16_t4x4_s4"
+    assert name(0, 0, 640, 640, 256, 1, 1, 152) == "simt_32x32x16_t4x4_s4"
     assert name(0, 0, 256, 256, 256, 1, 1, 152) == "simt_32x32x32_t4x4_s8_k4"
     # batches: QK^T (32768 tiles, r = 88, K = 128) whole; Score x V (2048 tiles, r = 72)
     assert name(0, 1, 2048, 2048, 128, 128, 1, 152) == "simt_128x128_t8x8"
