@@ -447,21 +447,36 @@ def run_fgemm(args, rank, world, local_rank):
                         "value": round(w.flops / per_call / 1e12, 4), "unit": UNIT,
                         "l2": "warm (calls back to back in one CUDA graph)"}
 
-    chosen = args.config
-    if chosen < 0:
-        aligned = True
-        chosen = fg.select_config(w.ta, w.tb, w.M, w.N, w.K, max(1, w.batch), aligned, sms)
-    kernel_name = fg.config_name(chosen)
-    n_batch_launches = (max(1, w.batch) + 65534) // 65535
-    if kernel_name.endswith(("_split", "_ksplit")):
-        # whole 128 x 128 tiles, then the last (tiles mod SMs) as quarter tiles or k-slices
-        total = -(-w.M // 128) * -(-w.N // 128) * max(1, w.batch)
-        n_batch_launches = int(total - total % sms > 0) + int(total % sms > 0)
-    if splitk is not None:  # partial GEMMs (one or two launches) + the reduction
-        Ks = -(-(-(-w.K // args.splitk)) // 32) * 32
-        n_batch_launches = (1 if w.K % Ks == 0 else 2) + 1
+    def launches(config, M, N, K, batch):
+        """Kernel launches of one library call with this configuration (None: select)."""
+        if config is None or config < 0:
+            config = fg.select_config(w.ta, w.tb, M, N, K, batch, True, sms)
+        name = fg.config_name(config)
+        if name.endswith(("_split", "_ksplit")):
+            # whole 128 x 128 tiles, then the last (tiles mod SMs) as quarter tiles or k-slices
+            total = -(-M // 128) * -(-N // 128) * batch
+            return name, int(total - total % sms > 0) + int(total % sms > 0)
+        return name, (batch + 65534) // 65535
+
+    kernel_name, n_batch_launches = launches(args.config, w.M, w.N, w.K, max(1, w.batch))
     if splitk is not None:
-        kernel_name = "%s_splitk%d" % (kernel_name, args.splitk)
+        # partial GEMMs: the slices of equal depth as one strided batch, the shorter last
+        # slice as a second call; then the reduction kernel
+        Ks = -(-(-(-w.K // args.splitk)) // 32) * 32
+        S = -(-w.K // Ks)
+        Klast = w.K - (S - 1) * Ks
+        full = S if Klast == Ks else S - 1
+        parts = []
+        n_batch_launches = 1
+        if full > 0:
+            name, n = launches(None, w.M, w.N, Ks, full)
+            parts.append(name)
+            n_batch_launches += n
+        if full < S:
+            name, n = launches(None, w.M, w.N, Klast, 1)
+            parts.append(name)
+            n_batch_launches += n
+        kernel_name = "splitk%d(%s)" % (args.splitk, "+".join(parts))
     # The tensor-core kernels take every layout of these (16-byte aligned) workloads;
     # TF32 runs 128 x 256 MMAs when one operand is stored K-major, 3xTF32 128 x 128.
     tensor_path = args.math != "fp32"
