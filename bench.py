@@ -499,7 +499,7 @@ def run_fgemm(args, rank, world, local_rank):
         "gpu_launches": args.steps * n_batch_launches,
         "roofline": {"bound": "alu", "achieved": round(achieved, 4), "peak": round(peak, 3),
                      "unit": UNIT, "frac": round(achieved / peak, 4),
-                     "traffic": recorded_traffic(fg.config_name(chosen), args.workload),
+                     "traffic": recorded_traffic(kernel_name, args.workload),
                      "peak_source": "derived: %d SMs x %d FP32 FMA/clk x 2 FLOP x %.0f MHz" % (
                          sms, FMA_PER_CLK_PER_SM, STATED_SM_MHZ)},
         "e2e": {"value": round(e2e_flops / e2e_max / 1e12, 4), "unit": UNIT,

@@ -1,0 +1,27 @@
+"""Static check of bench.py: every name it reads is bound somewhere in the file, imported,
+or a builtin.  The GPU arm of the benchmark cannot run without a GPU, so this catches a
+stale variable name there before a GPU run does."""
+
+import ast
+import builtins
+import os
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_bench_reads_only_bound_names():
+    tree = ast.parse(open(os.path.join(ROOT, "bench.py"), encoding="utf-8").read())
+    bound = set(dir(builtins)) | {"__file__", "__name__"}
+    for n in ast.walk(tree):
+        if isinstance(n, ast.Name) and isinstance(n.ctx, (ast.Store, ast.Del)):
+            bound.add(n.id)
+        elif isinstance(n, (ast.FunctionDef, ast.AsyncFunctionDef, ast.ClassDef)):
+            bound.add(n.name)
+        elif isinstance(n, (ast.Import, ast.ImportFrom)):
+            bound |= {a.asname or a.name.split(".")[0] for a in n.names}
+        elif isinstance(n, ast.arg):
+            bound.add(n.arg)
+        elif isinstance(n, ast.ExceptHandler) and n.name:
+            bound.add(n.name)
+    loads = {n.id for n in ast.walk(tree) if isinstance(n, ast.Name) and isinstance(n.ctx, ast.Load)}
+    assert not sorted(loads - bound)
