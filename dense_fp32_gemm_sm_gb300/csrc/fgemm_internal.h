@@ -16,7 +16,6 @@ using LaunchFn = fgemm_status (*)(const GemmParams &p, int batch, cudaStream_t s
 // Kernel configurations.  Ids are part of the test/bench interface.
 enum ConfigId {
     CFG_128x128 = 0,        // 128x128 CTA tile, 8x8 per thread, 2 CTAs/SM; BK=32 x 3 stages
-                            // (BK=16 x 5 stages when both operands are transposed on copy)
     CFG_128x64 = 1,         // 128x64x16, 8x8 per thread, 4 stages, 3 CTAs/SM (more CTAs for mid sizes)
     CFG_64x64 = 2,          // 64x64x16, 4x4 per thread, 4 stages (small problems)
     CFG_64x64_SCALAR = 3,   // 64x64x16 with element-wise copies: any alignment

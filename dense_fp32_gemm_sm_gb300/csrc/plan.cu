@@ -45,7 +45,7 @@ constexpr LaunchModel kModel[4][NUM_SLOTS] = {
         {10.91, -0.00391, 0.02504, 0.0290},  // quarter
     },
     {  // op(A) N, op(B) T
-        {9.31, 0.02485, 0.07644, 0.0000},  // 128x128
+        {8.77, 0.02036, 0.07595, 0.0000},  // 128x128 (refitted for its 32-deep stages)
         {9.88, 0.00193, 0.04351, 0.0465},  // 128x64
         {6.80, -0.00429, 0.03358, 0.0380},  // 64x64
         {7.15, -0.00007, 0.01026, 0.0185},  // 32x32
