@@ -215,14 +215,24 @@ const char *fgemm_status_string(fgemm_status status);
  * Kernel configurations (for tests and benchmarks).
  *
  * The plain entry points pick a kernel configuration from the shape, the
- * transposes, 16-byte alignment and the SM count.  The calls below expose that
+ * transposes, 16-byte alignment and the SM count: the one with the least launch
+ * time estimated by a model fitted to measurements (the number of CTAs the busiest
+ * SM runs, times a per-k cost, with a latency floor).  The calls below expose that
  * choice so every configuration can be tested on edge shapes, and timed.
+ *
+ * Two configurations issue two kernel launches on the caller's stream: whole
+ * 128 x 128 tiles first, then the last (tiles mod SMs) tiles either as 64 x 64
+ * quarter tiles ("..._split") or as thread-block clusters of four CTAs that each
+ * multiply one k-slice of a tile and add their partial sums through distributed
+ * shared memory in a fixed order ("..._ksplit").  Both allocate nothing and give
+ * the same result on every run.
  * ------------------------------------------------------------------------- */
 
 /* Number of kernel configurations; valid ids are 0 .. fgemm_num_configs()-1. */
 int fgemm_num_configs(void);
 
-/* Static name of a configuration ("simt_128x128x16_s4", ...), or NULL for a bad id. */
+/* Static name of a configuration ("simt_128x128_t8x8", "simt_128x128_t8x8_ksplit", ...),
+ * or NULL for a bad id. */
 const char *fgemm_config_name(int config);
 
 /*
