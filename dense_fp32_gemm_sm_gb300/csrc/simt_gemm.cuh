@@ -171,6 +171,16 @@ struct SimtCfg {
     static constexpr int RED_BYTES = (KS - 1) * GROUP_THREADS * TM * TN * 4;
     static constexpr int SMEM_BYTES = STAGE_BYTES > RED_BYTES ? STAGE_BYTES : RED_BYTES;
     static constexpr int GROUP_M = 8;
+    // k-step of each stage at which the copy of a later stage is issued.  NN tiles of
+    // 128 rows: halfway through the stage, away from the barrier where every warp also
+    // reloads its fragments (measured about 1 % faster at 4096^3, on the FC and PV
+    // workloads and at 2048^3).  Otherwise right after the barrier: NT measured 8 %
+    // faster so on QK^T, TN and TT spill registers with the later copy, and the small
+    // tiles lose latency hiding (256^3 on 32 x 32 tiles: 11 against 13 us).  At most
+    // KB - 2: the slot written is the one freed by the previous stage's barrier, and
+    // the slot index advances at KB - 1.
+    static constexpr int COPY_K = (TA == 0 && TB == 0 && BM >= 128) ? KB / 2 : 0;
+    static_assert(COPY_K <= KB - 2, "the copy is issued before the slot index advances");
 
     static_assert(BK % KS == 0 && KB % 2 == 0, "each k-group takes an even number of k per stage");
     static_assert(LR * LC == 32, "a warp is LR x LC lanes");
@@ -513,7 +523,7 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
                 } else {
                     load_frag(cur ^ 1, slot, kb0 + k + 1);
                 }
-                if (k == 0) {
+                if (k == Cfg::COPY_K) {
                     const int nk = kt + Cfg::STAGES - 1;
                     if (nk < KT) {
                         int ws = slot + Cfg::STAGES - 1;
