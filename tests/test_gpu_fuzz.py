@@ -47,3 +47,31 @@ def test_random_case(i):
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     check(Case(**draw(random.Random(1000 + i))))
+
+
+N_SPLIT_CASES = 24
+SPLITS = ("simt_128x128_t8x8_split", "simt_128x128_t8x8_ksplit")
+
+
+def draw_split(rng):
+    # grids larger than the SM count, so that whole tiles and a last wave of split
+    # tiles (quarters or k-slice clusters) meet in one call, on ragged edges
+    kw = dict(ta=rng.randint(0, 1), tb=rng.randint(0, 1), M=rng.randint(1500, 2600),
+              N=rng.randint(1500, 2600), K=rng.choice([1, 31, 64, 97, rng.randint(1, 200)]),
+              alpha=rng.choice([1.0, 2.0, -0.5]), beta=rng.choice([0.0, 1.0, -2.0]),
+              bias=rng.random() < 0.5, relu=rng.random() < 0.5,
+              batch=rng.choice([0, 0, 2]),
+              pad=(rng.choice([0, 4]), rng.choice([0, 8]), rng.choice([0, 4])),
+              seed=rng.randint(0, 1 << 30))
+    if kw["batch"]:
+        kw["bias"] = False
+    name = rng.choice(SPLITS)
+    kw["config"] = [i for i in range(fg.num_configs()) if fg.config_name(i) == name][0]
+    return kw
+
+
+@pytest.mark.parametrize("i", range(N_SPLIT_CASES))
+def test_random_split_case(i):
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    check(Case(**draw_split(random.Random(5000 + i))))
