@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <atomic>
+#include <cmath>
 
 #include "fgemm_internal.h"
 
@@ -70,15 +71,22 @@ constexpr LaunchModel kModel[4][NUM_SLOTS] = {
     },
 };
 
-double model_n_us(const LaunchModel &m, long long n, double K)
+double model_n_us(const LaunchModel &m, double n, double K)
 {
-    const double per_k = (double)n * m.b > m.L ? (double)n * m.b : m.L;
+    const double per_k = n * m.b > m.L ? n * m.b : m.L;
     return m.a + m.aK * K + K * per_k;
 }
 
-double model_us(const LaunchModel &m, long long ctas, long long K, int num_sms)
+// CTA counts are products of tile counts and the batch size, which can exceed 64
+// bits for arguments the entry points would never see; they are formed in double.
+double tiles_of(long long M, long long N, long long bm, long long bn, long long batch)
 {
-    return model_n_us(m, ceil_div(ctas, num_sms), (double)K);
+    return (double)ceil_div(M, bm) * (double)ceil_div(N, bn) * (double)batch;
+}
+
+double model_us(const LaunchModel &m, double ctas, long long K, int num_sms)
+{
+    return model_n_us(m, std::ceil(ctas / (double)num_sms), (double)K);
 }
 
 // Clusters of four k-slice CTAs that run at once with one CTA per SM.  Measured on
@@ -100,17 +108,20 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
     if (num_sms < 1) num_sms = 1;
     const long long b = batch > 0 ? batch : 1;
     const long long k = K > 0 ? K : 0;
-    const long long tiles128 = ceil_div(M, 128) * ceil_div(N, 128) * b;
+    const double tiles128 = tiles_of(M, N, 128, 128, b);
     // The last-wave split: whole 128 x 128 tiles for all but r = tiles mod SMs,
-    // then those r as 4r quarter tiles (a second launch; none when r = 0).
-    const long long r = tiles128 % num_sms, whole = tiles128 - r;
+    // then those r as 4r quarter tiles (a second launch; none when r = 0).  r by
+    // modular arithmetic, exact for any sizes.
+    const long long S = num_sms;
+    const long long r = ceil_div(M, 128) % S * (ceil_div(N, 128) % S) % S * (b % S) % S;
+    const double whole = tiles128 - (double)r;
     const LaunchModel *const mm = kModel[(ta ? 2 : 0) + (tb ? 1 : 0)];
     const double main_us = whole > 0 ? model_us(mm[M_128x128], whole, k, num_sms) : 0.0;
     // quarter tiles: 4r CTAs of the quarter model
-    const double split = main_us + (r > 0 ? model_us(mm[M_QUARTER], 4 * r, k, num_sms) : 0.0);
+    const double split = main_us + (r > 0 ? model_us(mm[M_QUARTER], 4.0 * (double)r, k, num_sms) : 0.0);
     // k-split tiles: whole-tile CTAs over K / 4 each, in rounds of clusters (measured
     // within 2-7 % of the whole-tile model at K / 4 on 152 SMs)
-    const long long rounds = ceil_div(r, ksplit_clusters_per_round(num_sms));
+    const double rounds = (double)ceil_div(r, ksplit_clusters_per_round(num_sms));
     const double ksplit = main_us + (r > 0 ? model_n_us(mm[M_128x128], rounds, (double)k / 4.0) : 0.0);
     struct Option {
         int config;
@@ -120,10 +131,10 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
         {CFG_128x128, model_us(mm[M_128x128], tiles128, k, num_sms)},
         {CFG_128x128_SPLIT, r > 0 ? split : 1e300},
         {CFG_128x128_KSPLIT, r > 0 ? ksplit : 1e300},
-        {CFG_128x64, model_us(mm[M_128x64], ceil_div(M, 128) * ceil_div(N, 64) * b, k, num_sms)},
-        {CFG_64x64, model_us(mm[M_64x64], ceil_div(M, 64) * ceil_div(N, 64) * b, k, num_sms)},
-        {CFG_32x32, model_us(mm[M_32x32], ceil_div(M, 32) * ceil_div(N, 32) * b, k, num_sms)},
-        {CFG_32x32_K4, model_us(mm[M_32x32_K4], ceil_div(M, 32) * ceil_div(N, 32) * b, k, num_sms)},
+        {CFG_128x64, model_us(mm[M_128x64], tiles_of(M, N, 128, 64, b), k, num_sms)},
+        {CFG_64x64, model_us(mm[M_64x64], tiles_of(M, N, 64, 64, b), k, num_sms)},
+        {CFG_32x32, model_us(mm[M_32x32], tiles_of(M, N, 32, 32, b), k, num_sms)},
+        {CFG_32x32_K4, model_us(mm[M_32x32_K4], tiles_of(M, N, 32, 32, b), k, num_sms)},
     };
     Option best = options[0];
     for (const Option &o : options)

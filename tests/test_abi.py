@@ -181,3 +181,17 @@ def test_row_bias_entry_validates_before_launch(kw):
     assert fg.sgemm_row_bias_relu(**dict(args, M=0), check=False) == fg.OK
     args.update(kw)
     assert fg.sgemm_row_bias_relu(**args, check=False) == fg.ERR_INVALID_VALUE
+
+
+def test_selector_extreme_arguments():
+    # Sizes no allocation could hold still get a valid configuration (host-only call),
+    # and a grid that divides evenly over the SMs never takes a last-wave split.
+    sel = fg.select_config
+    big = 2**31 - 1
+    for args in ((big, big, big, big), (big, 1, 1, big), (1, 1, big, 1), (big, big, 0, 1)):
+        for sms in (1, 152, 1000):
+            c = sel(0, 0, *args, 1, sms)
+            assert 0 <= c < fg.num_configs()
+    for M, N, b in ((128 * 152, 128, 1), (128 * 19, 128 * 8, 1), (128, 128, 152 * 3)):
+        assert (-(-M // 128) * -(-N // 128) * b) % 152 == 0
+        assert not fg.config_name(sel(0, 0, M, N, 4096, b, 1, 152)).endswith("split")
