@@ -43,6 +43,13 @@
 //    tiles while the other SMs idle.  A split launch runs the first tiles whole and
 //    then cuts each of the last r into four quarter tiles with four k-groups each,
 //    so the remainder's work spreads over the SMs in quarter-tile steps.
+//
+//  * Last-wave k-split (TILE_KSPLIT launches): the last r tiles stay whole, each
+//    computed by a thread-block cluster of four CTAs that multiply one k-slice each;
+//    the partial tiles are added in slice order through distributed shared memory
+//    (no workspace, no atomics, the same result on every run).
+//
+//  * The copy of a later stage is issued at k-step COPY_K of the current stage.
 #pragma once
 
 #include <cuda_runtime.h>
