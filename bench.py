@@ -66,7 +66,9 @@ def parse_args(argv=None):
     ap.add_argument("--workload", choices=workloads.WORKLOADS, default="square4096")
     ap.add_argument("--config", type=int, default=-1,
                     help="explicit kernel configuration id (default: the library's choice)")
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=50,
+                    help="pipelined end-to-end steps timed (the first inputs and the last "
+                         "result are not overlapped; more steps amortise them)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
