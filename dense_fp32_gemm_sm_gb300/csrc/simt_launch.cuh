@@ -117,6 +117,50 @@ static fgemm_status launch_simt(const GemmParams &p0, int batch, cudaStream_t st
     return FGEMM_OK;
 }
 
+// Plan of a last-wave split over Main-sized tiles: tile counts, the whole tiles of
+// all problems (p.full_units) and the remainder r = tiles mod SMs, whose tiles then
+// run as tail_ctas CTAs each.
+template <class Main>
+static fgemm_status plan_split(GemmParams &p, int batch, int tail_ctas, long long *rem)
+{
+    p.tiles_m = (p.M + Main::BM - 1) / Main::BM;
+    p.tiles_n = (p.N + Main::BN - 1) / Main::BN;
+    const long long total = (long long)p.tiles_m * p.tiles_n * batch;
+    int sms = 0;
+    if (device_sm_count(&sms) != 0 || sms < 1) {
+        (void)cudaGetLastError();
+        return FGEMM_ERR_LAUNCH;
+    }
+    *rem = total % sms;
+    if (total - *rem > INT_MAX || (long long)tail_ctas * *rem > INT_MAX)
+        return FGEMM_ERR_NOT_SUPPORTED;
+    p.full_units = (int)(total - *rem);
+    return FGEMM_OK;
+}
+
+// The first launch of a split: the whole tiles.  One problem: the per-problem kernel
+// over the first full_units tiles.  A batch: the linear-order kernel, whose whole
+// tiles may end inside a problem.
+template <class Main>
+static fgemm_status launch_whole_tiles(const GemmParams &p, int batch, cudaStream_t stream)
+{
+    struct LinearTag {};
+    if (prepare_kernel<Main>() != cudaSuccess ||
+        prepare_kernel_fn<LinearTag>(simt_gemm_kernel<Main, TILE_LINEAR>, Main::SMEM_BYTES) !=
+            cudaSuccess) {
+        (void)cudaGetLastError();
+        return FGEMM_ERR_LAUNCH;
+    }
+    if (p.full_units <= 0) return FGEMM_OK;
+    if (batch == 1)
+        simt_gemm_kernel<Main><<<(unsigned)p.full_units, Main::THREADS, Main::SMEM_BYTES,
+                                 stream>>>(p);
+    else
+        simt_gemm_kernel<Main, TILE_LINEAR><<<(unsigned)p.full_units, Main::THREADS,
+                                             Main::SMEM_BYTES, stream>>>(p);
+    return cudaGetLastError() == cudaSuccess ? FGEMM_OK : FGEMM_ERR_LAUNCH;
+}
+
 // Last-wave split: the first (tiles - r) tiles of all problems whole, then the
 // last r = tiles mod SMs as quarter tiles (TILE_QUARTER), two launches on
 // the stream.
@@ -126,37 +170,16 @@ static fgemm_status launch_simt_split(const GemmParams &p0, int batch, cudaStrea
     struct TailTag {};
     static_assert(Tail::THREADS == Main::THREADS, "tail CTAs fill the slots of main CTAs");
     GemmParams p = p0;
-    p.tiles_m = (p.M + Main::BM - 1) / Main::BM;
-    p.tiles_n = (p.N + Main::BN - 1) / Main::BN;
-    const long long total = (long long)p.tiles_m * p.tiles_n * batch;
-    int sms = 0;
-    if (device_sm_count(&sms) != 0 || sms < 1) {
+    long long rem = 0;
+    fgemm_status st = plan_split<Main>(p, batch, 4, &rem);
+    if (st != FGEMM_OK) return st;
+    if (prepare_kernel_fn<TailTag>(simt_gemm_kernel<Tail, TILE_QUARTER, Main>, Tail::SMEM_BYTES) !=
+        cudaSuccess) {
         (void)cudaGetLastError();
         return FGEMM_ERR_LAUNCH;
     }
-    const long long rem = total % sms;
-    if (total - rem > INT_MAX || 4 * rem > INT_MAX) return FGEMM_ERR_NOT_SUPPORTED;
-    p.full_units = (int)(total - rem);
-    struct LinearTag {};
-    if (prepare_kernel<Main>() != cudaSuccess ||
-        prepare_kernel_fn<LinearTag>(simt_gemm_kernel<Main, TILE_LINEAR>, Main::SMEM_BYTES) !=
-            cudaSuccess ||
-        prepare_kernel_fn<TailTag>(simt_gemm_kernel<Tail, TILE_QUARTER, Main>, Tail::SMEM_BYTES) !=
-            cudaSuccess) {
-        (void)cudaGetLastError();
-        return FGEMM_ERR_LAUNCH;
-    }
-    if (p.full_units > 0) {
-        // One problem: the per-problem kernel over the first full_units tiles.
-        // A batch: the linear-order kernel, whose whole tiles may end inside a problem.
-        if (batch == 1)
-            simt_gemm_kernel<Main><<<(unsigned)p.full_units, Main::THREADS, Main::SMEM_BYTES,
-                                     stream>>>(p);
-        else
-            simt_gemm_kernel<Main, TILE_LINEAR><<<(unsigned)p.full_units, Main::THREADS,
-                                                 Main::SMEM_BYTES, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return FGEMM_ERR_LAUNCH;
-    }
+    st = launch_whole_tiles<Main>(p, batch, stream);
+    if (st != FGEMM_OK) return st;
     if (rem > 0) {
         simt_gemm_kernel<Tail, TILE_QUARTER, Main><<<(unsigned)(4 * rem), Tail::THREADS,
                                                      Tail::SMEM_BYTES, stream>>>(p);
@@ -171,37 +194,18 @@ static fgemm_status launch_simt_split(const GemmParams &p0, int batch, cudaStrea
 template <class Main>
 static fgemm_status launch_simt_ksplit(const GemmParams &p0, int batch, cudaStream_t stream)
 {
-    struct LinearTag {};
     struct KsplitTag {};
     GemmParams p = p0;
-    p.tiles_m = (p.M + Main::BM - 1) / Main::BM;
-    p.tiles_n = (p.N + Main::BN - 1) / Main::BN;
-    const long long total = (long long)p.tiles_m * p.tiles_n * batch;
-    int sms = 0;
-    if (device_sm_count(&sms) != 0 || sms < 1) {
+    long long rem = 0;
+    fgemm_status st = plan_split<Main>(p, batch, KSPLIT, &rem);
+    if (st != FGEMM_OK) return st;
+    if (prepare_kernel_fn<KsplitTag>(simt_gemm_kernel<Main, TILE_KSPLIT>, Main::SMEM_BYTES) !=
+        cudaSuccess) {
         (void)cudaGetLastError();
         return FGEMM_ERR_LAUNCH;
     }
-    const long long rem = total % sms;
-    if (total - rem > INT_MAX || KSPLIT * rem > INT_MAX) return FGEMM_ERR_NOT_SUPPORTED;
-    p.full_units = (int)(total - rem);
-    if (prepare_kernel<Main>() != cudaSuccess ||
-        prepare_kernel_fn<LinearTag>(simt_gemm_kernel<Main, TILE_LINEAR>, Main::SMEM_BYTES) !=
-            cudaSuccess ||
-        prepare_kernel_fn<KsplitTag>(simt_gemm_kernel<Main, TILE_KSPLIT>, Main::SMEM_BYTES) !=
-            cudaSuccess) {
-        (void)cudaGetLastError();
-        return FGEMM_ERR_LAUNCH;
-    }
-    if (p.full_units > 0) {
-        if (batch == 1)
-            simt_gemm_kernel<Main><<<(unsigned)p.full_units, Main::THREADS, Main::SMEM_BYTES,
-                                     stream>>>(p);
-        else
-            simt_gemm_kernel<Main, TILE_LINEAR><<<(unsigned)p.full_units, Main::THREADS,
-                                                 Main::SMEM_BYTES, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return FGEMM_ERR_LAUNCH;
-    }
+    st = launch_whole_tiles<Main>(p, batch, stream);
+    if (st != FGEMM_OK) return st;
     if (rem > 0) {
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
