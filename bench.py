@@ -79,10 +79,10 @@ def parse_args(argv=None):
                     help="S > 1: split-K GEMM into S slices with a workspace (single problems)")
     ap.add_argument("--epilogue", choices=("workload", "none"), default="workload",
                     help="'none' drops the workload's bias/ReLU (plain sgemm at the same shape)")
-    ap.add_argument("--graph-calls", type=int, default=0,
+    ap.add_argument("--graph-calls", type=int, default=None,
                     help="N > 0: also time N back-to-back library calls captured in one CUDA "
                          "graph (warm L2, no host launch cost): the per-call latency of small "
-                         "shapes")
+                         "shapes (default: 200 for square256, 0 otherwise)")
     ap.add_argument("--cpu-baseline-table", action="store_true",
                     help="no GPU: time the FP64 oracle on every workload on one host core and on "
                          "all of them (bounded samples), one JSON line each")
@@ -426,6 +426,8 @@ def run_fgemm(args, rank, world, local_rank):
     e2e_flops, e2e_max = aggregate(w.flops, e2e_s, world, dev if world > 1 else None)
 
     back_to_back = None
+    if args.graph_calls is None:
+        args.graph_calls = 200 if args.workload == "square256" else 0
     if args.graph_calls > 0:
         # N calls back to back in one CUDA graph: no host launch cost and no L2 flush in
         # between, so this is the device time per call of a user's captured sequence.
@@ -516,6 +518,16 @@ def run_fgemm(args, rank, world, local_rank):
                                        "last wave's tiles as %s), timed together as one call" % (
                                            "k-slice clusters" if kernel_name.endswith("_ksplit")
                                            else "quarter tiles"))
+    # Algorithmic HBM bytes per step (A and B read, C written, C read when beta != 0,
+    # the bias) over the step time: the bandwidth side of the roofline, which matters
+    # for the skinny shapes (the QK^T batch writes 2 GiB).
+    alg_bytes = 4 * (w.M * w.K + w.K * w.N + w.M * w.N) * max(1, w.batch)
+    if w.beta != 0:
+        alg_bytes += 4 * w.M * w.N * max(1, w.batch)
+    if w.bias is not None:
+        alg_bytes += 4 * w.N
+    line["bandwidth"] = {"algorithmic_bytes_per_step": alg_bytes,
+                         "gb_s": round(alg_bytes / (kernel_ms / 1e3) / 1e9, 1)}
     if back_to_back is not None:
         line["back_to_back"] = back_to_back
     if tensor_path:
