@@ -456,11 +456,7 @@ def run_fgemm(args, rank, world, local_rank):
         if config is None or config < 0:
             config = fg.select_config(w.ta, w.tb, M, N, K, batch, True, sms)
         name = fg.config_name(config)
-        if name.endswith(("_split", "_ksplit")):
-            # whole 128 x 128 tiles, then the last (tiles mod SMs) as quarter tiles or k-slices
-            total = -(-M // 128) * -(-N // 128) * batch
-            return name, int(total - total % sms > 0) + int(total % sms > 0)
-        return name, (batch + 65534) // 65535
+        return name, call_launches(name, M, N, batch, sms)
 
     kernel_name, n_batch_launches = launches(args.config, w.M, w.N, w.K, max(1, w.batch))
     if splitk is not None:
@@ -546,6 +542,16 @@ def run_fgemm(args, rank, world, local_rank):
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     return line
+
+
+def call_launches(config_name, M, N, batch, sms):
+    """Kernel launches of one CUDA-core library call: the last-wave splits launch their
+    whole 128 x 128 tiles, then the last (tiles mod SMs) tiles, each part only when it
+    is not empty; the other configurations launch once per 65535 problems."""
+    if config_name.endswith(("_split", "_ksplit")):
+        total = -(-M // 128) * -(-N // 128) * batch
+        return int(total - total % sms > 0) + int(total % sms > 0)
+    return (batch + 65534) // 65535
 
 
 def describe(w):

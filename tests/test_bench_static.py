@@ -25,3 +25,18 @@ def test_bench_reads_only_bound_names():
             bound.add(n.name)
     loads = {n.id for n in ast.walk(tree) if isinstance(n, ast.Name) and isinstance(n.ctx, ast.Load)}
     assert not sorted(loads - bound)
+
+
+def test_call_launches():
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    # whole tiles only, two launches, or only the split tiles
+    assert bench.call_launches("simt_128x128_t8x8", 4096, 4096, 1, 152) == 1
+    assert bench.call_launches("simt_128x128_t8x8_split", 4096, 4096, 1, 152) == 2  # 912 + 112
+    assert bench.call_launches("simt_128x128_t8x8_ksplit", 4096, 4864, 1, 152) == 1  # 8 x 152
+    assert bench.call_launches("simt_128x128_t8x8_ksplit", 1024, 1024, 1, 152) == 1  # 64 < 152
+    assert bench.call_launches("simt_128x128_t8x8_ksplit", 2048, 128, 128, 152) == 2
+    # the per-problem grid splits a batch into chunks of 65535 problems
+    assert bench.call_launches("simt_32x32x16_t4x4_s4", 64, 64, 65535, 152) == 1
+    assert bench.call_launches("simt_32x32x16_t4x4_s4", 64, 64, 65536, 152) == 2
