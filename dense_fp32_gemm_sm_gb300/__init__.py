@@ -23,6 +23,7 @@ from ._binding import (  # noqa: F401
     gemm_math,
     gemm_explicit,
     library,
+    math_supported,
     num_configs,
     select_config,
     sgemm,

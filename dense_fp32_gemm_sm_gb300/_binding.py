@@ -80,6 +80,10 @@ def library() -> ctypes.CDLL:
             lib.fgemm_sgemm_splitk_noalloc.restype = _c_int
             lib.fgemm_splitk_workspace_size.argtypes = [_c_int, _c_int, _c_int, _c_int]
             lib.fgemm_splitk_workspace_size.restype = ctypes.c_size_t
+            lib.fgemm_math_supported.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
+                                                 _c_float, _c_vp, _c_int, _c_ll, _c_vp, _c_int,
+                                                 _c_ll, _c_int]
+            lib.fgemm_math_supported.restype = _c_int
             lib.fgemm_debug_withhold_tensor_core.argtypes = [_c_int, _c_ll]
             lib.fgemm_debug_withhold_tensor_core.restype = None
             lib.fgemm_config_name.restype = ctypes.c_char_p
@@ -201,6 +205,15 @@ def gemm_math(math, transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, str
     if check:
         _check(st, "fgemm_gemm_math")
     return st
+
+
+def math_supported(math, transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, strideB,
+                   batch) -> int:
+    """``fgemm_math_supported``: 1 if ``gemm_math`` runs the requested arithmetic for these
+    operands, 0 if it would use the FP32 CUDA-core kernel instead, -1 for a bad ``math``.
+    Host-only; the pointers are only tested for alignment."""
+    return library().fgemm_math_supported(int(math), int(transa), int(transb), M, N, K, alpha,
+                                          _ptr(A), lda, strideA, _ptr(B), ldb, strideB, batch)
 
 
 def device_status(clear=True) -> int:

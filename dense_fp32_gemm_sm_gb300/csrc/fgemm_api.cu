@@ -247,13 +247,8 @@ fgemm_status run_splitk(const Problem &p, int splits, float *W, size_t ws_bytes)
                                 p.stream);
 }
 
-fgemm_status run_math(fgemm_math math, const Problem &p)
+TcProblem tc_problem(const Problem &p)
 {
-    if (math == FGEMM_MATH_FP32) return run(-1, p);
-    if (math != FGEMM_MATH_TF32 && math != FGEMM_MATH_3XTF32) return FGEMM_ERR_INVALID_VALUE;
-    bool noop = false;
-    const fgemm_status st = validate(p, &noop);
-    if (st != FGEMM_OK || noop) return st;
     TcProblem q;
     q.ta = p.ta;
     q.tb = p.tb;
@@ -274,9 +269,43 @@ fgemm_status run_math(fgemm_math math, const Problem &p)
     q.batch = p.batch;
     q.bias = p.bias;
     q.relu = p.relu;
+    return q;
+}
+
+fgemm_status run_math(fgemm_math math, const Problem &p)
+{
+    if (math == FGEMM_MATH_FP32) return run(-1, p);
+    if (math != FGEMM_MATH_TF32 && math != FGEMM_MATH_3XTF32) return FGEMM_ERR_INVALID_VALUE;
+    bool noop = false;
+    const fgemm_status st = validate(p, &noop);
+    if (st != FGEMM_OK || noop) return st;
+    const TcProblem q = tc_problem(p);
     if (!tc_supported(q)) return run(-1, p);
     return launch_tc(math == FGEMM_MATH_3XTF32 ? 3 : 1, q, p.stream);
 }
+
+}  // namespace
+
+fgemm_status splitk_plan(int ta, int tb, int M, int N, int K, float alpha, const float *A, int lda,
+                         const float *B, int ldb, float beta, float *C, int ldc, int splits,
+                         size_t *workspace_bytes)
+{
+    *workspace_bytes = 0;
+    const Problem p = make_problem((fgemm_op)ta, (fgemm_op)tb, M, N, K, alpha, A, lda, 0, B, ldb,
+                                   0, beta, C, ldc, 0, 1, nullptr, 0, nullptr);
+    bool noop = false;
+    const fgemm_status st = validate(p, &noop);
+    if (st != FGEMM_OK || noop) return st;
+    if (splits < 1 || splits > 64) return FGEMM_ERR_INVALID_VALUE;
+    const bool products = p.K > 0 && p.alpha != 0.0f;
+    if (splits == 1 || !products) return FGEMM_OK;
+    const long long Ks = splitk_slice(p.K, splits);
+    const long long S = (p.K + Ks - 1) / Ks;
+    *workspace_bytes = (size_t)S * (size_t)p.M * (size_t)p.N * sizeof(float);
+    return FGEMM_OK;
+}
+
+namespace {
 
 }  // namespace
 }  // namespace fgemm
@@ -344,6 +373,17 @@ fgemm_status fgemm_gemm_math(fgemm_math math, fgemm_op transa, fgemm_op transb, 
 }
 
 fgemm_status fgemm_device_status(int clear) { return fgemm::tc_device_status(clear); }
+
+int fgemm_math_supported(fgemm_math math, fgemm_op transa, fgemm_op transb, int M, int N, int K,
+                         float alpha, const float *A, int lda, long long strideA, const float *B,
+                         int ldb, long long strideB, int batch)
+{
+    if (math == FGEMM_MATH_FP32) return 1;
+    if (math != FGEMM_MATH_TF32 && math != FGEMM_MATH_3XTF32) return -1;
+    const fgemm::Problem p = make_problem(transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb,
+                                          strideB, 0.0f, nullptr, 1, 0, batch, nullptr, 0, nullptr);
+    return fgemm::tc_supported(fgemm::tc_problem(p)) ? 1 : 0;
+}
 
 size_t fgemm_splitk_workspace_size(int M, int N, int K, int splits)
 {

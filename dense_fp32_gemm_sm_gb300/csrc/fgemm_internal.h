@@ -69,6 +69,13 @@ fgemm_status tc_device_status(int clear);
 // Testing: withhold one k-block in later tensor-core launches (k_block < 0: normal).
 void tc_debug_withhold(int k_block, long long wait_limit_ns);
 
+// Validates a split-K call (the rules of fgemm_sgemm_splitk without its workspace)
+// and gives the workspace bytes it will use: 0 when it runs without one (splits == 1,
+// no products, or nothing to do).
+fgemm_status splitk_plan(int ta, int tb, int M, int N, int K, float alpha, const float *A, int lda,
+                         const float *B, int ldb, float beta, float *C, int ldc, int splits,
+                         size_t *workspace_bytes);
+
 // C = act(alpha * sum_s W[s] + beta * C + bias), W: S slices of M x N (ld N).
 fgemm_status launch_splitk_reduce(const float *W, int S, float *C, long long ldc, int M, int N,
                                   float alpha, float beta, const float *bias, int relu,

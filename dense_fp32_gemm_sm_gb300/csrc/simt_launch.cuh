@@ -4,6 +4,7 @@
 #include <atomic>
 #include <climits>
 
+#include "ctx_id.h"
 #include "fgemm_internal.h"
 #include "simt_gemm.cuh"
 
@@ -64,22 +65,25 @@ struct SplitTailOf {
     using type = SimtCfg<64, 64, BOTH_T ? 32 : 64, 64, 32, 8, 8, BOTH_T ? 4 : 3, 2, TA, TB, true, 4>;
 };
 
-// Opt a kernel in to its dynamic shared memory once per device.  Tag makes the
-// once-per-device flag distinct per kernel.
+// Opt a kernel in to its dynamic shared memory once per context (attributes belong to
+// the context's copy of the kernel; a device reset drops them).  Tag makes the
+// per-context record distinct per kernel.
 template <class Tag, class KernelFn>
 static cudaError_t prepare_kernel_fn(KernelFn kernel, int smem_bytes)
 {
-    static std::atomic<unsigned long long> ready{0};
+    static std::atomic<unsigned long long> ready_ctx[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (ready.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    std::atomic<unsigned long long> &ready = ready_ctx[dev & 63];
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0 && ready.load(std::memory_order_acquire) == ctx) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
-    ready.fetch_or(bit, std::memory_order_acq_rel);
+    // the calls above made the device's primary context current if none was
+    ready.store(current_context_id(), std::memory_order_release);
     return cudaSuccess;
 }
 

@@ -8,7 +8,9 @@
 #include <climits>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
+#include "ctx_id.h"
 #include "fgemm_internal.h"
 #include "tc_gemm.cuh"
 
@@ -84,36 +86,49 @@ bool make_output_map(CUtensorMap *map, float *base, long long M, long long N, lo
 
 int current_device(int *dev) { return cudaGetDevice(dev) == cudaSuccess ? 0 : -1; }
 
-// Device address of g_tc_error on the current device (looked up once per device).
+// Device address of g_tc_error in the current context, looked up once per context
+// (a device reset loads the module again, and the variable may move).
 unsigned *error_word()
 {
-    static std::atomic<unsigned *> cache[64];
+    struct Entry {
+        unsigned long long ctx;
+        unsigned *addr;
+    };
+    static Entry cache[64];
+    static std::mutex mu;
     int dev = 0;
     if (current_device(&dev) != 0) return nullptr;
-    unsigned *p = cache[dev & 63].load(std::memory_order_acquire);
-    if (!p) {
-        void *addr = nullptr;
-        if (cudaGetSymbolAddress(&addr, g_tc_error) != cudaSuccess) return nullptr;
-        p = static_cast<unsigned *>(addr);
-        cache[dev & 63].store(p, std::memory_order_release);
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0) {
+        std::lock_guard<std::mutex> lock(mu);
+        if (cache[dev & 63].ctx == ctx) return cache[dev & 63].addr;
     }
-    return p;
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_tc_error) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    cache[dev & 63] = Entry{current_context_id(), static_cast<unsigned *>(addr)};
+    return static_cast<unsigned *>(addr);
 }
 
+// The kernel's dynamic shared memory attribute, set once per context.
 template <int MODE, int TA, int TB>
 cudaError_t prepare_tc()
 {
-    static std::atomic<unsigned long long> ready{0};
+    static std::atomic<unsigned long long> ready_ctx[64];
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    const unsigned long long bit = 1ull << (dev & 63);
-    if (ready.load(std::memory_order_acquire) & bit) return cudaSuccess;
+    std::atomic<unsigned long long> &ready = ready_ctx[dev & 63];
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0 && ready.load(std::memory_order_acquire) == ctx) return cudaSuccess;
     e = cudaFuncSetAttribute(tc::tc_gemm_kernel<MODE, TA, TB>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              tc::TcShape<MODE, TA, TB>::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    ready.fetch_or(bit, std::memory_order_acq_rel);
+    ready.store(current_context_id(), std::memory_order_release);
     return cudaSuccess;
 }
 

@@ -33,7 +33,13 @@
  *   - Arithmetic is IEEE FP32 fused multiply-add on the CUDA cores, summing k
  *     in an order that differs from the plain loop; results agree with an FP64
  *     evaluation to within 1e-5 * (|alpha| sum_k |a_ik||b_kj| + |beta||c_ij| + |bias_j|).
- *   - Thread safety: calls from several host threads are safe.
+ *   - Thread safety: calls from several host threads are safe, with two
+ *     exceptions: fgemm_sgemm_splitk_noalloc calls whose kernels overlap on the GPU
+ *     share one scratch array and must be ordered (see there), and the test hook
+ *     fgemm_debug_withhold_tensor_core must not run beside tensor-core calls.
+ *   - Per-context state: the library caches a few per-context facts (the device
+ *     address of its own __device__ variables, kernel attributes) keyed on the
+ *     context's id, so they are looked up again after cudaDeviceReset.
  */
 #ifndef FGEMM_H
 #define FGEMM_H
@@ -138,12 +144,16 @@ fgemm_status fgemm_sgemm_splitk(fgemm_op transa, fgemm_op transb, int M, int N, 
  * Same arguments and result as fgemm_sgemm_splitk, without the workspace: the
  * partial products go to one fixed array of FGEMM_NOALLOC_SCRATCH_BYTES in the
  * global memory of every GPU that loads the library, held until the process exits.
- *   - A problem needing more than that (fgemm_splitk_workspace_size(M, N, K, splits)
- *     > FGEMM_NOALLOC_SCRATCH_BYTES) is rejected with FGEMM_ERR_NOT_SUPPORTED before
- *     anything else happens; 16 MiB holds, e.g., 4 slices of a 1024 x 1024 C.
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call before
- *     any stream capture.
+ *   - Order of checks: first the argument rules of fgemm_sgemm_splitk
+ *     (FGEMM_ERR_INVALID_VALUE); then, for a call that uses partial products
+ *     (splits > 1, K > 0, alpha != 0), their size: more than the array holds
+ *     (fgemm_splitk_workspace_size(M, N, K, splits) > FGEMM_NOALLOC_SCRATCH_BYTES)
+ *     returns FGEMM_ERR_NOT_SUPPORTED before anything is launched.  16 MiB holds,
+ *     e.g., 4 slices of a 1024 x 1024 C.  A call that needs no partial products
+ *     runs at any size, exactly as fgemm_sgemm_splitk runs it.
+ *   - The first call in each CUDA context (per device, and again after
+ *     cudaDeviceReset) looks up the array's device address (cudaGetSymbolAddress,
+ *     with that device current); make that first call before any stream capture.
  *   - Every call uses the same array and leaves its contents behind; nothing in it has
  *     to start at zero (each partial product is written before it is read).  Calls
  *     whose kernels overlap on the GPU -- on different streams, or from different
@@ -179,7 +189,8 @@ typedef enum fgemm_math {
  * zero strides is a single GEMM).  The tensor-core modes take every transpose
  * combination; they need 16-byte aligned A and B and lda, ldb, strideA, strideB
  * multiples of 4.  A call they cannot run (unaligned operands, K == 0, alpha == 0)
- * uses the FP32 CUDA-core kernel instead (at least as accurate).  A tensor-core kernel bounds
+ * uses the FP32 CUDA-core kernel instead (at least as accurate);
+ * fgemm_math_supported tells beforehand which one a call will use.  A tensor-core kernel bounds
  * every internal wait; if one runs out it stops, leaves C undefined and records it
  * for fgemm_device_status.
  */
@@ -196,6 +207,21 @@ fgemm_status fgemm_gemm_math(fgemm_math math, fgemm_op transa, fgemm_op transb, 
  * finished.  Nonzero `clear` resets the record.
  */
 fgemm_status fgemm_device_status(int clear);
+
+/*
+ * Which arithmetic fgemm_gemm_math will use for a call with these operands: 1 when
+ * it runs the requested one (always for FGEMM_MATH_FP32; for the tensor-core modes
+ * when the layout, alignment and sizes suit the tcgen05 kernel), 0 when it would run
+ * the FP32 CUDA-core kernel instead (unaligned operands, K == 0, alpha == 0, an empty
+ * problem, or no driver), -1 when `math` is not an fgemm_math value.  The arguments
+ * mean what they mean for fgemm_gemm_math; the pointers are only tested for 16-byte
+ * alignment, never dereferenced, and nothing else is validated.  Host-only: no
+ * kernel runs and no device memory is touched (the first call looks up the driver's
+ * tensor-map encoder).
+ */
+int fgemm_math_supported(fgemm_math math, fgemm_op transa, fgemm_op transb, int M, int N, int K,
+                         float alpha, const float *A, int lda, long long strideA, const float *B,
+                         int ldb, long long strideB, int batch);
 
 /*
  * Testing only (failure detection without a GPU fault).  Makes later tensor-core

@@ -50,6 +50,10 @@ class Case:
     c_nan: bool = False  # fill the initial C with NaN (only meaningful for beta == 0)
     a_nan: bool = False  # fill A with NaN (only meaningful for alpha == 0)
     row_bias: bool = False  # call fgemm_sgemm_row_bias_relu with a per-row bias (single GEMM)
+    # With a tensor-core math: whether the call must run on the tensor cores (True) or
+    # fall back to the CUDA-core kernel (False), as fgemm_math_supported reports; None
+    # leaves it open (random cases whose alignment may go either way).
+    expect_tc: object = True
 
 
 def _draw(g, shape, ints):
@@ -113,6 +117,12 @@ def run(case: Case):
         fg.sgemm_row_bias_relu(case.ta, case.tb, M, N, K, case.alpha, pA, lda, pB, ldb, case.beta,
                                pC, ldc, prow, case.relu, stream=stream)
     elif case.math >= 0:
+        if case.math != fg.MATH_FP32 and case.expect_tc is not None:
+            path = fg.math_supported(case.math, case.ta, case.tb, M, N, K, case.alpha, pA, lda, sA,
+                                     pB, ldb, sB, nb)
+            assert path == (1 if case.expect_tc else 0), (
+                "fgemm_math_supported says %d, the case expects %s" % (
+                    path, "the tensor cores" if case.expect_tc else "the CUDA-core fallback"))
         fg.gemm_math(case.math, case.ta, case.tb, M, N, K, case.alpha, pA, lda, sA, pB, ldb, sB,
                      case.beta, pC, ldc, sC, nb, pbias, case.relu, stream=stream)
     else:

@@ -195,3 +195,35 @@ def test_selector_extreme_arguments():
     for M, N, b in ((128 * 152, 128, 1), (128 * 19, 128 * 8, 1), (128, 128, 152 * 3)):
         assert (-(-M // 128) * -(-N // 128) * b) % 152 == 0
         assert not fg.config_name(sel(0, 0, M, N, 4096, b, 1, 152)).endswith("split")
+
+
+def test_math_supported_host_query():
+    q = fg.math_supported
+    # FP32 is always what it says; an unknown arithmetic is -1
+    assert q(fg.MATH_FP32, 0, 0, 4, 4, 4, 1.0, FAKE + 4, 5, 0, FAKE, 4, 0, 1) == 1
+    assert q(7, 0, 0, 4, 4, 4, 1.0, FAKE, 4, 0, FAKE, 4, 0, 1) == -1
+    for math in (fg.MATH_TF32, fg.MATH_3XTF32):
+        # calls the tensor-core kernel cannot take fall back to the CUDA cores
+        assert q(math, 0, 0, 4, 4, 4, 1.0, FAKE + 4, 4, 0, FAKE, 4, 0, 1) == 0  # A unaligned
+        assert q(math, 0, 0, 4, 4, 4, 1.0, FAKE, 4, 0, FAKE, 5, 0, 1) == 0  # ldb not x4
+        assert q(math, 0, 0, 4, 4, 4, 1.0, FAKE, 4, 6, FAKE, 4, 16, 2) == 0  # strideA not x4
+        assert q(math, 0, 0, 4, 4, 0, 1.0, FAKE, 4, 0, FAKE, 4, 0, 1) == 0  # K == 0
+        assert q(math, 0, 0, 4, 4, 4, 0.0, FAKE, 4, 0, FAKE, 4, 0, 1) == 0  # alpha == 0
+        assert q(math, 0, 0, 0, 4, 4, 1.0, FAKE, 4, 0, FAKE, 4, 0, 1) == 0  # empty
+
+
+def test_noalloc_checks_arguments_before_the_scratch_size():
+    # 4 slices of a 2048 x 2048 C need 64 MiB of partial products, more than the array
+    # holds: a valid call is refused as not supported, an invalid one as invalid --
+    # both before any CUDA call.
+    M = N = 2048
+    K, splits = 4096, 4
+    assert fg.splitk_workspace_size(M, N, K, splits) > fg.NOALLOC_SCRATCH_BYTES
+    ok = dict(transa=0, transb=0, M=M, N=N, K=K, alpha=1.0, A=FAKE, lda=K, B=FAKE, ldb=N,
+              beta=0.0, C=FAKE, ldc=N, bias=None, apply_relu=False, splits=splits)
+    assert fg.sgemm_splitk_noalloc(**ok, check=False) == fg.ERR_NOT_SUPPORTED
+    for bad in (dict(ldc=N - 1), dict(lda=K - 1), dict(M=-1), dict(splits=0), dict(splits=65),
+                dict(C=None), dict(A=None)):
+        assert fg.sgemm_splitk_noalloc(**dict(ok, **bad), check=False) == fg.ERR_INVALID_VALUE
+    # nothing to do is a no-op at any size
+    assert fg.sgemm_splitk_noalloc(**dict(ok, M=0), check=False) == fg.OK

@@ -37,6 +37,7 @@ def draw(rng):
         kw["bias"] = False  # the strided-batch entry point has no epilogue options
     if path < 0.3:
         kw["math"] = rng.choice([fg.MATH_TF32, fg.MATH_3XTF32])
+        kw["expect_tc"] = None  # random offsets and padding decide the path
     elif path < 0.7 and not unaligned:
         kw["config"] = rng.randrange(fg.num_configs())
     return kw

@@ -91,6 +91,7 @@ def test_tensor_core_path_replays(math):
     A, B = _ints((M, K), 8), _ints((K, N), 9)
     C = torch.empty(M, N, device="cuda")
     mode = fg.MATH_TF32 if math == "tf32" else fg.MATH_3XTF32
+    assert fg.math_supported(mode, 0, 0, M, N, K, 1.0, A, K, 0, B, N, 0, 1) == 1
     _capture_and_compare(
         lambda: fg.gemm_math(mode, 0, 0, M, N, K, 1.0, A, K, 0, B, N, 0, 0.0, C, N, 0, 1), C)
     # small integers are exact in TF32

@@ -84,15 +84,17 @@ def test_unaligned_falls_back_to_fp32(math, ta, tb):
     # Calls the tensor-core kernel cannot take run the FP32 kernel: exact on integers and
     # within the FP32 bound on floats.
     check(Case(ta=ta, tb=tb, M=100, N=60, K=50, math=math, offset=(1, 0, 0), align_ld=False,
-               seed=13))
+               seed=13, expect_tc=False))
     check(Case(ta=ta, tb=tb, M=100, N=60, K=50, math=math, offset=(0, 0, 0), pad=(1, 3, 0),
-               align_ld=False, ints=False, seed=14))
+               align_ld=False, ints=False, seed=14, expect_tc=False))
 
 
 @pytest.mark.parametrize("math", MODES, ids=["tf32", "3xtf32"])
 def test_k_zero_and_alpha_zero(math):
-    check(Case(ta=0, tb=1, M=70, N=90, K=0, alpha=3.0, beta=-2.0, bias=True, relu=True, math=math))
-    check(Case(ta=0, tb=0, M=70, N=90, K=33, alpha=0.0, beta=0.5, a_nan=True, math=math))
+    check(Case(ta=0, tb=1, M=70, N=90, K=0, alpha=3.0, beta=-2.0, bias=True, relu=True, math=math,
+               expect_tc=False))
+    check(Case(ta=0, tb=0, M=70, N=90, K=33, alpha=0.0, beta=0.5, a_nan=True, math=math,
+               expect_tc=False))
 
 
 def test_fp32_math_is_the_cuda_core_kernel():
