@@ -73,6 +73,8 @@ def parse_args(argv=None):
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the fused-vs-unfused FC layer timing added to the default run")
     ap.add_argument("--math", choices=("fp32", "tf32", "3xtf32"), default="fp32",
                     help="arithmetic: FP32 CUDA cores (the metric) or the tcgen05 tensor-core path")
     ap.add_argument("--splitk", type=int, default=0,
@@ -181,7 +183,7 @@ def aggregate(units: float, seconds: float, world: int, device=None):
 # ---- clocks -------------------------------------------------------------------------------
 
 class ClockSampler:
-    """nvidia-smi samples every 200 ms while the timed region runs."""
+    """nvidia-smi samples every 50 ms while the timed region runs."""
 
     def __init__(self, gpu_index: int, enabled: bool = True):
         self.gpu_index, self.enabled = gpu_index, enabled
@@ -194,7 +196,7 @@ class ClockSampler:
             try:
                 self.proc = subprocess.Popen(
                     ["nvidia-smi", "-i", str(self.gpu_index), "--query-gpu=" + SMI_FIELDS,
-                     "--format=csv,noheader,nounits", "-lms", "200"],
+                     "--format=csv,noheader,nounits", "-lms", "50"],
                     stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
                 time.sleep(0.3)
             except OSError:
@@ -243,9 +245,9 @@ class ClockSampler:
 # ---- the library arm ----------------------------------------------------------------------
 
 def tensor_peak_tflops(math: str):
-    """Dense TF32 tensor peak from the measured BF16 peak (MEASURED_PEAKS.json, burst)
-    times the nominal TF32/BF16 ratio 1.1/2.25; 3xTF32 does three TF32 products per
-    FP32 product, so its FP32-equivalent peak is a third of that."""
+    """Dense TF32 tensor peak derived from the measured BF16 peak (MEASURED_PEAKS.json,
+    burst) times the nominal TF32/BF16 ratio 1.1/2.25; 3xTF32 does three TF32 products
+    per FP32 product, so its FP32-equivalent peak is a third of that."""
     bf16, src = 1900.0, "fallback 1.9 PFLOP/s bf16"
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -255,6 +257,82 @@ def tensor_peak_tflops(math: str):
     div = 3.0 if math == "3xtf32" else 1.0
     return tf32 / div, "%s %.1f TFLOP/s x 1.1/2.25 (nominal TF32/BF16)%s" % (
         src, bf16, " / 3 products" if div == 3.0 else "")
+
+
+def calibrate_tf32_tflops(dev, n: int = 8192, reps: int = 5):
+    """Calibration of the dense TF32 tensor rate on this GPU (never a product path):
+    the vendor library's TF32 GEMM (torch.matmul with TF32 allowed) on one n^3 problem,
+    best of `reps` calls after warm-up, CUDA events.  Returns TFLOP/s."""
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        g = torch.Generator(device=dev).manual_seed(0)
+        a = torch.rand((n, n), device=dev, generator=g)
+        b = torch.rand((n, n), device=dev, generator=g)
+        c = torch.empty((n, n), device=dev)
+        for _ in range(3):
+            torch.matmul(a, b, out=c)
+        best = None
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b, out=c)
+            e1.record()
+            torch.cuda.synchronize()
+            t = e0.elapsed_time(e1) / 1e3
+            best = t if best is None else min(best, t)
+        del a, b, c
+        torch.cuda.empty_cache()
+        return 2.0 * n ** 3 / best / 1e12
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+def fc_secondary(fg, dev, stream, calls: int = 3, clocks: bool = True):
+    """The fully-connected layer (X 8192 x 4096, W 4096 x 11008, bias, ReLU) fused in the
+    GEMM epilogue against the plain GEMM of the same shape: `calls` timed calls each
+    (one warm-up call, L2 flushed before every call, CUDA events on the stream), and
+    the fused/unfused throughput ratio."""
+    w = workloads.make("fc8192x4096x11008")
+    dA, dB, dbias = w.A.to(dev), w.B.to(dev), w.bias.to(dev)
+    dC = torch.empty((w.M, w.N), device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sh = stream.cuda_stream
+
+    def fused():
+        fg.sgemm_bias_relu(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, dB, w.ldb, w.beta, dC,
+                           w.ldc, dbias, True, stream=sh)
+
+    def plain():
+        fg.sgemm(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, dB, w.ldb, w.beta, dC, w.ldc,
+                 stream=sh)
+
+    out = {}
+    sampler = ClockSampler(dev.index or 0, enabled=clocks)
+    with sampler, torch.cuda.stream(stream):
+        for name, fn in (("fused_bias_relu", fused), ("plain_gemm", plain)):
+            fn()
+            times = []
+            for _ in range(calls):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                e1.synchronize()
+                times.append(e0.elapsed_time(e1) / 1e3)
+            t = statistics.median(times)
+            out[name] = {"tflops": round(w.flops / t / 1e12, 3), "ms": round(t * 1e3, 4)}
+    del dA, dB, dbias, dC, flush
+    torch.cuda.empty_cache()
+    res = {"workload": describe(w), "calls_each": calls,
+           "l2": "flushed before every call",
+           "fused_over_unfused": round(out["fused_bias_relu"]["tflops"] /
+                                       out["plain_gemm"]["tflops"], 4), **out}
+    clk = sampler.summary()
+    if clk is not None:
+        res["clocks"] = clk
+    return res
 
 
 def stated_peak_tflops(device) -> tuple:
@@ -527,18 +605,30 @@ def run_fgemm(args, rank, world, local_rank):
     if back_to_back is not None:
         line["back_to_back"] = back_to_back
     if tensor_path:
-        tpeak, tsrc = tensor_peak_tflops(args.math)
+        derived, dsrc = tensor_peak_tflops(args.math)
+        cal = calibrate_tf32_tflops(dev)
+        div = 3.0 if args.math == "3xtf32" else 1.0
+        tpeak = cal / div
         line["roofline"] = {"bound": "tensor", "achieved": round(achieved, 4),
                             "peak": round(tpeak, 2), "unit": UNIT,
                             "frac": round(achieved / tpeak, 4),
                             "traffic": recorded_traffic(kernel_name, args.workload),
-                            "peak_source": tsrc}
+                            "peak_source": "calibrated on this GPU: vendor TF32 GEMM (torch.matmul, "
+                                           "TF32 allowed) 8192^3, best of 5 = %.1f TFLOP/s%s" % (
+                                               cal, " / 3 products" if div == 3.0 else ""),
+                            "peak_derived": round(derived, 2), "peak_derived_source": dsrc,
+                            "frac_of_derived": round(achieved / derived, 4)}
     clk = sampler.summary()
     if clk is not None:
         line["clocks"] = clk
         if clk.get("sm_mhz") and not tensor_path:
             line["roofline"]["frac_at_measured_clock"] = round(
                 achieved / (peak * clk["sm_mhz"] / STATED_SM_MHZ), 4)
+    if (rank == 0 and not args.no_secondary and args.workload == "square4096"
+            and not tensor_path and args.config < 0 and splitk is None):
+        # the fused-epilogue target: FC layer fused against the plain GEMM of its shape
+        line["secondary"] = {"fc_fused_vs_unfused": fc_secondary(
+            fg, dev, stream, clocks=not args.no_clocks)}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     return line
