@@ -587,11 +587,13 @@ def run_fgemm(args, rank, world, local_rank):
                     "max": round(max(step_ms), 5)},
         "build": build_info(),
     }
-    if kernel_name.endswith(("_split", "_ksplit")) and not tensor_path:
-        line["roofline"]["kernels"] = ("two launches of simt_gemm_kernel (whole tiles, then the "
-                                       "last wave's tiles as %s), timed together as one call" % (
-                                           "k-slice clusters" if kernel_name.endswith("_ksplit")
-                                           else "quarter tiles"))
+    if kernel_name.endswith(("_split", "_ksplit", "_kchain")) and not tensor_path:
+        line["roofline"]["kernels"] = (
+            "launches of simt_gemm_kernel (whole tiles, then the last wave's tiles as %s), "
+            "timed together as one call" % (
+                "k-slice clusters" if kernel_name.endswith("_ksplit")
+                else "%d chained k-slice launches" % KCHAIN_SLICES
+                if kernel_name.endswith("_kchain") else "quarter tiles"))
     # Algorithmic HBM bytes per step (A and B read, C written, C read when beta != 0,
     # the bias) over the step time: the bandwidth side of the roofline, which matters
     # for the skinny shapes (the QK^T batch writes 2 GiB).
@@ -634,13 +636,18 @@ def run_fgemm(args, rank, world, local_rank):
     return line
 
 
+KCHAIN_SLICES = 4  # k-slices (one launch each) of the last wave in the k-chain configuration
+
+
 def call_launches(config_name, M, N, batch, sms):
     """Kernel launches of one CUDA-core library call: the last-wave splits launch their
-    whole 128 x 128 tiles, then the last (tiles mod SMs) tiles, each part only when it
-    is not empty; the other configurations launch once per 65535 problems."""
-    if config_name.endswith(("_split", "_ksplit")):
+    whole 128 x 128 tiles, then the last (tiles mod SMs) tiles -- one launch, or one per
+    k-slice for the k-chain -- each part only when it is not empty; the other
+    configurations launch once per 65535 problems."""
+    if config_name.endswith(("_split", "_ksplit", "_kchain")):
         total = -(-M // 128) * -(-N // 128) * batch
-        return int(total - total % sms > 0) + int(total % sms > 0)
+        tail = KCHAIN_SLICES if config_name.endswith("_kchain") else 1
+        return int(total - total % sms > 0) + tail * int(total % sms > 0)
     return (batch + 65534) // 65535
 
 

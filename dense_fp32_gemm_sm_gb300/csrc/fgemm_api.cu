@@ -26,6 +26,7 @@ const ConfigInfo kConfigs[NUM_CONFIGS] = {
     {"simt_32x32x32_t4x4_s8_k4", 32, 32, true},
     {"simt_128x128_t8x8_split", 128, 128, true},
     {"simt_128x128_t8x8_ksplit", 128, 128, true},
+    {"simt_128x128_t8x8_kchain", 128, 128, true},
 };
 
 namespace {

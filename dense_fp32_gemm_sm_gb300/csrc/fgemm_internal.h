@@ -26,7 +26,10 @@ enum ConfigId {
                             // then run as 64x64 quarters with four k-groups (second launch)
     CFG_128x128_KSPLIT = 7, // CFG_128x128 for all but the last (tiles mod SMs) tiles, which
                             // then run as clusters of four k-slices of whole tiles (second launch)
-    NUM_CONFIGS = 8,
+    CFG_128x128_KCHAIN = 8, // CFG_128x128 for all but the last (tiles mod SMs) tiles, which
+                            // then run as four k-slices of whole tiles, one launch each,
+                            // added into C in slice order (programmatic dependent launches)
+    NUM_CONFIGS = 9,
 };
 
 struct ConfigInfo {

@@ -93,6 +93,10 @@ double model_us(const LaunchModel &m, double ctas, long long K, int num_sms)
 // 152 SMs: 74 clusters of four are resident at two CTAs per SM (296 CTAs, not 304:
 // a cluster stays inside one GPC), and the k-split tail of r tiles takes
 // ceil(r / 37) rounds of a quarter of a whole-tile period.
+// Fixed cost of the k-chain's four programmatically dependent launches (their
+// ordered additions into C), measured on GB300.
+constexpr double kKchainUs = 10.0;
+
 long long ksplit_clusters_per_round(int num_sms)
 {
     const long long c = num_sms / 4 - 1;
@@ -123,6 +127,13 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
     // within 2-7 % of the whole-tile model at K / 4 on 152 SMs)
     const double rounds = (double)ceil_div(r, ksplit_clusters_per_round(num_sms));
     const double ksplit = main_us + (r > 0 ? model_n_us(mm[M_128x128], rounds, (double)k / 4.0) : 0.0);
+    // k-chain tiles: 4r whole-tile CTAs over K / 4 each, spread over the SMs without
+    // cluster placement, plus the cost of chaining four launches (measured on 152 SMs:
+    // 4096^3 tail 257 us against 248 us for the model's 448 CTAs at K = 1024; FC and
+    // 2048^3 tails 10-15 us above the cluster k-split's single round).
+    const double kchain = main_us + (r > 0 ? model_us(mm[M_128x128], 4.0 * (double)r,
+                                                      (double)k / 4.0, num_sms) + kKchainUs
+                                           : 0.0);
     struct Option {
         int config;
         double us;
@@ -131,6 +142,7 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
         {CFG_128x128, model_us(mm[M_128x128], tiles128, k, num_sms)},
         {CFG_128x128_SPLIT, r > 0 ? split : 1e300},
         {CFG_128x128_KSPLIT, r > 0 ? ksplit : 1e300},
+        {CFG_128x128_KCHAIN, r > 0 ? kchain : 1e300},
         {CFG_128x64, model_us(mm[M_128x64], tiles_of(M, N, 128, 64, b), k, num_sms)},
         {CFG_64x64, model_us(mm[M_64x64], tiles_of(M, N, 64, 64, b), k, num_sms)},
         {CFG_32x32, model_us(mm[M_32x32], tiles_of(M, N, 32, 32, b), k, num_sms)},

@@ -405,15 +405,40 @@ enum TileMap {
     // add their partial sums through distributed shared memory in slice order and
     // write the tile, a 1/KSPLIT band of rows each.
     TILE_KSPLIT = 3,
+    // One-dimensional grid, one launch per k-slice (argument `chain` = slice | slices
+    // << 8): CTA t multiplies that k-slice of tile full_units + t of the linear tile
+    // order.  The slices of a tile are added in C itself, in slice order: slice 0
+    // writes alpha * P_0 (+ beta * C), slice s > 0 waits for the launch of slice s - 1
+    // to complete (griddepcontrol.wait: programmatic dependent launch), adds alpha * P_s
+    // to what is in C and writes it back, and the last slice applies bias and ReLU.
+    // Each launch lets the next one start as soon as all of its CTAs are running
+    // (griddepcontrol.launch_dependents), so the slices' products overlap and only the
+    // additions into C are ordered.
+    TILE_KCHAIN = 4,
 };
 constexpr int KSPLIT = 4;
+
+// griddepcontrol (programmatic dependent launch, sm_90+): let the next kernel of the
+// stream start launching; wait until the preceding kernel has completed and its
+// memory operations are visible.  Both are no-ops without a programmatic dependency.
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void pdl_wait_prerequisite()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
 
 // MAP and Parent select the tile of each CTA; the body is the same for every map.
 // (Moving the body into a function called from three kernels measured 1 % slower
 // at 4096^3, so the maps live here as compile-time branches.)
 template <class Cfg, int MAP = TILE_GRID, class Parent = Cfg>
-__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(const GemmParams p)
+__global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
+    simt_gemm_kernel(const GemmParams p, int chain = 0)
 {
+    if constexpr (MAP == TILE_KCHAIN) pdl_launch_dependents();
     extern __shared__ __align__(128) float smem[];
     float *const sA_all = smem;
     float *const sB_all = smem + Cfg::STAGES * Cfg::A_STAGE;
@@ -449,7 +474,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
                       "a quarter CTA computes one quarter of a parent tile");
         const long long tiles = (long long)p.tiles_m * p.tiles_n;
         const long long t = MAP == TILE_LINEAR ? (long long)blockIdx.x
-                                               : (long long)p.full_units + (blockIdx.x >> 2);
+                            : MAP == TILE_KCHAIN ? (long long)p.full_units + blockIdx.x
+                                                 : (long long)p.full_units + (blockIdx.x >> 2);
         static_assert(MAP != TILE_KSPLIT || KSPLIT == 4, "k-slice CTAs are numbered 4 t' + slice");
         bz = t / tiles;
         const int pid = (int)(t - bz * tiles);
@@ -472,9 +498,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
     // k range of this CTA: all of K, or one k-slice (whole stages) of a k-split tile.
     int k_len = p.K;
     long long a_koff = 0, b_koff = 0;
-    if constexpr (MAP == TILE_KSPLIT) {
-        const int slice = (int)cluster_rank();
-        const int per = ((p.K + KSPLIT - 1) / KSPLIT + Cfg::BK - 1) / Cfg::BK * Cfg::BK;
+    if constexpr (MAP == TILE_KSPLIT || MAP == TILE_KCHAIN) {
+        const int slice = MAP == TILE_KSPLIT ? (int)cluster_rank() : (chain & 0xFF);
+        const int slices = MAP == TILE_KSPLIT ? KSPLIT : (chain >> 8);
+        const int per = ((p.K + slices - 1) / slices + Cfg::BK - 1) / Cfg::BK * Cfg::BK;
         const int kb = min(p.K, slice * per);
         k_len = min(p.K - kb, per);
         a_koff = Cfg::TA ? (long long)kb * p.lda : kb;
@@ -673,6 +700,64 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB) simt_gemm_kernel(cons
             }
         }
         cluster_sync();  // no CTA leaves while another still reads its shared memory
+        return;
+    }
+
+    // ---- k-chain tiles: add this slice's products to C in slice order.
+    if constexpr (MAP == TILE_KCHAIN) {
+        const int slice = chain & 0xFF, slices = chain >> 8;
+        const bool first = slice == 0, last = slice + 1 == slices;
+        const bool products = KT > 0;
+        // C holds the sum of the earlier slices once the previous launch is complete;
+        // read it past L1 (.cg), which may hold lines an earlier slice replaced.
+        if (!first) pdl_wait_prerequisite();
+        const bool has_bias = last && p.bias != nullptr;
+        const bool has_row_bias = last && p.row_bias != nullptr;
+        const bool relu = last && p.relu;
+#pragma unroll
+        for (int i = 0; i < TM; ++i) {
+            const int gr = m0 + frag_row<Cfg>(wm0, lr, i);
+            if (gr >= p.M) continue;
+            float *const crow = C + (long long)gr * p.ldc;
+            const float rb = has_row_bias ? __ldg(p.row_bias + gr) : 0.0f;
+#pragma unroll
+            for (int g = 0; g < TN / 4; ++g) {
+                const int gc = n0 + frag_col<Cfg>(wn0, lc, 4 * g);
+                float v[4] = {acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
+                              acc[i][2 * g + 1].y};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) v[e] = products ? p.alpha * v[e] : 0.0f;
+                float *const dst = crow + gc;
+                if (p.c_vec && gc + 3 < p.N) {
+                    if (!first || p.beta != 0.0f) {
+                        const float4 c = __ldcg(reinterpret_cast<const float4 *>(dst));
+                        const float w = first ? p.beta : 1.0f;
+                        v[0] = fmaf(w, c.x, v[0]);
+                        v[1] = fmaf(w, c.y, v[1]);
+                        v[2] = fmaf(w, c.z, v[2]);
+                        v[3] = fmaf(w, c.w, v[3]);
+                    }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (has_bias) v[e] += __ldg(p.bias + gc + e);
+                        if (has_row_bias) v[e] += rb;
+                        if (relu) v[e] = fmaxf(v[e], 0.0f);
+                    }
+                    *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        if (gc + e >= p.N) break;
+                        float o = v[e];
+                        if (!first || p.beta != 0.0f) o = fmaf(first ? p.beta : 1.0f, __ldcg(dst + e), o);
+                        if (has_bias) o += __ldg(p.bias + gc + e);
+                        if (has_row_bias) o += rb;
+                        if (relu) o = fmaxf(o, 0.0f);
+                        dst[e] = o;
+                    }
+                }
+            }
+        }
         return;
     }
 

@@ -223,7 +223,49 @@ static fgemm_status launch_simt_ksplit(const GemmParams &p0, int batch, cudaStre
         cfg.stream = stream;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, simt_gemm_kernel<Main, TILE_KSPLIT>, p) != cudaSuccess) {
+        if (cudaLaunchKernelEx(&cfg, simt_gemm_kernel<Main, TILE_KSPLIT>, p, 0) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return FGEMM_ERR_LAUNCH;
+        }
+    }
+    return FGEMM_OK;
+}
+
+// Last-wave k-chain: the first (tiles - r) tiles whole, then the last r = tiles mod SMs
+// tiles in KCHAIN_SLICES k-slices, one launch per slice (TILE_KCHAIN).  The launches of
+// slices 1.. are programmatic dependents of the one before (they may start while it
+// runs and wait for it only before adding into C), so the slices' products run side by
+// side over r * KCHAIN_SLICES CTAs; the additions into C happen in slice order.
+constexpr int KCHAIN_SLICES = 4;
+
+template <class Main>
+static fgemm_status launch_simt_kchain(const GemmParams &p0, int batch, cudaStream_t stream)
+{
+    struct KchainTag {};
+    GemmParams p = p0;
+    long long rem = 0;
+    fgemm_status st = plan_split<Main>(p, batch, 1, &rem);
+    if (st != FGEMM_OK) return st;
+    if (prepare_kernel_fn<KchainTag>(simt_gemm_kernel<Main, TILE_KCHAIN>, Main::SMEM_BYTES) !=
+        cudaSuccess) {
+        (void)cudaGetLastError();
+        return FGEMM_ERR_LAUNCH;
+    }
+    st = launch_whole_tiles<Main>(p, batch, stream);
+    if (st != FGEMM_OK) return st;
+    for (int s = 0; rem > 0 && s < KCHAIN_SLICES; ++s) {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)rem, 1, 1);
+        cfg.blockDim = dim3(Main::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = Main::SMEM_BYTES;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = s > 0 ? 1 : 0;  // slice 0 follows the whole tiles in stream order
+        const int chain = s | (KCHAIN_SLICES << 8);
+        if (cudaLaunchKernelEx(&cfg, simt_gemm_kernel<Main, TILE_KCHAIN>, p, chain) != cudaSuccess) {
             (void)cudaGetLastError();
             return FGEMM_ERR_LAUNCH;
         }
@@ -242,7 +284,8 @@ static fgemm_status launch_simt_ksplit(const GemmParams &p0, int batch, cudaStre
         &launch_simt_split<ConfigOf<CFG_128x128, TA, TB>::type,            \
                            SplitTailOf<TA, TB>::type>,                     \
         &launch_simt_ksplit<ConfigOf<CFG_128x128, TA, TB>::type>,          \
+        &launch_simt_kchain<ConfigOf<CFG_128x128, TA, TB>::type>,          \
     };                                                                     \
-    static_assert(NUM_CONFIGS == 8, "one launcher per configuration");
+    static_assert(NUM_CONFIGS == 9, "one launcher per configuration");
 
 }  // namespace fgemm

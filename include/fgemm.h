@@ -246,12 +246,16 @@ const char *fgemm_status_string(fgemm_status status);
  * SM runs, times a per-k cost, with a latency floor).  The calls below expose that
  * choice so every configuration can be tested on edge shapes, and timed.
  *
- * Two configurations issue two kernel launches on the caller's stream: whole
- * 128 x 128 tiles first, then the last (tiles mod SMs) tiles either as 64 x 64
- * quarter tiles ("..._split") or as thread-block clusters of four CTAs that each
- * multiply one k-slice of a tile and add their partial sums through distributed
- * shared memory in a fixed order ("..._ksplit").  Both allocate nothing and give
- * the same result on every run.
+ * Three configurations issue more than one kernel launch on the caller's stream:
+ * whole 128 x 128 tiles first, then the last (tiles mod SMs) tiles either as 64 x 64
+ * quarter tiles ("..._split", one more launch), as thread-block clusters of four CTAs
+ * that each multiply one k-slice of a tile and add their partial sums through
+ * distributed shared memory in a fixed order ("..._ksplit", one more launch), or as
+ * four k-slices of every tile, one launch per slice, each adding its products into C
+ * in slice order ("..._kchain", four more launches; slices 1-3 are programmatic
+ * dependent launches that start while the previous slice runs and wait for it only
+ * before their additions).  All allocate nothing and give the same result on every
+ * run.
  * ------------------------------------------------------------------------- */
 
 /* Number of kernel configurations; valid ids are 0 .. fgemm_num_configs()-1. */

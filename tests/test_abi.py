@@ -112,7 +112,8 @@ def test_selector():
     assert sel(0, 0, 4096, 4096, 4096, 1, 0, 152) in scalar
     # Choices of the fitted launch-time model on 152 SMs (each measured fastest, or
     # within 1 %, on a GB300):
-    assert name(0, 0, 4096, 4096, 4096, 1, 1, 152) == "simt_128x128_t8x8_split"  # r = 112
+    assert name(0, 0, 4096, 4096, 4096, 1, 1, 152) == "simt_128x128_t8x8_kchain"  # r = 112
+    assert name(0, 1, 4096, 4096, 4096, 1, 1, 152) == "simt_128x128_t8x8_kchain"
     assert name(0, 0, 4096, 4864, 4096, 1, 1, 152) == "simt_128x128_t8x8"  # 8 x 152 tiles
     assert name(0, 0, 4096, 3648, 4096, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # r = 16
     assert name(0, 0, 8192, 11008, 4096, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # r = 32

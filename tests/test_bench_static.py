@@ -37,6 +37,10 @@ def test_call_launches():
     assert bench.call_launches("simt_128x128_t8x8_ksplit", 4096, 4864, 1, 152) == 1  # 8 x 152
     assert bench.call_launches("simt_128x128_t8x8_ksplit", 1024, 1024, 1, 152) == 1  # 64 < 152
     assert bench.call_launches("simt_128x128_t8x8_ksplit", 2048, 128, 128, 152) == 2
+    # the k-chain: whole tiles, then one launch per k-slice of the last wave
+    assert bench.call_launches("simt_128x128_t8x8_kchain", 4096, 4096, 1, 152) == 1 + 4
+    assert bench.call_launches("simt_128x128_t8x8_kchain", 4096, 4864, 1, 152) == 1
+    assert bench.call_launches("simt_128x128_t8x8_kchain", 1024, 1024, 1, 152) == 4
     # the per-problem grid splits a batch into chunks of 65535 problems
     assert bench.call_launches("simt_32x32x16_t4x4_s4", 64, 64, 65535, 152) == 1
     assert bench.call_launches("simt_32x32x16_t4x4_s4", 64, 64, 65536, 152) == 2

@@ -50,7 +50,8 @@ def _capture_and_compare(call, out):
 
 
 @pytest.mark.parametrize("name", ["simt_128x128_t8x8", "simt_128x128_t8x8_split",
-                                  "simt_128x128_t8x8_ksplit", "simt_32x32x32_t4x4_s8_k4"])
+                                  "simt_128x128_t8x8_ksplit", "simt_128x128_t8x8_kchain",
+                                  "simt_32x32x32_t4x4_s8_k4"])
 def test_explicit_configs_replay(name):
     M, N, K = 1700, 1652, 200  # 182 tiles of 128 x 128: whole tiles and a last wave
     A, B, bias = _ints((M, K), 1), _ints((K, N), 2), _ints((N,), 3)

@@ -18,14 +18,15 @@ pytestmark = pytest.mark.gpu
 # For each configuration and layout the test takes the smallest shape of this list
 # on which the selector, at this GPU's SM count, picks that configuration.
 CANDIDATES = sorted(
-    ((M, N, K) for K in (40, 64, 100, 256, 512) for M in range(96, 2500, 100)
+    ((M, N, K) for K in (40, 64, 100, 256, 512, 2048) for M in range(96, 2500, 100)
      for N in (M, M + 36, 2 * M + 10)),
     key=lambda s: s[0] * s[1] * s[2])
 TARGETS = ["simt_128x128_t8x8", "simt_128x128_t8x8_split", "simt_128x128_t8x8_ksplit",
-           "simt_128x64x16_t8x8_s4", "simt_64x64x16_t4x4_s4", "simt_32x32x16_t4x4_s4",
-           "simt_32x32x32_t4x4_s8_k4"]
-# The quarter-tile split wins only in narrow bands of the tile remainder; where no
-# candidate reaches it, its epilogue (the whole-tile one) is covered by the others.
+           "simt_128x128_t8x8_kchain", "simt_128x64x16_t8x8_s4", "simt_64x64x16_t4x4_s4",
+           "simt_32x32x16_t4x4_s4", "simt_32x32x32_t4x4_s8_k4"]
+# The quarter-tile split wins only in narrow bands of the tile remainder (the k-chain
+# takes most of them); where no candidate reaches it, its epilogue (the whole-tile one)
+# is covered by the others.
 OPTIONAL = {"simt_128x128_t8x8_split"}
 
 

@@ -1,10 +1,11 @@
 """The last-wave split launches against the FP64 oracle.
 
-Both compute the first (tiles - r) 128 x 128 tiles whole and then the last
+All compute the first (tiles - r) 128 x 128 tiles whole and then the last
 r = tiles mod SMs another way: simt_128x128_t8x8_split as 64 x 64 quarter tiles
 with four k-groups, simt_128x128_t8x8_ksplit as clusters of four CTAs that each
 multiply one k-slice of a whole tile and add the partial sums through distributed
-shared memory.  These cases put whole and split tiles in one call, with split
+shared memory, simt_128x128_t8x8_kchain as four chained launches, one k-slice of
+every tile each, that add their products into C in slice order.  These cases put whole and split tiles in one call, with split
 tiles on the ragged bottom and right edges (quarters wholly outside the matrix are
 skipped), on the last problem of a strided batch, with k-slices that are short or
 empty, and in all four transpose layouts; integer data must come back bit-exact,
@@ -24,7 +25,7 @@ pytestmark = pytest.mark.gpu
 COMBOS = list(itertools.product((0, 1), (0, 1)))
 
 
-SPLITS = ["simt_128x128_t8x8_split", "simt_128x128_t8x8_ksplit"]
+SPLITS = ["simt_128x128_t8x8_split", "simt_128x128_t8x8_ksplit", "simt_128x128_t8x8_kchain"]
 
 
 def _config(name):
@@ -85,12 +86,24 @@ def test_every_tile_split_when_fewer_tiles_than_sms(split):
                    config=_config(split), seed=40 + 2 * ta + tb))
 
 
+@pytest.mark.parametrize("split", ["simt_128x128_t8x8_ksplit", "simt_128x128_t8x8_kchain"])
 @pytest.mark.parametrize("K", [0, 1, 31, 32, 33, 97, 128, 129])
-def test_k_slices_short_and_empty(K):
+def test_k_slices_short_and_empty(split, K):
     # K slices are whole 32-deep stages: K <= 96 leaves the last slices empty.
     for ta, tb in COMBOS:
         check(Case(ta=ta, tb=tb, M=300, N=260, K=K, alpha=1.0, beta=0.5, bias=True, relu=True,
-                   config=_config("simt_128x128_t8x8_ksplit"), seed=60 + K + 2 * ta + tb))
+                   config=_config(split), seed=60 + K + 2 * ta + tb))
+
+
+@pytest.mark.parametrize("ta,tb", COMBOS)
+def test_kchain_beta_zero_never_reads_c(ta, tb):
+    # beta = 0: the first slice writes alpha * P_0 without reading C (which holds NaN);
+    # later slices read only what earlier slices wrote.  Row bias on the last slice.
+    check(Case(ta=ta, tb=tb, M=1900, N=1700, K=300, alpha=1.0, beta=0.0, c_nan=True, bias=True,
+               relu=True, config=_config("simt_128x128_t8x8_kchain"), pad=(4, 8, 4),
+               seed=70 + 2 * ta + tb))
+    check(Case(ta=ta, tb=tb, M=1900, N=1700, K=300, alpha=-1.0, beta=0.0, c_nan=True,
+               ints=False, config=_config("simt_128x128_t8x8_kchain"), seed=75 + 2 * ta + tb))
 
 
 @pytest.mark.parametrize("split", SPLITS)
@@ -107,7 +120,7 @@ def test_selector_on_this_gpu():
     if sms != 152:
         pytest.skip("expectations measured on 152 SMs")
     name = lambda *a: fg.config_name(fg.select_config(*a, True, sms))
-    assert name(0, 0, 4096, 4096, 4096, 1) == "simt_128x128_t8x8_split"
+    assert name(0, 0, 4096, 4096, 4096, 1) == "simt_128x128_t8x8_kchain"
     assert name(0, 0, 8192, 11008, 4096, 1) == "simt_128x128_t8x8_ksplit"
     assert name(0, 0, 2048, 128, 2048, 128) == "simt_128x128_t8x8_ksplit"
     assert name(0, 1, 2048, 2048, 128, 128) == "simt_128x128_t8x8"
