@@ -10,9 +10,12 @@
 //    whose rows already run along m (A stored K x M) or n (B stored K x N) is
 //    copied with 16-byte vectors; an operand stored with k contiguous is
 //    transposed by the copy itself (4-byte cp.async, one element per lane, a
-//    warp covering 8 k x 4 rows so both the global reads and the shared writes
-//    are conflict-free).  Out-of-range rows/columns and the K tail are
-//    zero-filled by the copy (src-size 0), so the inner loop has no edge checks.
+//    warp covering 8 k x 4 rows: the global reads are whole 32-byte sectors and
+//    the 32 shared addresses fall in 32 distinct banks; ncu nevertheless counts
+//    about five shared wavefronts per such copy instruction, about one per
+//    sector read, where a 16-byte copy of a row takes one per 128 bytes).
+//    Out-of-range rows/columns and the K tail are zero-filled by the copy
+//    (src-size 0), so the inner loop has no edge checks.
 //
 //  * k-major tiles let every thread read its A and B fragments for one k with
 //    16-byte loads along m and n (the transposed-A idea of the same page, and the
@@ -48,6 +51,11 @@
 //    computed by a thread-block cluster of four CTAs that multiply one k-slice each;
 //    the partial tiles are added in slice order through distributed shared memory
 //    (no workspace, no atomics, the same result on every run).
+//
+//  * Last-wave k-chain (TILE_KCHAIN launches): the last r tiles stay whole, each in
+//    four k-slices, one launch per slice; each launch adds its slice's products into
+//    C in slice order, the later ones as programmatic dependent launches that run
+//    alongside the earlier ones and wait for them only before adding into C.
 //
 //  * The copy of a later stage is issued at k-step COPY_K of the current stage.
 #pragma once
@@ -270,8 +278,9 @@ struct KRowsCopy {
 // Stored block whose rows run along m (or n) with k contiguous (MN x K storage):
 // rows [r0, r0+ROWS) x k [k0, k0+BK) -> s[k][r] (a transpose).  Each warp moves
 // 8 (k) x 4 (rows) patches: lane&7 picks k, lane>>3 picks the row, so a warp reads
-// four full 32-byte sectors and writes 32 distinct banks.  A thread keeps one k and
-// copies rows r_base + it * RSTEP.
+// four full 32-byte sectors and writes 32 distinct banks (measured: about five
+// shared wavefronts per instruction all the same, see the file header).  A thread
+// keeps one k and copies rows r_base + it * RSTEP.
 template <int BK, int ROWS, int S_LD, int THREADS, bool FAST>
 struct KColsCopy {
     static constexpr int WARPS = THREADS / 32;
