@@ -19,7 +19,7 @@ from gpu_harness import Case, check
 pytestmark = pytest.mark.gpu
 
 COMBOS = list(itertools.product((0, 1), (0, 1)))
-VEC_CONFIGS = [0, 1, 2, 4, 5, 6, 7]
+VEC_CONFIGS = [0, 1, 2, 4, 5, 6, 7, 8]
 SCALAR_CONFIG = 3
 SHAPES = [(300, 200, 130), (1, 1, 1), (129, 65, 17), (64, 128, 3), (7, 333, 64), (257, 31, 515)]
 
