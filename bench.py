@@ -14,6 +14,8 @@ Reported, besides the contract keys:
   cpu_baseline  the FP64 oracle timed on this host's cores on a bounded sample
                 of the same problem (whole rows of C)
   clocks        nvidia-smi samples taken during the timed region
+  secondary     (default run) the fused FC layer against the plain GEMM of its shape,
+                256^3 back to back in a CUDA graph, 1024^3 with alpha and beta
 
 ``--impl reference`` times the FP64 oracle instead (the only reference
 implementation this project has), each step a bounded sample of the workload.
@@ -286,6 +288,68 @@ def calibrate_tf32_tflops(dev, n: int = 8192, reps: int = 5):
         return 2.0 * n ** 3 / best / 1e12
     finally:
         torch.backends.cuda.matmul.allow_tf32 = prev
+
+
+def small_secondary(fg, dev, stream, graph_calls: int = 200, calls: int = 20):
+    """The small workloads beside the headline: 256^3 as the device time per call of
+    `graph_calls` calls captured back to back in one CUDA graph (warm L2, no host launch
+    cost), and 1024^3 with alpha = 1.5, beta = 0.5 as the median of `calls` single calls
+    with L2 flushed (C restored from C0 outside the timed events)."""
+    out = {}
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    sh = stream.cuda_stream
+    w = workloads.make("square256")
+    dA, dB, dC = w.A.to(dev), w.B.to(dev), torch.empty((w.M, w.N), device=dev)
+
+    def call256():
+        fg.sgemm(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, dB, w.ldb, w.beta, dC, w.ldc,
+                 stream=sh)
+
+    with torch.cuda.stream(stream):
+        call256()  # one-time setup outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        for _ in range(graph_calls):
+            call256()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        graph.replay()
+        torch.cuda.synchronize()
+        g0.record(stream)
+        graph.replay()
+        g1.record(stream)
+    torch.cuda.synchronize()
+    per = g0.elapsed_time(g1) / 1e3 / graph_calls
+    out["square256_back_to_back"] = {"workload": describe(w), "calls": graph_calls,
+                                     "us_per_call": round(per * 1e6, 3),
+                                     "tflops": round(w.flops / per / 1e12, 3),
+                                     "l2": "warm (calls back to back in one CUDA graph)"}
+    del graph
+    w = workloads.make("square1024")
+    dA, dB = w.A.to(dev), w.B.to(dev)
+    dC0, dC = w.C0.to(dev), torch.empty((w.M, w.N), device=dev)
+    times = []
+    with torch.cuda.stream(stream):
+        for i in range(calls + 3):
+            flush.zero_()
+            dC.copy_(dC0)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fg.sgemm(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, dB, w.ldb, w.beta, dC, w.ldc,
+                     stream=sh)
+            e1.record(stream)
+            e1.synchronize()
+            if i >= 3:
+                times.append(e0.elapsed_time(e1) / 1e3)
+    t = statistics.median(times)
+    out["square1024_alpha_beta"] = {"workload": describe(w), "calls": calls,
+                                    "us_per_call": round(t * 1e6, 2),
+                                    "tflops": round(w.flops / t / 1e12, 3),
+                                    "l2": "flushed before every call"}
+    del flush
+    torch.cuda.empty_cache()
+    return out
 
 
 def fc_secondary(fg, dev, stream, calls: int = 3, clocks: bool = True):
@@ -630,7 +694,7 @@ def run_fgemm(args, rank, world, local_rank):
             and not tensor_path and args.config < 0 and splitk is None):
         # the fused-epilogue target: FC layer fused against the plain GEMM of its shape
         line["secondary"] = {"fc_fused_vs_unfused": fc_secondary(
-            fg, dev, stream, clocks=not args.no_clocks)}
+            fg, dev, stream, clocks=not args.no_clocks), **small_secondary(fg, dev, stream)}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     return line
