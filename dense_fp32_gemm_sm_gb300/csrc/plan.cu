@@ -94,8 +94,10 @@ double model_us(const LaunchModel &m, double ctas, long long K, int num_sms)
 // a cluster stays inside one GPC), and the k-split tail of r tiles takes
 // ceil(r / 37) rounds of a quarter of a whole-tile period.
 // Fixed cost of the k-chain's four programmatically dependent launches (their
-// ordered additions into C), measured on GB300.
-constexpr double kKchainUs = 10.0;
+// ordered additions into C), and the time a last-wave launch saves by starting on the
+// SMs the whole tiles leave; measured on GB300.
+constexpr double kKchainUs = 8.0;
+constexpr double kTailOverlapUs = 35.0;
 
 long long ksplit_clusters_per_round(int num_sms)
 {
@@ -121,19 +123,28 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
     const double whole = tiles128 - (double)r;
     const LaunchModel *const mm = kModel[(ta ? 2 : 0) + (tb ? 1 : 0)];
     const double main_us = whole > 0 ? model_us(mm[M_128x128], whole, k, num_sms) : 0.0;
+    // Each last-wave launch is a programmatic dependent of the whole tiles: it starts on
+    // the SMs they leave, which hides its launch and the whole tiles' uneven end
+    // (measured on 152 SMs: the k-chain 25-40 us below whole tiles + tail model on nine
+    // shapes with K from 2048 to 4096).
+    // The saving grows with the whole tiles' length (K) up to the measured 35 us.
+    const double overlap = whole > 0 ? kTailOverlapUs * (k < 3072 ? (double)k / 3072.0 : 1.0) : 0.0;
     // quarter tiles: 4r CTAs of the quarter model
-    const double split = main_us + (r > 0 ? model_us(mm[M_QUARTER], 4.0 * (double)r, k, num_sms) : 0.0);
+    const double split = main_us - overlap +
+                         (r > 0 ? model_us(mm[M_QUARTER], 4.0 * (double)r, k, num_sms) : 0.0);
     // k-split tiles: whole-tile CTAs over K / 4 each, in rounds of clusters (measured
     // within 2-7 % of the whole-tile model at K / 4 on 152 SMs)
     const double rounds = (double)ceil_div(r, ksplit_clusters_per_round(num_sms));
-    const double ksplit = main_us + (r > 0 ? model_n_us(mm[M_128x128], rounds, (double)k / 4.0) : 0.0);
+    const double ksplit = main_us - overlap +
+                          (r > 0 ? model_n_us(mm[M_128x128], rounds, (double)k / 4.0) : 0.0);
     // k-chain tiles: 4r whole-tile CTAs over K / 4 each, spread over the SMs without
-    // cluster placement, plus the cost of chaining four launches (measured on 152 SMs:
-    // 4096^3 tail 257 us against 248 us for the model's 448 CTAs at K = 1024; FC and
-    // 2048^3 tails 10-15 us above the cluster k-split's single round).
-    const double kchain = main_us + (r > 0 ? model_us(mm[M_128x128], 4.0 * (double)r,
-                                                      (double)k / 4.0, num_sms) + kKchainUs
-                                           : 0.0);
+    // cluster placement, plus the cost of chaining four launches (measured with no
+    // whole tiles before them: 1024^3, 1280^2 x 4096, 1536^2 x 4096 3-11 us above the
+    // model's 4r CTAs at K / 4).
+    const double kchain = main_us - overlap +
+                          (r > 0 ? model_us(mm[M_128x128], 4.0 * (double)r, (double)k / 4.0,
+                                            num_sms) + kKchainUs
+                                 : 0.0);
     struct Option {
         int config;
         double us;

@@ -420,9 +420,10 @@ enum TileMap {
     // writes alpha * P_0 (+ beta * C), slice s > 0 waits for the launch of slice s - 1
     // to complete (griddepcontrol.wait: programmatic dependent launch), adds alpha * P_s
     // to what is in C and writes it back, and the last slice applies bias and ReLU.
-    // Each launch lets the next one start as soon as all of its CTAs are running
-    // (griddepcontrol.launch_dependents), so the slices' products overlap and only the
-    // additions into C are ordered.
+    // Each launch (and the whole-tile launch before slice 0) lets the next one start as
+    // soon as all of its CTAs are running (griddepcontrol.launch_dependents), so the
+    // slices' products overlap the launches before them and only the additions into C
+    // are ordered.
     TILE_KCHAIN = 4,
 };
 constexpr int KSPLIT = 4;
@@ -447,7 +448,11 @@ template <class Cfg, int MAP = TILE_GRID, class Parent = Cfg>
 __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
     simt_gemm_kernel(const GemmParams p, int chain = 0)
 {
-    if constexpr (MAP == TILE_KCHAIN) pdl_launch_dependents();
+    // Let a programmatic dependent launch of this call (the k-chain slices after the
+    // whole tiles, each slice after the one before) start as soon as every CTA of this
+    // launch is running.  Without such a dependent this does nothing.
+    if constexpr (MAP == TILE_KCHAIN || MAP == TILE_GRID || MAP == TILE_LINEAR)
+        pdl_launch_dependents();
     extern __shared__ __align__(128) float smem[];
     float *const sA_all = smem;
     float *const sB_all = smem + Cfg::STAGES * Cfg::A_STAGE;
@@ -655,6 +660,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
                                 acc[i][2 * g + 1].y);
         }
         cluster_sync();
+        // This launch may have started while the call's whole tiles were finishing;
+        // it completes only after them.
+        pdl_wait_prerequisite();
         const int band0 = (int)cluster_rank() * BAND;
         const bool products = p.K > 0;
         const bool has_bias = p.bias != nullptr, has_row_bias = p.row_bias != nullptr;
@@ -718,8 +726,10 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
         const bool first = slice == 0, last = slice + 1 == slices;
         const bool products = KT > 0;
         // C holds the sum of the earlier slices once the previous launch is complete;
-        // read it past L1 (.cg), which may hold lines an earlier slice replaced.
-        if (!first) pdl_wait_prerequisite();
+        // read it past L1 (.cg), which may hold lines an earlier slice replaced.  Slice 0
+        // waits too (for the whole tiles before it): its products need nothing from
+        // them, but then every launch of the call has completed when the last slice has.
+        pdl_wait_prerequisite();
         const bool has_bias = last && p.bias != nullptr;
         const bool has_row_bias = last && p.row_bias != nullptr;
         const bool relu = last && p.relu;
@@ -771,6 +781,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
     }
 
     // ---- Epilogue: alpha, beta, bias, ReLU in registers; vector stores where possible.
+    // (Quarter tiles may have started while the call's whole tiles were finishing;
+    // they complete only after them.)
+    if constexpr (MAP == TILE_QUARTER) pdl_wait_prerequisite();
     const bool products = KT > 0;
     const bool has_bias = p.bias != nullptr, has_row_bias = p.row_bias != nullptr;
     float bias_v[TN];

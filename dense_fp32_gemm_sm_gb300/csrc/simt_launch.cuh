@@ -185,9 +185,24 @@ static fgemm_status launch_simt_split(const GemmParams &p0, int batch, cudaStrea
     st = launch_whole_tiles<Main>(p, batch, stream);
     if (st != FGEMM_OK) return st;
     if (rem > 0) {
-        simt_gemm_kernel<Tail, TILE_QUARTER, Main><<<(unsigned)(4 * rem), Tail::THREADS,
-                                                     Tail::SMEM_BYTES, stream>>>(p);
-        if (cudaGetLastError() != cudaSuccess) return FGEMM_ERR_LAUNCH;
+        // A programmatic dependent of the whole tiles when there are any (it starts on
+        // the SMs they leave and waits for them before its stores); otherwise the call's
+        // first launch, in plain stream order.
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(4 * rem), 1, 1);
+        cfg.blockDim = dim3(Tail::THREADS, 1, 1);
+        cfg.dynamicSmemBytes = Tail::SMEM_BYTES;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = p.full_units > 0 ? 1 : 0;
+        if (cudaLaunchKernelEx(&cfg, simt_gemm_kernel<Tail, TILE_QUARTER, Main>, p, 0) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            return FGEMM_ERR_LAUNCH;
+        }
     }
     return FGEMM_OK;
 }
@@ -211,18 +226,22 @@ static fgemm_status launch_simt_ksplit(const GemmParams &p0, int batch, cudaStre
     st = launch_whole_tiles<Main>(p, batch, stream);
     if (st != FGEMM_OK) return st;
     if (rem > 0) {
-        cudaLaunchAttribute attr[1];
+        // Clusters of KSPLIT; a programmatic dependent of the whole tiles when there are
+        // any (see launch_simt_split).
+        cudaLaunchAttribute attr[2];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = KSPLIT;
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
+        attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[1].val.programmaticStreamSerializationAllowed = 1;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(KSPLIT * rem), 1, 1);
         cfg.blockDim = dim3(Main::THREADS, 1, 1);
         cfg.dynamicSmemBytes = Main::SMEM_BYTES;
         cfg.stream = stream;
         cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        cfg.numAttrs = p.full_units > 0 ? 2 : 1;
         if (cudaLaunchKernelEx(&cfg, simt_gemm_kernel<Main, TILE_KSPLIT>, p, 0) != cudaSuccess) {
             (void)cudaGetLastError();
             return FGEMM_ERR_LAUNCH;
@@ -232,10 +251,12 @@ static fgemm_status launch_simt_ksplit(const GemmParams &p0, int batch, cudaStre
 }
 
 // Last-wave k-chain: the first (tiles - r) tiles whole, then the last r = tiles mod SMs
-// tiles in KCHAIN_SLICES k-slices, one launch per slice (TILE_KCHAIN).  The launches of
-// slices 1.. are programmatic dependents of the one before (they may start while it
-// runs and wait for it only before adding into C), so the slices' products run side by
-// side over r * KCHAIN_SLICES CTAs; the additions into C happen in slice order.
+// tiles in KCHAIN_SLICES k-slices, one launch per slice (TILE_KCHAIN).  Every slice's
+// launch is a programmatic dependent of the launch before it (it may start while that
+// one runs and waits for it only before writing C), so the slices' products run side
+// by side over r * KCHAIN_SLICES CTAs and on SMs the whole tiles have left; the
+// additions into C happen in slice order.  The first launch of the call is never a
+// dependent: it follows the stream's earlier work, which may have written A or B.
 constexpr int KCHAIN_SLICES = 4;
 
 template <class Main>
@@ -263,7 +284,10 @@ static fgemm_status launch_simt_kchain(const GemmParams &p0, int batch, cudaStre
         cfg.dynamicSmemBytes = Main::SMEM_BYTES;
         cfg.stream = stream;
         cfg.attrs = attr;
-        cfg.numAttrs = s > 0 ? 1 : 0;  // slice 0 follows the whole tiles in stream order
+        // Slice 0 may start while the whole tiles of this call finish (they trigger their
+        // dependents at once); with no whole tiles it is the call's first launch and
+        // follows the stream's earlier work in plain stream order.
+        cfg.numAttrs = (s > 0 || p.full_units > 0) ? 1 : 0;
         const int chain = s | (KCHAIN_SLICES << 8);
         if (cudaLaunchKernelEx(&cfg, simt_gemm_kernel<Main, TILE_KCHAIN>, p, chain) != cudaSuccess) {
             (void)cudaGetLastError();

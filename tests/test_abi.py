@@ -117,9 +117,11 @@ def test_selector():
     assert name(0, 0, 4096, 4864, 4096, 1, 1, 152) == "simt_128x128_t8x8"  # 8 x 152 tiles
     assert name(0, 0, 4096, 3648, 4096, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # r = 16
     assert name(0, 0, 8192, 11008, 4096, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # r = 32
-    assert name(0, 0, 3072, 3072, 3072, 1, 1, 152) == "simt_128x128_t8x8"  # r = 120
+    # (last-wave launches start on the SMs the whole tiles leave: 3072^3 measured
+    # 928 us with the cluster k-split against 936 us with whole tiles only)
+    assert name(0, 0, 3072, 3072, 3072, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # r = 120
     assert name(0, 0, 2048, 2048, 2048, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # r = 104
-    assert name(0, 0, 1792, 1792, 1024, 1, 1, 152) == "simt_128x64x16_t8x8_s4"
+    assert name(0, 0, 1792, 1792, 1024, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # r = 44
     assert name(0, 0, 1280, 1280, 4096, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # all split
     assert name(0, 0, 768, 768, 768, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # 36 tiles
     assert name(0, 0, 768, 768, 128, 1, 1, 152) == "simt_64x64x16_t4x4_s4"
@@ -128,8 +130,9 @@ def test_selector():
     # batches: QK^T (32768 tiles, r = 88, K = 128) whole; Score x V (2048 tiles, r = 72)
     assert name(0, 1, 2048, 2048, 128, 128, 1, 152) == "simt_128x128_t8x8"
     assert name(0, 0, 2048, 128, 2048, 128, 1, 152) == "simt_128x128_t8x8_ksplit"
-    # the SM count enters: 1024 tiles on 148 SMs leave r = 136
-    assert name(0, 0, 4096, 4096, 4096, 1, 1, 148) == "simt_128x128_t8x8"
+    # the SM count enters: 1024 tiles on 148 SMs leave r = 136, which the k-chain would
+    # run in four CTAs per SM; the cluster k-split is estimated faster there
+    assert name(0, 0, 4096, 4096, 4096, 1, 1, 148) == "simt_128x128_t8x8_ksplit"
     assert sel(0, 0, -1, 4, 4, 1, 1, 152) == -1
     for ta in (0, 1):
         for tb in (0, 1):

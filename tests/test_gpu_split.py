@@ -124,4 +124,4 @@ def test_selector_on_this_gpu():
     assert name(0, 0, 8192, 11008, 4096, 1) == "simt_128x128_t8x8_ksplit"
     assert name(0, 0, 2048, 128, 2048, 128) == "simt_128x128_t8x8_ksplit"
     assert name(0, 1, 2048, 2048, 128, 128) == "simt_128x128_t8x8"
-    assert name(0, 0, 3072, 3072, 3072, 1) == "simt_128x128_t8x8"
+    assert name(0, 0, 3072, 3072, 3072, 1) == "simt_128x128_t8x8_ksplit"
