@@ -594,11 +594,13 @@ def run_fgemm(args, rank, world, local_rank):
                         "l2": "warm (calls back to back in one CUDA graph)"}
 
     def launches(config, M, N, K, batch):
-        """Kernel launches of one library call with this configuration (None: select)."""
+        """Kernel launches of one library call with this configuration (None: select),
+        as the library counts them (fgemm_launch_count)."""
         if config is None or config < 0:
             config = fg.select_config(w.ta, w.tb, M, N, K, batch, True, sms)
         name = fg.config_name(config)
-        return name, call_launches(name, M, N, batch, sms)
+        kk = K if w.alpha != 0 else 0
+        return name, fg.launch_count(config, w.ta, w.tb, M, N, kk, batch, True, sms)
 
     kernel_name, n_batch_launches = launches(args.config, w.M, w.N, w.K, max(1, w.batch))
     if splitk is not None:
@@ -656,7 +658,7 @@ def run_fgemm(args, rank, world, local_rank):
             "launches of simt_gemm_kernel (whole tiles, then the last wave's tiles as %s), "
             "timed together as one call" % (
                 "k-slice clusters" if kernel_name.endswith("_ksplit")
-                else "%d chained k-slice launches" % KCHAIN_SLICES
+                else "%d chained k-slice launches" % (n_batch_launches - 1)
                 if kernel_name.endswith("_kchain") else "quarter tiles"))
     # Algorithmic HBM bytes per step (A and B read, C written, C read when beta != 0,
     # the bias) over the step time: the bandwidth side of the roofline, which matters
@@ -698,21 +700,6 @@ def run_fgemm(args, rank, world, local_rank):
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     return line
-
-
-KCHAIN_SLICES = 4  # k-slices (one launch each) of the last wave in the k-chain configuration
-
-
-def call_launches(config_name, M, N, batch, sms):
-    """Kernel launches of one CUDA-core library call: the last-wave splits launch their
-    whole 128 x 128 tiles, then the last (tiles mod SMs) tiles -- one launch, or one per
-    k-slice for the k-chain -- each part only when it is not empty; the other
-    configurations launch once per 65535 problems."""
-    if config_name.endswith(("_split", "_ksplit", "_kchain")):
-        total = -(-M // 128) * -(-N // 128) * batch
-        tail = KCHAIN_SLICES if config_name.endswith("_kchain") else 1
-        return int(total - total % sms > 0) + tail * int(total % sms > 0)
-    return (batch + 65534) // 65535
 
 
 def describe(w):

@@ -22,6 +22,7 @@ from ._binding import (  # noqa: F401
     device_status,
     gemm_math,
     gemm_explicit,
+    launch_count,
     library,
     math_supported,
     num_configs,

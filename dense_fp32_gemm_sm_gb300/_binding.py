@@ -60,6 +60,7 @@ def library() -> ctypes.CDLL:
                                     _c_vp, _c_int, _c_ll, _c_int, _c_vp, _c_int, _c_vp],
                 "fgemm_device_status": [_c_int],
                 "fgemm_select_config": [_c_int] * 8,
+                "fgemm_launch_count": [_c_int] * 9,
                 "fgemm_num_configs": [],
                 "fgemm_config_name": [_c_int],
                 "fgemm_status_string": [_c_int],
@@ -137,6 +138,12 @@ def config_name(config: int):
 def select_config(transa, transb, M, N, K, batch, aligned, num_sms) -> int:
     return library().fgemm_select_config(int(transa), int(transb), M, N, K, batch,
                                          1 if aligned else 0, num_sms)
+
+
+def launch_count(config, transa, transb, M, N, K, batch, aligned, num_sms) -> int:
+    """``fgemm_launch_count``: kernel launches of one call (config < 0: as selected)."""
+    return library().fgemm_launch_count(int(config), int(transa), int(transb), M, N, K, batch,
+                                        1 if aligned else 0, num_sms)
 
 
 def sgemm(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, stream=None,

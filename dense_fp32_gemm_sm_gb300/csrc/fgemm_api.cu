@@ -432,6 +432,29 @@ const char *fgemm_config_name(int config)
     return fgemm::kConfigs[config].name;
 }
 
+int fgemm_launch_count(int config, fgemm_op transa, fgemm_op transb, int M, int N, int K,
+                       int batch, int aligned, int num_sms)
+{
+    if ((transa != FGEMM_OP_N && transa != FGEMM_OP_T) ||
+        (transb != FGEMM_OP_N && transb != FGEMM_OP_T) || M < 0 || N < 0 || K < 0 || batch < 0 ||
+        config >= fgemm::NUM_CONFIGS || num_sms < 1)
+        return -1;
+    if (M == 0 || N == 0 || batch == 0) return 0;
+    if (config < 0)
+        config = fgemm::select_config((int)transa, (int)transb, M, N, K, batch, aligned != 0,
+                                      num_sms);
+    if (config == fgemm::CFG_128x128_SPLIT || config == fgemm::CFG_128x128_KSPLIT ||
+        config == fgemm::CFG_128x128_KCHAIN) {
+        const long long total = (long long)((M + 127) / 128) * ((N + 127) / 128) * batch;
+        const long long r = total % num_sms;
+        const int tail = config == fgemm::CFG_128x128_KCHAIN
+                             ? fgemm::kchain_slices((int)transa, (int)transb, r, K, num_sms)
+                             : 1;
+        return (total - r > 0 ? 1 : 0) + (r > 0 ? tail : 0);
+    }
+    return (batch + 65534) / 65535;
+}
+
 int fgemm_select_config(fgemm_op transa, fgemm_op transb, int M, int N, int K, int batch,
                         int aligned, int num_sms)
 {

@@ -43,6 +43,11 @@ extern const ConfigInfo kConfigs[NUM_CONFIGS];
 // SM count of the current device (cached per device).  Returns 0 on success.
 int device_sm_count(int *out);
 
+// Number of k-slices (2..8) the k-chain configuration cuts the last r tiles into in the
+// given transpose layout: the count with the shortest modelled time (S r whole-tile CTAs
+// over K / S, plus the chaining of S launches), the smaller count on a tie.
+int kchain_slices(int ta, int tb, long long r, long long K, int num_sms);
+
 // The configuration for a problem (host-only; see fgemm_select_config).
 int select_config(int ta, int tb, long long M, long long N, long long K, long long batch,
                   bool aligned, int num_sms);

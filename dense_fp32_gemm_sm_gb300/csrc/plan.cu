@@ -84,19 +84,25 @@ double tiles_of(long long M, long long N, long long bm, long long bn, long long 
     return (double)ceil_div(M, bm) * (double)ceil_div(N, bn) * (double)batch;
 }
 
-double model_us(const LaunchModel &m, double ctas, long long K, int num_sms)
+double model_us(const LaunchModel &m, double ctas, double K, int num_sms)
 {
-    return model_n_us(m, std::ceil(ctas / (double)num_sms), (double)K);
+    return model_n_us(m, std::ceil(ctas / (double)num_sms), K);
 }
 
 // Clusters of four k-slice CTAs that run at once with one CTA per SM.  Measured on
 // 152 SMs: 74 clusters of four are resident at two CTAs per SM (296 CTAs, not 304:
 // a cluster stays inside one GPC), and the k-split tail of r tiles takes
 // ceil(r / 37) rounds of a quarter of a whole-tile period.
-// Fixed cost of the k-chain's four programmatically dependent launches (their
-// ordered additions into C), and the time a last-wave launch saves by starting on the
-// SMs the whole tiles leave; measured on GB300.
-constexpr double kKchainUs = 8.0;
+// The k-chain's cost over the whole-tile model of its S r CTAs at K / S: each of its S
+// programmatically dependent launches waits for the one before it to finish before its
+// ordered addition into C (8 us a launch), and the model's one launch constant overstates
+// a tail whose launches start early (16 us less).  Both fitted to CUDA-event times of
+// every slice count 2..8 on 16 shapes on 152 SMs (4096^3, 3072^3, 2048^3, 1024^3, FC,
+// PV, TN 3072^2 x 2048, ragged 1700 x 1652, ...): the choice they make is within 0.7 %
+// of the fastest slice count and tail on every one.  kTailOverlapUs is the time a
+// last-wave launch saves by starting on the SMs the whole tiles leave.
+constexpr double kKchainUsPerSlice = 8.0;
+constexpr double kKchainCreditUs = 16.0;
 constexpr double kTailOverlapUs = 35.0;
 
 long long ksplit_clusters_per_round(int num_sms)
@@ -106,6 +112,24 @@ long long ksplit_clusters_per_round(int num_sms)
 }
 
 }  // namespace
+
+int kchain_slices(int ta, int tb, long long r, long long K, int num_sms)
+{
+    if (num_sms < 1) num_sms = 1;
+    const LaunchModel &m = kModel[(ta ? 2 : 0) + (tb ? 1 : 0)][M_128x128];
+    const double k = K > 0 ? (double)K : 0.0;
+    const double ctas = r > 0 ? (double)r : 0.0;
+    int best = 2;
+    double best_us = 0.0;
+    for (int S = 2; S <= 8; ++S) {
+        const double us = model_us(m, S * ctas, k / S, num_sms) + kKchainUsPerSlice * S;
+        if (S == 2 || us < best_us) {
+            best_us = us;
+            best = S;
+        }
+    }
+    return best;
+}
 
 int select_config(int ta, int tb, long long M, long long N, long long K, long long batch,
                   bool aligned, int num_sms)
@@ -137,13 +161,13 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
     const double rounds = (double)ceil_div(r, ksplit_clusters_per_round(num_sms));
     const double ksplit = main_us - overlap +
                           (r > 0 ? model_n_us(mm[M_128x128], rounds, (double)k / 4.0) : 0.0);
-    // k-chain tiles: 4r whole-tile CTAs over K / 4 each, spread over the SMs without
-    // cluster placement, plus the cost of chaining four launches (measured with no
-    // whole tiles before them: 1024^3, 1280^2 x 4096, 1536^2 x 4096 3-11 us above the
-    // model's 4r CTAs at K / 4).
+    // k-chain tiles: S r whole-tile CTAs over K / S each (S from kchain_slices), spread
+    // over the SMs without cluster placement, plus the cost of chaining S launches
+    const int slices = kchain_slices(ta, tb, r, k, num_sms);
     const double kchain = main_us - overlap +
-                          (r > 0 ? model_us(mm[M_128x128], 4.0 * (double)r, (double)k / 4.0,
-                                            num_sms) + kKchainUs
+                          (r > 0 ? model_us(mm[M_128x128], (double)slices * (double)r,
+                                            (double)k / slices, num_sms) +
+                                       kKchainUsPerSlice * slices - kKchainCreditUs
                                  : 0.0);
     struct Option {
         int config;

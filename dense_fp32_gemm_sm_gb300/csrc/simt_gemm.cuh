@@ -53,9 +53,10 @@
 //    (no workspace, no atomics, the same result on every run).
 //
 //  * Last-wave k-chain (TILE_KCHAIN launches): the last r tiles stay whole, each in
-//    four k-slices, one launch per slice; each launch adds its slice's products into
-//    C in slice order, the later ones as programmatic dependent launches that run
-//    alongside the earlier ones and wait for them only before adding into C.
+//    two to eight k-slices (as many as the launch-time model finds fastest), one
+//    launch per slice; each launch adds its slice's products into C in slice order,
+//    the later ones as programmatic dependent launches that run alongside the earlier
+//    ones and wait for them only before adding into C.
 //
 //  * The copy of a later stage is issued at k-step COPY_K of the current stage.
 #pragma once

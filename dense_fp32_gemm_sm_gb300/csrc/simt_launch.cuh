@@ -251,13 +251,13 @@ static fgemm_status launch_simt_ksplit(const GemmParams &p0, int batch, cudaStre
 }
 
 // Last-wave k-chain: the first (tiles - r) tiles whole, then the last r = tiles mod SMs
-// tiles in KCHAIN_SLICES k-slices, one launch per slice (TILE_KCHAIN).  Every slice's
-// launch is a programmatic dependent of the launch before it (it may start while that
-// one runs and waits for it only before writing C), so the slices' products run side
-// by side over r * KCHAIN_SLICES CTAs and on SMs the whole tiles have left; the
-// additions into C happen in slice order.  The first launch of the call is never a
-// dependent: it follows the stream's earlier work, which may have written A or B.
-constexpr int KCHAIN_SLICES = 4;
+// tiles in S k-slices (S = kchain_slices, from the launch-time model: 4 for the 112
+// tiles of 4096^3), one launch per slice (TILE_KCHAIN).  Every slice's launch is a
+// programmatic dependent of the launch before it (it may start while that one runs and
+// waits for it only before writing C), so the slices' products run side by side over
+// r * S CTAs and on SMs the whole tiles have left; the additions into C happen in slice
+// order.  The first launch of the call is never a dependent: it follows the stream's
+// earlier work, which may have written A or B.
 
 template <class Main>
 static fgemm_status launch_simt_kchain(const GemmParams &p0, int batch, cudaStream_t stream)
@@ -272,9 +272,15 @@ static fgemm_status launch_simt_kchain(const GemmParams &p0, int batch, cudaStre
         (void)cudaGetLastError();
         return FGEMM_ERR_LAUNCH;
     }
+    int sms = 0;
+    if (device_sm_count(&sms) != 0) {
+        (void)cudaGetLastError();
+        return FGEMM_ERR_LAUNCH;
+    }
+    const int slices = kchain_slices(Main::TA, Main::TB, rem, p.K, sms);
     st = launch_whole_tiles<Main>(p, batch, stream);
     if (st != FGEMM_OK) return st;
-    for (int s = 0; rem > 0 && s < KCHAIN_SLICES; ++s) {
+    for (int s = 0; rem > 0 && s < slices; ++s) {
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -288,7 +294,7 @@ static fgemm_status launch_simt_kchain(const GemmParams &p0, int batch, cudaStre
         // dependents at once); with no whole tiles it is the call's first launch and
         // follows the stream's earlier work in plain stream order.
         cfg.numAttrs = (s > 0 || p.full_units > 0) ? 1 : 0;
-        const int chain = s | (KCHAIN_SLICES << 8);
+        const int chain = s | (slices << 8);
         if (cudaLaunchKernelEx(&cfg, simt_gemm_kernel<Main, TILE_KCHAIN>, p, chain) != cudaSuccess) {
             (void)cudaGetLastError();
             return FGEMM_ERR_LAUNCH;

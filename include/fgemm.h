@@ -251,11 +251,11 @@ const char *fgemm_status_string(fgemm_status status);
  * quarter tiles ("..._split", one more launch), as thread-block clusters of four CTAs
  * that each multiply one k-slice of a tile and add their partial sums through
  * distributed shared memory in a fixed order ("..._ksplit", one more launch), or as
- * four k-slices of every tile, one launch per slice, each adding its products into C
- * in slice order ("..._kchain", four more launches; slices 1-3 are programmatic
- * dependent launches that start while the previous slice runs and wait for it only
- * before their additions).  All allocate nothing and give the same result on every
- * run.
+ * two to eight k-slices of every tile, one launch per slice, each adding its products
+ * into C in slice order ("..._kchain"; fgemm_launch_count gives the number).  Every
+ * last-wave launch is a programmatic dependent of the launch before it: it may start
+ * while that one runs and waits for it only before writing C.  All allocate nothing and
+ * give the same result on every run.
  * ------------------------------------------------------------------------- */
 
 /* Number of kernel configurations; valid ids are 0 .. fgemm_num_configs()-1. */
@@ -273,6 +273,18 @@ const char *fgemm_config_name(int config);
  */
 int fgemm_select_config(fgemm_op transa, fgemm_op transb, int M, int N, int K, int batch,
                         int aligned, int num_sms);
+
+/*
+ * Kernel launches one call with this configuration (config < 0: the one the plain entry
+ * points would select) makes on a GPU with `num_sms` SMs: 1 for most configurations (1
+ * per 65535 problems of a batch), and for the last-wave configurations one for the
+ * whole tiles (if any) plus one for the last (tiles mod SMs) tiles -- or, for
+ * "..._kchain", one per k-slice (2 to 8, chosen from the remainder and K).  K is the
+ * depth the kernels see: 0 when alpha == 0.  0 for an empty problem, -1 for arguments
+ * the entry points would reject.  Host-only: no CUDA call is made.
+ */
+int fgemm_launch_count(int config, fgemm_op transa, fgemm_op transb, int M, int N, int K,
+                       int batch, int aligned, int num_sms);
 
 /*
  * The most general call, with an explicit configuration (config < 0 means

@@ -117,12 +117,14 @@ def test_selector():
     assert name(0, 0, 4096, 4864, 4096, 1, 1, 152) == "simt_128x128_t8x8"  # 8 x 152 tiles
     assert name(0, 0, 4096, 3648, 4096, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # r = 16
     assert name(0, 0, 8192, 11008, 4096, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # r = 32
-    # (last-wave launches start on the SMs the whole tiles leave: 3072^3 measured
-    # 928 us with the cluster k-split against 936 us with whole tiles only)
-    assert name(0, 0, 3072, 3072, 3072, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # r = 120
+    # the k-chain in as many slices as the model finds fastest (3072^3 measured 898 us
+    # in five slices against 929 us as cluster k-split; 1792^2 x 1024 128 against 144 us
+    # in three; 1280^2 x 4096, no whole tiles, 233 against 249 us in three)
+    assert name(0, 0, 3072, 3072, 3072, 1, 1, 152) == "simt_128x128_t8x8_kchain"  # r = 120
     assert name(0, 0, 2048, 2048, 2048, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # r = 104
-    assert name(0, 0, 1792, 1792, 1024, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # r = 44
-    assert name(0, 0, 1280, 1280, 4096, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # all split
+    assert name(0, 0, 1792, 1792, 1024, 1, 1, 152) == "simt_128x128_t8x8_kchain"  # r = 44
+    assert name(0, 0, 1280, 1280, 4096, 1, 1, 152) == "simt_128x128_t8x8_kchain"  # 100 tiles
+    assert name(0, 0, 1700, 1652, 4096, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # r = 30
     assert name(0, 0, 768, 768, 768, 1, 1, 152) == "simt_128x128_t8x8_ksplit"  # 36 tiles
     assert name(0, 0, 768, 768, 128, 1, 1, 152) == "simt_64x64x16_t4x4_s4"
     assert name(0, 0, 640, 640, 256, 1, 1, 152) == "simt_32x32x16_t4x4_s4"

@@ -27,20 +27,32 @@ def test_bench_reads_only_bound_names():
     assert not sorted(loads - bound)
 
 
-def test_call_launches():
+def test_launch_count():
+    # the library's own count of the kernel launches of one call (bench.py reports it)
     import sys
     sys.path.insert(0, ROOT)
-    import bench
-    # whole tiles only, two launches, or only the split tiles
-    assert bench.call_launches("simt_128x128_t8x8", 4096, 4096, 1, 152) == 1
-    assert bench.call_launches("simt_128x128_t8x8_split", 4096, 4096, 1, 152) == 2  # 912 + 112
-    assert bench.call_launches("simt_128x128_t8x8_ksplit", 4096, 4864, 1, 152) == 1  # 8 x 152
-    assert bench.call_launches("simt_128x128_t8x8_ksplit", 1024, 1024, 1, 152) == 1  # 64 < 152
-    assert bench.call_launches("simt_128x128_t8x8_ksplit", 2048, 128, 128, 152) == 2
-    # the k-chain: whole tiles, then one launch per k-slice of the last wave
-    assert bench.call_launches("simt_128x128_t8x8_kchain", 4096, 4096, 1, 152) == 1 + 4
-    assert bench.call_launches("simt_128x128_t8x8_kchain", 4096, 4864, 1, 152) == 1
-    assert bench.call_launches("simt_128x128_t8x8_kchain", 1024, 1024, 1, 152) == 4
+    import dense_fp32_gemm_sm_gb300 as fg
+    cfg = {fg.config_name(i): i for i in range(fg.num_configs())}
+    lc = fg.launch_count
+    assert lc(cfg["simt_128x128_t8x8"], 0, 0, 4096, 4096, 4096, 1, True, 152) == 1
+    assert lc(cfg["simt_128x128_t8x8_split"], 0, 0, 4096, 4096, 4096, 1, True, 152) == 2
+    assert lc(cfg["simt_128x128_t8x8_ksplit"], 0, 0, 4096, 4864, 4096, 1, True, 152) == 1
+    assert lc(cfg["simt_128x128_t8x8_ksplit"], 0, 0, 1024, 1024, 1024, 1, True, 152) == 1
+    assert lc(cfg["simt_128x128_t8x8_ksplit"], 0, 0, 2048, 128, 2048, 128, True, 152) == 2
+    # the k-chain: whole tiles, then one launch per k-slice of the last wave: four for
+    # the 112 tiles of 4096^3, three for 44 tiles at K = 1024, five for 120 at 3072, seven
+    # for 16 at 4096; two for the 136 tiles 148 SMs leave at 4096^3
+    assert lc(cfg["simt_128x128_t8x8_kchain"], 0, 0, 4096, 4096, 4096, 1, True, 152) == 1 + 4
+    assert lc(cfg["simt_128x128_t8x8_kchain"], 0, 0, 1792, 1792, 1024, 1, True, 152) == 1 + 3
+    assert lc(cfg["simt_128x128_t8x8_kchain"], 0, 0, 3072, 3072, 3072, 1, True, 152) == 1 + 5
+    assert lc(cfg["simt_128x128_t8x8_kchain"], 0, 0, 4096, 3648, 4096, 1, True, 152) == 1 + 7
+    assert lc(cfg["simt_128x128_t8x8_kchain"], 0, 0, 4096, 4096, 4096, 1, True, 148) == 1 + 2
+    assert lc(cfg["simt_128x128_t8x8_kchain"], 0, 0, 4096, 4864, 4096, 1, True, 152) == 1
     # the per-problem grid splits a batch into chunks of 65535 problems
-    assert bench.call_launches("simt_32x32x16_t4x4_s4", 64, 64, 65535, 152) == 1
-    assert bench.call_launches("simt_32x32x16_t4x4_s4", 64, 64, 65536, 152) == 2
+    assert lc(cfg["simt_32x32x16_t4x4_s4"], 0, 0, 64, 64, 64, 65535, True, 152) == 1
+    assert lc(cfg["simt_32x32x16_t4x4_s4"], 0, 0, 64, 64, 64, 65536, True, 152) == 2
+    # selection, empty problems and bad arguments
+    assert lc(-1, 0, 0, 4096, 4096, 4096, 1, True, 152) == 5
+    assert lc(-1, 0, 0, 0, 4096, 4096, 1, True, 152) == 0
+    assert lc(-1, 0, 0, -1, 4096, 4096, 1, True, 152) == -1
+    assert lc(fg.num_configs(), 0, 0, 8, 8, 8, 1, True, 152) == -1

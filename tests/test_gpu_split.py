@@ -4,8 +4,9 @@ All compute the first (tiles - r) 128 x 128 tiles whole and then the last
 r = tiles mod SMs another way: simt_128x128_t8x8_split as 64 x 64 quarter tiles
 with four k-groups, simt_128x128_t8x8_ksplit as clusters of four CTAs that each
 multiply one k-slice of a whole tile and add the partial sums through distributed
-shared memory, simt_128x128_t8x8_kchain as four chained launches, one k-slice of
-every tile each, that add their products into C in slice order.  These cases put whole and split tiles in one call, with split
+shared memory, simt_128x128_t8x8_kchain as S chained launches (S from 2 to 8, by the
+launch-time model), one k-slice of every tile each, that add their products into C in
+slice order.  These cases put whole and split tiles in one call, with split
 tiles on the ragged bottom and right edges (quarters wholly outside the matrix are
 skipped), on the last problem of a strided batch, with k-slices that are short or
 empty, and in all four transpose layouts; integer data must come back bit-exact,
@@ -106,6 +107,33 @@ def test_kchain_beta_zero_never_reads_c(ta, tb):
                ints=False, config=_config("simt_128x128_t8x8_kchain"), seed=75 + 2 * ta + tb))
 
 
+@pytest.mark.parametrize("slices", range(2, 9))
+def test_kchain_every_slice_count(slices):
+    # The k-chain cuts the last wave into 2 to 8 k-slices, as many as the launch-time
+    # model finds fastest for the wave's size and K; fgemm_launch_count reports the
+    # choice (one whole-tile launch, then one launch per slice).  The smallest ragged
+    # shape with whole tiles that takes this many slices, in one of the four layouts.
+    sms = _sms()
+    cfg = _config("simt_128x128_t8x8_kchain")
+    ta, tb = COMBOS[slices % 4]
+    best = None
+    for K in (96, 256, 512, 1024, 1536, 2048, 3072, 4096, 6144, 8192):
+        for mt in range(10, 21):
+            for nt in range(10, 21):
+                M, N = 128 * mt - 37, 128 * nt - 5
+                if mt * nt > sms and fg.launch_count(cfg, ta, tb, M, N, K, 1, True,
+                                                     sms) == 1 + slices:
+                    if best is None or M * N * K < best[0]:
+                        best = (M * N * K, M, N, K)
+    if best is None:
+        assert sms != 152, "no shape takes %d slices on 152 SMs" % slices
+        pytest.skip("no shape in the search takes %d slices on %d SMs" % (slices, sms))
+    _, M, N, K = best
+    check(Case(ta=ta, tb=tb, M=M, N=N, K=K, alpha=1.5, beta=-0.5, bias=True,
+               relu=slices % 2 == 0, ints=slices % 2 == 1, config=cfg, pad=(4, 8, 4),
+               seed=80 + slices))
+
+
 @pytest.mark.parametrize("split", SPLITS)
 def test_no_remainder_runs_whole_tiles_only(split):
     sms = _sms()
@@ -124,4 +152,4 @@ def test_selector_on_this_gpu():
     assert name(0, 0, 8192, 11008, 4096, 1) == "simt_128x128_t8x8_ksplit"
     assert name(0, 0, 2048, 128, 2048, 128) == "simt_128x128_t8x8_ksplit"
     assert name(0, 1, 2048, 2048, 128, 128) == "simt_128x128_t8x8"
-    assert name(0, 0, 3072, 3072, 3072, 1) == "simt_128x128_t8x8_ksplit"
+    assert name(0, 0, 3072, 3072, 3072, 1) == "simt_128x128_t8x8_kchain"
