@@ -4,7 +4,10 @@
 A step is one call of the library on the workload's synthetic inputs, already
 resident in HBM (default workload: M = N = K = 4096, alpha = 1, beta = 0,
 row-major, A and B uniform[-1, 1) from seed 2).  The L2 is flushed between
-timed steps by a 256 MiB memset outside the step's event pair.
+timed steps by a 256 MiB memset outside the step's event pair.  The call is
+fgemm_sgemm_staged with the launch-time model's staging choice and a workspace
+allocated once beforehand (``--entry plain``: the plain entry points, no workspace);
+its copies of the operands stored with k contiguous are part of every timed step.
 
 Reported, besides the contract keys:
   roofline      the GEMM kernel against the CUDA-core FP32 peak
@@ -66,6 +69,10 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("fgemm", "reference"), default="fgemm")
     ap.add_argument("--workload", choices=workloads.WORKLOADS, default="square4096")
+    ap.add_argument("--entry", choices=("staged", "plain"), default="staged",
+                    help="FP32 calls through fgemm_sgemm_staged (the model decides whether to "
+                         "copy k-contiguous operands k-major into a workspace first) or the "
+                         "plain entry points")
     ap.add_argument("--config", type=int, default=-1,
                     help="explicit kernel configuration id (default: the library's choice)")
     ap.add_argument("--e2e-steps", type=int, default=50,
@@ -96,6 +103,7 @@ def parse_args(argv=None):
 KERNEL_SOURCES = {
     "simt": ("simt_gemm.cuh", "simt_launch.cuh", "inst_nn.cu", "inst_nt.cu", "inst_tn.cu",
              "inst_tt.cu"),
+    "stage": ("stage.cu",),
     "tcgen05": ("tc_gemm.cuh", "tc_gemm.cu"),
 }
 
@@ -109,10 +117,11 @@ def _code_only(text: str) -> str:
 
 
 def kernel_source_hash(family: str) -> str:
-    """Short hash of one kernel family's CUDA code (comments and layout ignored);
-    profile summaries record the hash of the code they measured."""
+    """Short hash of one kernel family's CUDA code (comments and layout ignored), or of
+    several joined by '+' (a staged call: "simt+stage"); profile summaries record the
+    hash of the code they measured."""
     m = hashlib.sha256()
-    for name in KERNEL_SOURCES[family]:
+    for name in [n for f in family.split("+") for n in KERNEL_SOURCES[f]]:
         m.update(name.encode())
         with open(os.path.join(ROOT, "dense_fp32_gemm_sm_gb300", "csrc", name), encoding="utf-8") as fh:
             m.update(_code_only(fh.read()).encode())
@@ -147,6 +156,8 @@ def recorded_traffic(config_name: str, workload: str):
     family = config_name.split("_")[0]
     if family not in KERNEL_SOURCES:
         return None
+    if "_staged_" in config_name:
+        family += "+stage"
     if (fields.get("source_sha256") != kernel_source_hash(family)
             or "traffic_bytes_per_launch" not in fields):
         return None
@@ -352,24 +363,36 @@ def small_secondary(fg, dev, stream, graph_calls: int = 200, calls: int = 20):
     return out
 
 
-def fc_secondary(fg, dev, stream, calls: int = 3, clocks: bool = True):
+def fc_secondary(fg, dev, stream, calls: int = 3, clocks: bool = True, entry: str = "staged"):
     """The fully-connected layer (X 8192 x 4096, W 4096 x 11008, bias, ReLU) fused in the
     GEMM epilogue against the plain GEMM of the same shape: `calls` timed calls each
     (one warm-up call, L2 flushed before every call, CUDA events on the stream), and
-    the fused/unfused throughput ratio."""
+    the fused/unfused throughput ratio.  Both through the same entry point as the
+    headline (`entry`)."""
     w = workloads.make("fc8192x4096x11008")
     dA, dB, dbias = w.A.to(dev), w.B.to(dev), w.bias.to(dev)
     dC = torch.empty((w.M, w.N), device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     sh = stream.cuda_stream
+    ws, need = staged_workspace(fg, w, dev) if entry == "staged" else (None, 0)
+
+    def call(bias, relu):
+        if entry == "staged":
+            fg.sgemm_staged(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, 0, dB, w.ldb, 0,
+                            w.beta, dC, w.ldc, 0, 1, bias, relu, fg.STAGE_AUTO, ws, need,
+                            stream=sh)
+        elif bias is not None or relu:
+            fg.sgemm_bias_relu(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, dB, w.ldb, w.beta,
+                               dC, w.ldc, bias, relu, stream=sh)
+        else:
+            fg.sgemm(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, dB, w.ldb, w.beta, dC, w.ldc,
+                     stream=sh)
 
     def fused():
-        fg.sgemm_bias_relu(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, dB, w.ldb, w.beta, dC,
-                           w.ldc, dbias, True, stream=sh)
+        call(dbias, True)
 
     def plain():
-        fg.sgemm(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, dB, w.ldb, w.beta, dC, w.ldc,
-                 stream=sh)
+        call(None, False)
 
     out = {}
     sampler = ClockSampler(dev.index or 0, enabled=clocks)
@@ -387,9 +410,9 @@ def fc_secondary(fg, dev, stream, calls: int = 3, clocks: bool = True):
                 times.append(e0.elapsed_time(e1) / 1e3)
             t = statistics.median(times)
             out[name] = {"tflops": round(w.flops / t / 1e12, 3), "ms": round(t * 1e3, 4)}
-    del dA, dB, dbias, dC, flush
+    del dA, dB, dbias, dC, flush, ws
     torch.cuda.empty_cache()
-    res = {"workload": describe(w), "calls_each": calls,
+    res = {"workload": describe(w), "calls_each": calls, "entry": entry,
            "l2": "flushed before every call",
            "fused_over_unfused": round(out["fused_bias_relu"]["tflops"] /
                                        out["plain_gemm"]["tflops"], 4), **out}
@@ -407,13 +430,18 @@ def stated_peak_tflops(device) -> tuple:
 MATHS = {"fp32": 0, "tf32": 1, "3xtf32": 2}
 
 
-def _launch(fg, w, cfg, dA, dB, dC, dbias, stream, math="fp32", splitk=None):
-    """One step: the library call of the workload (the bench's unit of work)."""
+def _launch(fg, w, cfg, dA, dB, dC, dbias, stream, math="fp32", splitk=None, staged=None):
+    """One step: the library call of the workload (the bench's unit of work).
+    staged: (workspace, bytes) to call fgemm_sgemm_staged with the model's choice."""
     nb = max(1, w.batch)
     sA = w.M * w.K if w.batch else 0
     sB = w.N * w.K if w.batch else 0
     sC = w.M * w.N if w.batch else 0
-    if splitk is not None:
+    if staged is not None and splitk is None and math == "fp32" and cfg < 0:
+        ws, need = staged
+        fg.sgemm_staged(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, sA, dB, w.ldb, sB, w.beta,
+                        dC, w.ldc, sC, nb, dbias, w.relu, fg.STAGE_AUTO, ws, need, stream=stream)
+    elif splitk is not None:
         splits, ws, need = splitk
         fg.sgemm_splitk(w.ta, w.tb, w.M, w.N, w.K, w.alpha, dA, w.lda, dB, w.ldb, w.beta, dC,
                         w.ldc, dbias, w.relu, splits, ws, need, stream=stream)
@@ -485,12 +513,13 @@ def run_fgemm(args, rank, world, local_rank):
             raise SystemExit("bench.py: --splitk takes single problems")
         need = fg.splitk_workspace_size(w.M, w.N, w.K, args.splitk)
         splitk = (args.splitk, torch.empty(need // 4, device=dev), need)
+    staged = staged_workspace(fg, w, dev) if args.entry == "staged" else None
     torch.cuda.synchronize()
 
     def step():
         if dC0 is not None:  # beta != 0: restore C so every step computes the same thing
             dC.copy_(dC0)
-        _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math, splitk)
+        _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math, splitk, staged)
 
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
@@ -509,7 +538,7 @@ def run_fgemm(args, rank, world, local_rank):
             if dC0 is not None:
                 dC.copy_(dC0)
             starts[i].record(stream)
-            _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math, splitk)
+            _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math, splitk, staged)
             ends[i].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
@@ -556,7 +585,7 @@ def run_fgemm(args, rank, world, local_rank):
         ev_in[b].record(h2d_s)
         stream.wait_event(ev_in[b])
         with torch.cuda.stream(stream):
-            _launch(fg, w, args.config, xA, xB, xC, dbias, sh, args.math, splitk)
+            _launch(fg, w, args.config, xA, xB, xC, dbias, sh, args.math, splitk, staged)
         ev_done[b].record(stream)
         d2h_s.wait_event(ev_done[b])
         with torch.cuda.stream(d2h_s):
@@ -579,7 +608,7 @@ def run_fgemm(args, rank, world, local_rank):
         torch.cuda.synchronize()
         with torch.cuda.graph(graph, stream=stream):
             for _ in range(args.graph_calls):
-                _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math, splitk)
+                _launch(fg, w, args.config, dA, dB, dC, dbias, sh, args.math, splitk, staged)
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         with torch.cuda.stream(stream):  # replay() launches on the current stream
             graph.replay()
@@ -593,16 +622,29 @@ def run_fgemm(args, rank, world, local_rank):
                         "value": round(w.flops / per_call / 1e12, 4), "unit": UNIT,
                         "l2": "warm (calls back to back in one CUDA graph)"}
 
-    def launches(config, M, N, K, batch):
+    def launches(config, M, N, K, batch, ta=w.ta, tb=w.tb):
         """Kernel launches of one library call with this configuration (None: select),
         as the library counts them (fgemm_launch_count)."""
         if config is None or config < 0:
-            config = fg.select_config(w.ta, w.tb, M, N, K, batch, True, sms)
+            config = fg.select_config(ta, tb, M, N, K, batch, True, sms)
         name = fg.config_name(config)
         kk = K if w.alpha != 0 else 0
-        return name, fg.launch_count(config, w.ta, w.tb, M, N, kk, batch, True, sms)
+        return name, fg.launch_count(config, ta, tb, M, N, kk, batch, True, sms)
 
-    kernel_name, n_batch_launches = launches(args.config, w.M, w.N, w.K, max(1, w.batch))
+    stage_mask = 0
+    if staged is not None and args.config < 0 and splitk is None and args.math == "fp32":
+        stage_mask = fg.staged_choice(w.ta, w.tb, w.M, w.N, w.K, max(1, w.batch), False, False,
+                                      True, True, sms)
+    if stage_mask:
+        # the copies (one launch per staged operand and 65535 problems), then the GEMM
+        # in the layout they leave
+        nb = max(1, w.batch)
+        kernel_name, n_batch_launches = launches(
+            None, w.M, w.N, w.K, nb, 1 if stage_mask & 1 else w.ta, 0 if stage_mask & 2 else w.tb)
+        n_batch_launches += bin(stage_mask).count("1") * (-(-nb // 65535))
+        kernel_name += {1: "_staged_a", 2: "_staged_b", 3: "_staged_ab"}[stage_mask]
+    else:
+        kernel_name, n_batch_launches = launches(args.config, w.M, w.N, w.K, max(1, w.batch))
     if splitk is not None:
         # partial GEMMs: the slices of equal depth as one strided batch, the shorter last
         # slice as a second call; then the reduction kernel
@@ -638,6 +680,7 @@ def run_fgemm(args, rank, world, local_rank):
                   "3xtf32": "3xtf32 (tf32 hi/lo split, fp32 accumulate)"}[args.math]
         if tensor_path else "f32", "data": "synthetic",
         "config": {"workload": describe(w), "kernel_config": kernel_name,
+                   "entry": entry_text(args, staged, stage_mask),
                    "l2": "flushed between steps (256 MiB memset outside the timed event pair)",
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "gpu_launches": args.steps * n_batch_launches,
@@ -653,13 +696,21 @@ def run_fgemm(args, rank, world, local_rank):
                     "max": round(max(step_ms), 5)},
         "build": build_info(),
     }
-    if kernel_name.endswith(("_split", "_ksplit", "_kchain")) and not tensor_path:
+    gemm_name = re.sub(r"_staged_(a|b|ab)$", "", kernel_name)
+    copies = bin(stage_mask).count("1") * (-(-max(1, w.batch) // 65535))
+    if gemm_name.endswith(("_split", "_ksplit", "_kchain")) and not tensor_path:
         line["roofline"]["kernels"] = (
-            "launches of simt_gemm_kernel (whole tiles, then the last wave's tiles as %s), "
+            "%slaunches of simt_gemm_kernel (whole tiles, then the last wave's tiles as %s), "
             "timed together as one call" % (
-                "k-slice clusters" if kernel_name.endswith("_ksplit")
-                else "%d chained k-slice launches" % (n_batch_launches - 1)
-                if kernel_name.endswith("_kchain") else "quarter tiles"))
+                "the k-major copy of %s (stage_transpose_kernel), then " % (
+                    {1: "A", 2: "B", 3: "A and B"}[stage_mask]) if stage_mask else "",
+                "k-slice clusters" if gemm_name.endswith("_ksplit")
+                else "%d chained k-slice launches" % (n_batch_launches - copies - 1)
+                if gemm_name.endswith("_kchain") else "quarter tiles"))
+    elif stage_mask and not tensor_path:
+        line["roofline"]["kernels"] = (
+            "the k-major copy of %s (stage_transpose_kernel), then simt_gemm_kernel, timed "
+            "together as one call" % {1: "A", 2: "B", 3: "A and B"}[stage_mask])
     # Algorithmic HBM bytes per step (A and B read, C written, C read when beta != 0,
     # the bias) over the step time: the bandwidth side of the roofline, which matters
     # for the skinny shapes (the QK^T batch writes 2 GiB).
@@ -696,10 +747,32 @@ def run_fgemm(args, rank, world, local_rank):
             and not tensor_path and args.config < 0 and splitk is None):
         # the fused-epilogue target: FC layer fused against the plain GEMM of its shape
         line["secondary"] = {"fc_fused_vs_unfused": fc_secondary(
-            fg, dev, stream, clocks=not args.no_clocks), **small_secondary(fg, dev, stream)}
+            fg, dev, stream, clocks=not args.no_clocks, entry=args.entry),
+            **small_secondary(fg, dev, stream)}
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     return line
+
+
+def staged_workspace(fg, w, dev):
+    """(workspace tensor, bytes) for fgemm_sgemm_staged on this workload, allocated once."""
+    need = fg.staged_workspace_size(w.ta, w.tb, w.M, w.N, w.K, max(1, w.batch))
+    return torch.empty(max(1, need // 4), dtype=torch.float32, device=dev), need
+
+
+def entry_text(args, staged, stage_mask):
+    if args.math != "fp32":
+        return "fgemm_gemm_math"
+    if args.splitk > 1:
+        return "fgemm_sgemm_splitk"
+    if args.config >= 0:
+        return "fgemm_gemm_explicit"
+    if staged is None:
+        return "plain (fgemm_sgemm / _bias_relu / _strided_batched)"
+    what = {0: "no copy (the model keeps the operands as stored)", 1: "A copied k-major",
+            2: "B copied k-major", 3: "A and B copied k-major"}[stage_mask]
+    return "fgemm_sgemm_staged, the model's choice: %s; workspace %.0f MiB allocated once" % (
+        what, staged[1] / 2**20)
 
 
 def describe(w):

@@ -31,8 +31,12 @@ from ._binding import (  # noqa: F401
     sgemm_bias_relu,
     sgemm_row_bias_relu,
     NOALLOC_SCRATCH_BYTES,
+    STAGE_AUTO,
     sgemm_splitk,
     sgemm_splitk_noalloc,
+    sgemm_staged,
+    staged_choice,
+    staged_workspace_size,
     splitk_workspace_size,
     sgemm_strided_batched,
     status_string,

@@ -81,6 +81,15 @@ def library() -> ctypes.CDLL:
             lib.fgemm_sgemm_splitk_noalloc.restype = _c_int
             lib.fgemm_splitk_workspace_size.argtypes = [_c_int, _c_int, _c_int, _c_int]
             lib.fgemm_splitk_workspace_size.restype = ctypes.c_size_t
+            lib.fgemm_staged_workspace_size.argtypes = [_c_int] * 6
+            lib.fgemm_staged_workspace_size.restype = ctypes.c_size_t
+            lib.fgemm_staged_choice.argtypes = [_c_int] * 11
+            lib.fgemm_staged_choice.restype = _c_int
+            lib.fgemm_sgemm_staged.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
+                                               _c_vp, _c_int, _c_ll, _c_vp, _c_int, _c_ll,
+                                               _c_float, _c_vp, _c_int, _c_ll, _c_int, _c_vp,
+                                               _c_int, _c_int, _c_vp, ctypes.c_size_t, _c_vp]
+            lib.fgemm_sgemm_staged.restype = _c_int
             lib.fgemm_math_supported.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                  _c_float, _c_vp, _c_int, _c_ll, _c_vp, _c_int,
                                                  _c_ll, _c_int]
@@ -265,4 +274,36 @@ def sgemm_splitk_noalloc(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C
         _ptr(bias), 1 if apply_relu else 0, int(splits), _stream(stream, C, A, B))
     if check:
         _check(st, "fgemm_sgemm_splitk_noalloc")
+    return st
+
+
+# stage = -1 for fgemm_sgemm_staged: the launch-time model chooses.
+STAGE_AUTO = -1
+
+
+def staged_workspace_size(transa, transb, M, N, K, batch) -> int:
+    """``fgemm_staged_workspace_size``: bytes of workspace fgemm_sgemm_staged needs."""
+    return int(library().fgemm_staged_workspace_size(int(transa), int(transb), M, N, K, batch))
+
+
+def staged_choice(transa, transb, M, N, K, batch, shared_a, shared_b, aligned_a, aligned_b,
+                  num_sms) -> int:
+    """``fgemm_staged_choice``: which operands a staged call copies k-major (bit 0: A,
+    bit 1: B) by the launch-time model; host-only."""
+    return library().fgemm_staged_choice(int(transa), int(transb), M, N, K, batch,
+                                         1 if shared_a else 0, 1 if shared_b else 0,
+                                         1 if aligned_a else 0, 1 if aligned_b else 0, num_sms)
+
+
+def sgemm_staged(transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
+                 strideC, batch, bias, apply_relu, stage, workspace, workspace_bytes,
+                 stream=None, check=True) -> int:
+    """``fgemm_sgemm_staged``: the GEMM after copying the k-contiguous operands k-major
+    into a caller workspace (stage = STAGE_AUTO: when the model finds it faster)."""
+    st = library().fgemm_sgemm_staged(
+        int(transa), int(transb), M, N, K, alpha, _ptr(A), lda, strideA, _ptr(B), ldb, strideB,
+        beta, _ptr(C), ldc, strideC, batch, _ptr(bias), 1 if apply_relu else 0, int(stage),
+        _ptr(workspace), int(workspace_bytes), _stream(stream, C, A, B))
+    if check:
+        _check(st, "fgemm_sgemm_staged")
     return st

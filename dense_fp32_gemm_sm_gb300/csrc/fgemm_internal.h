@@ -27,7 +27,7 @@ enum ConfigId {
     CFG_128x128_KSPLIT = 7, // CFG_128x128 for all but the last (tiles mod SMs) tiles, which
                             // then run as clusters of four k-slices of whole tiles (second launch)
     CFG_128x128_KCHAIN = 8, // CFG_128x128 for all but the last (tiles mod SMs) tiles, which
-                            // then run as four k-slices of whole tiles, one launch each,
+                            // then run as 2..8 k-slices of whole tiles, one launch each,
                             // added into C in slice order (programmatic dependent launches)
     NUM_CONFIGS = 9,
 };
@@ -51,6 +51,21 @@ int kchain_slices(int ta, int tb, long long r, long long K, int num_sms);
 // The configuration for a problem (host-only; see fgemm_select_config).
 int select_config(int ta, int tb, long long M, long long N, long long K, long long batch,
                   bool aligned, int num_sms);
+
+// Which k-contiguous operands a staged call copies k-major first (bit 0: A stored M x K,
+// bit 1: B stored N x K; 0: none), by the launch-time model: the copies' modelled time
+// plus the GEMM in the layout they leave, against the GEMM as stored.  problems_a/_b:
+// how many distinct problems each operand holds (1 when a batch shares it); aligned_a/_b:
+// whether the operand as stored allows the 16-byte copies.  Host-only.
+int staging_choice(int ta, int tb, long long M, long long N, long long K, long long batch,
+                   long long problems_a, long long problems_b, bool aligned_a, bool aligned_b,
+                   int num_sms);
+
+// Y = X^T for each of `batch` problems (stage.cu): X is R x Cc (leading dimension ldx,
+// problems sx elements apart), Y is Cc x R (ldy, sy).  Asynchronous on `stream`.
+fgemm_status launch_stage_transpose(const float *X, long long ldx, long long sx, int R, int Cc,
+                                    int batch, float *Y, long long ldy, long long sy,
+                                    cudaStream_t stream);
 
 // A validated problem for the tensor-core path (tc_gemm.cu).
 struct TcProblem {

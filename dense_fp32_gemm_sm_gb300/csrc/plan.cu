@@ -103,6 +103,20 @@ double model_us(const LaunchModel &m, double ctas, double K, int num_sms)
 // last-wave launch saves by starting on the SMs the whole tiles leave.
 constexpr double kKchainUsPerSlice = 8.0;
 constexpr double kKchainCreditUs = 16.0;
+
+// The k-major copy of one operand (stage.cu): a launch plus its bytes read and written
+// at the copy's measured rate.
+constexpr double kStageLaunchUs = 4.0;
+constexpr double kStageBytesPerUs = 5.5e6;
+
+// Time of the 128 x 128 kernel per k and CTA round in each transpose layout (NN, NT,
+// TN, TT), relative to TN, the layout whose two operands both arrive by 16-byte copies.
+// Fitted on 152 SMs to whole-tile launches with many CTAs per SM (4096^3 and batched
+// 2048 x 2048 problems with K = 128, 256, 512; t = a + n (c + K b)): b = 0.0750 NN,
+// 0.0809 NT, 0.0717 TN us; TT measured 4.6 % above TN at K = 128.  The fitted model
+// above, from grids of at most a few CTAs per SM, puts the layouts closer together; the
+// staging decision compares layouts, so it uses these.
+constexpr double kLayoutFactor[4] = {1.046, 1.129, 1.000, 1.046};
 constexpr double kTailOverlapUs = 35.0;
 
 long long ksplit_clusters_per_round(int num_sms)
@@ -131,10 +145,13 @@ int kchain_slices(int ta, int tb, long long r, long long K, int num_sms)
     return best;
 }
 
-int select_config(int ta, int tb, long long M, long long N, long long K, long long batch,
-                  bool aligned, int num_sms)
+double select_config_us(int ta, int tb, long long M, long long N, long long K, long long batch,
+                        bool aligned, int num_sms, int *config)
 {
-    if (!aligned) return CFG_64x64_SCALAR;
+    if (!aligned) {
+        *config = CFG_64x64_SCALAR;
+        return 1e300;  // element-wise copies: not modelled
+    }
     if (num_sms < 1) num_sms = 1;
     const long long b = batch > 0 ? batch : 1;
     const long long k = K > 0 ? K : 0;
@@ -186,7 +203,54 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
     Option best = options[0];
     for (const Option &o : options)
         if (o.us < best.us) best = o;
-    return best.config;
+    *config = best.config;
+    return best.us;
+}
+
+int select_config(int ta, int tb, long long M, long long N, long long K, long long batch,
+                  bool aligned, int num_sms)
+{
+    int config = CFG_128x128;
+    (void)select_config_us(ta, tb, M, N, K, batch, aligned, num_sms, &config);
+    return config;
+}
+
+double stage_transpose_us(long long R, long long Cc, long long problems)
+{
+    const double bytes = 8.0 * (double)R * (double)Cc * (double)problems;  // read + write
+    return kStageLaunchUs + bytes / kStageBytesPerUs;
+}
+
+int staging_choice(int ta, int tb, long long M, long long N, long long K, long long batch,
+                   long long problems_a, long long problems_b, bool aligned_a, bool aligned_b,
+                   int num_sms)
+{
+    const int needed = (ta == 0 ? 1 : 0) | (tb == 1 ? 2 : 0);
+    if (needed == 0 || M <= 0 || N <= 0 || K <= 0 || batch <= 0) return 0;
+    // Every candidate from one estimate: the GEMM with both operands k-major (op(A) = T,
+    // op(B) = N) scaled by the layout's measured cost relative to it.
+    int unused = 0;
+    const double base = select_config_us(1, 0, M, N, K, batch, true, num_sms, &unused);
+    const auto layout_us = [&](int a, int b) { return base * kLayoutFactor[(a ? 2 : 0) + (b ? 1 : 0)]; };
+    // As stored: only with 16-byte aligned operands (the element-wise kernel is not modelled
+    // and always slower than the vector kernels after the copies).
+    double best_us = aligned_a && aligned_b ? layout_us(ta, tb) : 1e300;
+    int best = 0;
+    for (int mask = 1; mask <= 3; ++mask) {
+        if ((mask & needed) != mask) continue;
+        const bool sa = (mask & 1) != 0, sb = (mask & 2) != 0;
+        if (!((sa || aligned_a) && (sb || aligned_b))) continue;
+        double us = layout_us(sa ? 1 : ta, sb ? 0 : tb);
+        if (sa) us += stage_transpose_us(M, K, problems_a);
+        if (sb) us += stage_transpose_us(N, K, problems_b);
+        // Stage only for a clear gain (1 % and 1 us over the best so far).
+        const double margin = best_us >= 1e299 ? 0.0 : 0.01 * best_us + 1.0;
+        if (us + margin < best_us) {
+            best_us = us;
+            best = mask;
+        }
+    }
+    return best;
 }
 
 int device_sm_count(int *out)

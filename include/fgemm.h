@@ -168,6 +168,59 @@ fgemm_status fgemm_sgemm_splitk_noalloc(fgemm_op transa, fgemm_op transb, int M,
                                         int apply_relu, int splits, cudaStream_t stream);
 
 /*
+ * GEMM with operand staging through a caller workspace.  GEMM 优化详解, "Level 1:
+ * Naive 实现" (its table of bottlenecks), gives the remedy for an operand read across
+ * its stored rows: transpose it or change its layout.  The CUDA-core kernels keep
+ * op(A) and op(B) k-major in shared memory, so an operand stored with k contiguous
+ * (A for transa == N, B for transb == T) is transposed on its way in, by 4-byte
+ * copies in every tile that reads it.  This call can instead copy such an operand
+ * once, k-major, into `workspace` (a transpose at HBM speed: 8 bytes moved per
+ * element), then run the GEMM on the copy with 16-byte copies only.  On a 152-SM
+ * GB300 this pays for large products (4096^3 NN, the 8192 x 4096 x 11008 FC layer,
+ * batched Q x K^T) and not for small ones, so by default the launch-time model
+ * decides per call.
+ *
+ * Result: that of fgemm_gemm_explicit with config -1 and the same arguments (strided
+ * batch, bias (may be NULL), ReLU), within the same error bound; the sum order can
+ * differ from the unstaged call, so the last bits may too.
+ *   stage: -1 lets the model choose; otherwise a mask -- bit 0 copies A (only when
+ *     transa == N), bit 1 copies B (only when transb == T); bits for an operand that
+ *     is already k-major are ignored, and 0 runs the plain kernels.  Anything outside
+ *     [-1, 3] returns FGEMM_ERR_INVALID_VALUE.
+ *   workspace: caller-owned device memory, 16-byte aligned, at least
+ *     fgemm_staged_workspace_size(transa, transb, M, N, K, batch) bytes, not
+ *     overlapping A, B, C or bias; its contents are overwritten.  Required whenever
+ *     that size is nonzero and the call forms products (K > 0, alpha != 0), whatever
+ *     the choice; a missing, misaligned or too small workspace returns
+ *     FGEMM_ERR_INVALID_VALUE before anything is launched.  An operand a batch shares
+ *     (stride 0) is copied once.
+ *   Any alignment of A and B is accepted: the copies are always 16-byte aligned, so
+ *   staging also lets unaligned operands use the vector kernels.
+ * A staged call is two or three launches on `stream` (the copies, then the GEMM);
+ * it may be captured in a CUDA graph.  Other rules as for fgemm_gemm_explicit.
+ */
+size_t fgemm_staged_workspace_size(fgemm_op transa, fgemm_op transb, int M, int N, int K,
+                                   int batch);
+
+fgemm_status fgemm_sgemm_staged(fgemm_op transa, fgemm_op transb, int M, int N, int K,
+                                float alpha, const float *A, int lda, long long strideA,
+                                const float *B, int ldb, long long strideB, float beta, float *C,
+                                int ldc, long long strideC, int batch, const float *bias,
+                                int apply_relu, int stage, void *workspace,
+                                size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * The mask fgemm_sgemm_staged(stage = -1) would use on a GPU with `num_sms` SMs:
+ * bit 0 set when it copies A, bit 1 when it copies B, 0 when it runs the plain
+ * kernels.  shared_a / shared_b: nonzero when the batch shares the operand (its stride
+ * is 0); aligned_a / aligned_b: nonzero when the operand as stored is 16-byte aligned
+ * (pointer, leading dimension and batch stride).  -1 for arguments out of range.
+ * Host-only: no CUDA call is made.
+ */
+int fgemm_staged_choice(fgemm_op transa, fgemm_op transb, int M, int N, int K, int batch,
+                        int shared_a, int shared_b, int aligned_a, int aligned_b, int num_sms);
+
+/*
  * Arithmetic of the contraction (GEMM 优化详解, "进一步优化方向": tensor cores are the
  * next step after the CUDA-core ladder):
  *   FGEMM_MATH_FP32    FP32 FMA on the CUDA cores (the plain entry points use this).

@@ -54,6 +54,12 @@ class Case:
     # fall back to the CUDA-core kernel (False), as fgemm_math_supported reports; None
     # leaves it open (random cases whose alignment may go either way).
     expect_tc: object = True
+    # Not None: call fgemm_sgemm_staged with this stage argument (-1: the model's choice,
+    # 0..3: the operands to copy k-major) and a NaN-filled workspace of the size
+    # fgemm_staged_workspace_size gives.
+    stage: object = None
+    share_a: bool = False  # batch stride 0 for A (every problem reads the same A)
+    share_b: bool = False
 
 
 def _draw(g, shape, ints):
@@ -82,6 +88,10 @@ def run(case: Case):
     sA, sB, sC = up(a_rows * lda + 3), up(b_rows * ldb + 5), up(M * ldc + 7)
     if case.batch == 0:
         sA = sB = sC = 0
+    if case.share_a:
+        sA = 0
+    if case.share_b:
+        sB = 0
 
     def stored(rows, ld, cols, stride, ints):
         flat = np.full(max(stride * (nb - 1) + rows * ld, 1), np.nan, np.float32)
@@ -125,6 +135,13 @@ def run(case: Case):
                     path, "the tensor cores" if case.expect_tc else "the CUDA-core fallback"))
         fg.gemm_math(case.math, case.ta, case.tb, M, N, K, case.alpha, pA, lda, sA, pB, ldb, sB,
                      case.beta, pC, ldc, sC, nb, pbias, case.relu, stream=stream)
+    elif case.stage is not None:
+        assert case.config < 0
+        ws_bytes = fg.staged_workspace_size(case.ta, case.tb, M, N, K, nb)
+        ws = torch.full((ws_bytes // 4 + 1,), float("nan"), device="cuda")
+        fg.sgemm_staged(case.ta, case.tb, M, N, K, case.alpha, pA, lda, sA, pB, ldb, sB,
+                        case.beta, pC, ldc, sC, nb, pbias, case.relu, case.stage, ws, ws_bytes,
+                        stream=stream)
     else:
         fg.gemm_explicit(case.config, case.ta, case.tb, M, N, K, case.alpha, pA, lda, sA, pB, ldb,
                          sB, case.beta, pC, ldc, sC, nb, pbias, case.relu, stream=stream)

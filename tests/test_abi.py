@@ -233,3 +233,51 @@ def test_noalloc_checks_arguments_before_the_scratch_size():
         assert fg.sgemm_splitk_noalloc(**dict(ok, **bad), check=False) == fg.ERR_INVALID_VALUE
     # nothing to do is a no-op at any size
     assert fg.sgemm_splitk_noalloc(**dict(ok, M=0), check=False) == fg.OK
+
+
+def test_staged_workspace_size():
+    sz = fg.staged_workspace_size
+    # A's k-major copy: K rows of ld4(M) floats a problem; B's after it at 256 bytes
+    assert sz(0, 0, 4096, 4096, 4096, 1) == 4096 * 4096 * 4
+    assert sz(0, 0, 5, 7, 3, 2) == 2 * 3 * 8 * 4  # ld4(5) = 8
+    a = 2 * 3 * 8 * 4
+    assert sz(0, 1, 5, 7, 3, 2) == (a + 255) // 256 * 256 + 2 * 3 * 8 * 4  # ld4(7) = 8
+    assert sz(1, 1, 5, 7, 3, 2) == 2 * 3 * 8 * 4  # B only
+    assert sz(1, 0, 4096, 4096, 4096, 1) == 0  # both operands already k-major
+    for bad in ((0, 0, -1, 4, 4, 1), (0, 0, 4, 4, 0, 1), (0, 0, 4, 4, 4, 0), (2, 0, 4, 4, 4, 1)):
+        assert sz(*bad) == 0
+
+
+def test_staged_choice_host_query():
+    ch = fg.staged_choice
+    # the model on 152 SMs: copy where the 16-byte-copy layout repays the copy
+    assert ch(0, 0, 4096, 4096, 4096, 1, 0, 0, 1, 1, 152) == 1
+    assert ch(0, 1, 4096, 4096, 4096, 1, 0, 0, 1, 1, 152) == 3
+    assert ch(1, 1, 4096, 4096, 4096, 1, 0, 0, 1, 1, 152) == 2
+    assert ch(1, 0, 4096, 4096, 4096, 1, 0, 0, 1, 1, 152) == 0
+    assert ch(0, 1, 2048, 2048, 128, 128, 0, 0, 1, 1, 152) == 3
+    assert ch(0, 0, 2048, 128, 2048, 128, 0, 0, 1, 1, 152) == 0
+    assert ch(0, 0, 1024, 1024, 1024, 1, 0, 0, 1, 1, 152) == 0
+    # unaligned A: copying it is the way to the 16-byte kernels, even when small
+    assert ch(0, 0, 256, 256, 256, 1, 0, 0, 0, 1, 152) == 1
+    # ... but not when the other operand (not copied in this layout) is unaligned too
+    assert ch(1, 1, 256, 256, 256, 1, 0, 0, 0, 1, 152) == 0
+    # a batch-shared operand is copied once: cheaper, so copied at least as readily
+    assert ch(0, 0, 2048, 128, 2048, 128, 1, 0, 1, 1, 152) == 1
+    assert ch(0, 0, 0, 4, 4, 1, 0, 0, 1, 1, 152) == 0
+    assert ch(0, 0, -1, 4, 4, 1, 0, 0, 1, 1, 152) == -1
+    assert ch(0, 0, 4, 4, 4, 1, 0, 0, 1, 1, 0) == -1
+
+
+@pytest.mark.parametrize("kw", [dict(stage=4), dict(stage=-2), dict(M=-1), dict(lda=1),
+                                dict(workspace=0), dict(workspace_bytes=16),
+                                dict(workspace=FAKE + 4)])
+def test_staged_validates_before_launch(kw):
+    args = dict(ta=0, tb=1, M=64, N=64, K=64, lda=64, workspace=FAKE, stage=fg.STAGE_AUTO)
+    args.update(kw)
+    need = fg.staged_workspace_size(0, 1, 64, 64, 64, 1)
+    wsb = args.get("workspace_bytes", need)
+    st = fg.sgemm_staged(args["ta"], args["tb"], args["M"], args["N"], args["K"], 1.0, FAKE,
+                         args["lda"], 0, FAKE, 64, 0, 0.0, FAKE, 64, 0, 1, None, False,
+                         args["stage"], args["workspace"], wsb, check=False)
+    assert st == fg.ERR_INVALID_VALUE
