@@ -196,8 +196,10 @@ fgemm_status fgemm_sgemm_splitk_noalloc(fgemm_op transa, fgemm_op transb, int M,
  *     (stride 0) is copied once.
  *   Any alignment of A and B is accepted: the copies are always 16-byte aligned, so
  *   staging also lets unaligned operands use the vector kernels.
- * A staged call is two or three launches on `stream` (the copies, then the GEMM);
- * it may be captured in a CUDA graph.  Other rules as for fgemm_gemm_explicit.
+ * A staged call launches on `stream` one copy kernel per copied operand (and per 65535
+ * problems of a batch), then the GEMM's launches (fgemm_launch_count of the layout the
+ * copies leave); it may be captured in a CUDA graph.  Other rules as for
+ * fgemm_gemm_explicit.
  */
 size_t fgemm_staged_workspace_size(fgemm_op transa, fgemm_op transb, int M, int N, int K,
                                    int batch);
