@@ -309,15 +309,17 @@ fgemm_status run_staged(const Problem &p, int stage, void *workspace, size_t wor
     if (noop) return FGEMM_OK;
     const bool products = p.K > 0 && p.alpha != 0.0f;
     if (!products) return run(-1, p);
+    const int needed = (p.ta == 0 ? 1 : 0) | (p.tb == 1 ? 2 : 0);
+    // The workspace is checked whenever the stage argument allows a copy (the model's
+    // choice or a mask naming an operand that has to be copied), whatever is chosen.
     const StageLayout full = stage_layout(p.ta, p.tb, p.M, p.N, p.K, p.batch, p.batch);
-    if (full.bytes > 0 &&
+    if ((stage < 0 || (stage & needed) != 0) && full.bytes > 0 &&
         (workspace == nullptr || workspace_bytes < full.bytes ||
          reinterpret_cast<uintptr_t>(workspace) % 16 != 0))
         return FGEMM_ERR_INVALID_VALUE;
     // An operand a batch shares (stride 0) is copied once.
     const long long problems_a = p.batch > 1 && p.sA != 0 ? p.batch : 1;
     const long long problems_b = p.batch > 1 && p.sB != 0 ? p.batch : 1;
-    const int needed = (p.ta == 0 ? 1 : 0) | (p.tb == 1 ? 2 : 0);
     int mask = stage & needed;
     if (stage < 0) {
         int sms = 0;

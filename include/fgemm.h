@@ -190,10 +190,11 @@ fgemm_status fgemm_sgemm_splitk_noalloc(fgemm_op transa, fgemm_op transb, int M,
  *   workspace: caller-owned device memory, 16-byte aligned, at least
  *     fgemm_staged_workspace_size(transa, transb, M, N, K, batch) bytes, not
  *     overlapping A, B, C or bias; its contents are overwritten.  Required whenever
- *     that size is nonzero and the call forms products (K > 0, alpha != 0), whatever
- *     the choice; a missing, misaligned or too small workspace returns
- *     FGEMM_ERR_INVALID_VALUE before anything is launched.  An operand a batch shares
- *     (stride 0) is copied once.
+ *     that size is nonzero, the call forms products (K > 0, alpha != 0) and `stage`
+ *     allows a copy (-1, or a mask naming an operand stored with k contiguous),
+ *     whatever the model then chooses; a missing, misaligned or too small workspace
+ *     returns FGEMM_ERR_INVALID_VALUE before anything is launched.  With nothing to
+ *     copy it may be NULL.  An operand a batch shares (stride 0) is copied once.
  *   Any alignment of A and B is accepted: the copies are always 16-byte aligned, so
  *   staging also lets unaligned operands use the vector kernels.
  * A staged call launches on `stream` one copy kernel per copied operand (and per 65535

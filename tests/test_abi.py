@@ -271,7 +271,8 @@ def test_staged_choice_host_query():
 
 @pytest.mark.parametrize("kw", [dict(stage=4), dict(stage=-2), dict(M=-1), dict(lda=1),
                                 dict(workspace=0), dict(workspace_bytes=16),
-                                dict(workspace=FAKE + 4)])
+                                dict(workspace=FAKE + 4), dict(workspace=0, stage=1),
+                                dict(workspace=0, stage=3), dict(workspace_bytes=16, stage=2)])
 def test_staged_validates_before_launch(kw):
     args = dict(ta=0, tb=1, M=64, N=64, K=64, lda=64, workspace=FAKE, stage=fg.STAGE_AUTO)
     args.update(kw)

@@ -147,6 +147,13 @@ def test_argument_checks_launch_nothing():
         assert st == fg.ERR_INVALID_VALUE, kw
     torch.cuda.synchronize()
     assert bool((C == 7.0).all())
+    # stage = 0, or a mask naming only operands already k-major: no copy, no workspace
+    for stage, ta in ((0, 0), (2, 0)):
+        C.fill_(7.0)
+        fg.sgemm_staged(ta, 0, M, N, K, 1.0, A, K, 0, B, N, 0, 0.0, C, N, 0, 1, None, False,
+                        stage, None, 0)
+        torch.cuda.synchronize()
+        assert bool((C == float(K)).all())
     # op(A) = T, op(B) = N needs no copy and no workspace
     assert fg.staged_workspace_size(1, 0, M, N, K, 1) == 0
     fg.sgemm_staged(1, 0, M, N, K, 1.0, A, M, 0, B, N, 0, 0.0, C, N, 0, 1, None, False,
