@@ -3,8 +3,10 @@
 Each case draws a transpose combination, ragged M, N, K, alpha/beta from values that
 keep integer arithmetic exact, the epilogue options, a strided batch, padded leading
 dimensions, unaligned pointers, an explicit kernel configuration or the library's own
-choice, and the arithmetic (CUDA cores, TF32, 3xTF32).  Integer-valued data makes every
-case bit-exact, so any dropped, duplicated or misplaced partial product shows.
+choice, and the arithmetic (CUDA cores, TF32, 3xTF32); further cases go through the
+staged entry with a random staging mask, shared batch operands and any alignment.
+Integer-valued data makes every case bit-exact, so any dropped, duplicated or misplaced
+partial product shows.
 """
 
 import random
@@ -51,12 +53,13 @@ def test_random_case(i):
 
 
 N_SPLIT_CASES = 24
-SPLITS = ("simt_128x128_t8x8_split", "simt_128x128_t8x8_ksplit")
+SPLITS = ("simt_128x128_t8x8_split", "simt_128x128_t8x8_ksplit", "simt_128x128_t8x8_kchain")
 
 
 def draw_split(rng):
     # grids larger than the SM count, so that whole tiles and a last wave of split
-    # tiles (quarters or k-slice clusters) meet in one call, on ragged edges
+    # tiles (quarters, k-slice clusters or chained k-slices) meet in one call, on
+    # ragged edges
     kw = dict(ta=rng.randint(0, 1), tb=rng.randint(0, 1), M=rng.randint(1500, 2600),
               N=rng.randint(1500, 2600), K=rng.choice([1, 31, 64, 97, rng.randint(1, 200)]),
               alpha=rng.choice([1.0, 2.0, -0.5]), beta=rng.choice([0.0, 1.0, -2.0]),
@@ -76,3 +79,32 @@ def test_random_split_case(i):
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     check(Case(**draw_split(random.Random(5000 + i))))
+
+
+N_STAGED_CASES = 40
+
+
+def draw_staged(rng):
+    # fgemm_sgemm_staged: a random staging mask (or the model's choice) over the whole
+    # argument space, with bias and ReLU on batches and operands a batch shares
+    kw = dict(ta=rng.randint(0, 1), tb=rng.randint(0, 1), M=rng.randint(1, 700),
+              N=rng.randint(1, 700), K=rng.choice([0, 1, 5, 32, 65, rng.randint(1, 400)]),
+              alpha=rng.choice([1.0, 2.0, -0.5, 0.0]), beta=rng.choice([0.0, 1.0, -2.0]),
+              bias=rng.random() < 0.5, relu=rng.random() < 0.5,
+              batch=rng.choice([0, 0, 1, 3, 5]),
+              pad=(rng.choice([0, 1, 4]), rng.choice([0, 3, 8]), rng.choice([0, 2, 4])),
+              stage=rng.choice([fg.STAGE_AUTO, 0, 1, 2, 3]), seed=rng.randint(0, 1 << 30))
+    if rng.random() < 0.3:
+        kw.update(offset=(rng.randint(0, 3), rng.randint(0, 3), rng.randint(0, 3)), align_ld=False)
+    if kw["batch"] > 1:
+        kw["share_a"] = rng.random() < 0.3
+        kw["share_b"] = rng.random() < 0.3
+    kw["c_nan"] = kw["beta"] == 0.0 and rng.random() < 0.5
+    return kw
+
+
+@pytest.mark.parametrize("i", range(N_STAGED_CASES))
+def test_random_staged_case(i):
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    check(Case(**draw_staged(random.Random(9000 + i))))
