@@ -233,9 +233,14 @@ int staging_choice(int ta, int tb, long long M, long long N, long long K, long l
     int unused = 0;
     const double base = select_config_us(1, 0, M, N, K, batch, true, num_sms, &unused);
     const auto layout_us = [&](int a, int b) { return base * kLayoutFactor[(a ? 2 : 0) + (b ? 1 : 0)]; };
-    // As stored: only with 16-byte aligned operands (the element-wise kernel is not modelled
-    // and always slower than the vector kernels after the copies).
-    double best_us = aligned_a && aligned_b ? layout_us(ta, tb) : 1e300;
+    // As stored: the selected kernel with 16-byte aligned operands, else the 64 x 64
+    // element-wise kernel (measured within 4 % of the vector 64 x 64 tile from 64^3 to
+    // 4096^3, so that tile's model with a 4 % allowance).
+    double best_us = layout_us(ta, tb);
+    if (!(aligned_a && aligned_b)) {
+        const LaunchModel &m64 = kModel[(ta ? 2 : 0) + (tb ? 1 : 0)][M_64x64];
+        best_us = 1.04 * model_us(m64, tiles_of(M, N, 64, 64, batch), (double)K, num_sms);
+    }
     int best = 0;
     for (int mask = 1; mask <= 3; ++mask) {
         if ((mask & needed) != mask) continue;
@@ -245,7 +250,7 @@ int staging_choice(int ta, int tb, long long M, long long N, long long K, long l
         if (sa) us += stage_transpose_us(M, K, problems_a);
         if (sb) us += stage_transpose_us(N, K, problems_b);
         // Stage only for a clear gain (1 % and 1 us over the best so far).
-        const double margin = best_us >= 1e299 ? 0.0 : 0.01 * best_us + 1.0;
+        const double margin = 0.01 * best_us + 1.0;
         if (us + margin < best_us) {
             best_us = us;
             best = mask;
