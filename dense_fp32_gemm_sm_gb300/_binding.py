@@ -83,7 +83,7 @@ def library() -> ctypes.CDLL:
             lib.fgemm_splitk_workspace_size.restype = ctypes.c_size_t
             lib.fgemm_staged_workspace_size.argtypes = [_c_int] * 6
             lib.fgemm_staged_workspace_size.restype = ctypes.c_size_t
-            lib.fgemm_staged_choice.argtypes = [_c_int] * 11
+            lib.fgemm_staged_choice.argtypes = [_c_int] * 10 + [ctypes.c_size_t, _c_int]
             lib.fgemm_staged_choice.restype = _c_int
             lib.fgemm_sgemm_staged.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int, _c_float,
                                                _c_vp, _c_int, _c_ll, _c_vp, _c_int, _c_ll,
@@ -287,19 +287,24 @@ def staged_workspace_size(transa, transb, M, N, K, batch) -> int:
 
 
 def staged_choice(transa, transb, M, N, K, batch, shared_a, shared_b, aligned_a, aligned_b,
-                  num_sms) -> int:
-    """``fgemm_staged_choice``: which operands a staged call copies k-major (bit 0: A,
-    bit 1: B) by the launch-time model; host-only."""
+                  num_sms, workspace_bytes=None) -> int:
+    """``fgemm_staged_choice``: which operands a staged call copies into its workspace
+    (bit 0: A, bit 1: B) by the launch-time model; host-only.  workspace_bytes=None:
+    the full fgemm_staged_workspace_size."""
+    if workspace_bytes is None:
+        workspace_bytes = staged_workspace_size(transa, transb, M, N, K, max(1, batch))
     return library().fgemm_staged_choice(int(transa), int(transb), M, N, K, batch,
                                          1 if shared_a else 0, 1 if shared_b else 0,
-                                         1 if aligned_a else 0, 1 if aligned_b else 0, num_sms)
+                                         1 if aligned_a else 0, 1 if aligned_b else 0,
+                                         int(workspace_bytes), num_sms)
 
 
 def sgemm_staged(transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, strideB, beta, C, ldc,
                  strideC, batch, bias, apply_relu, stage, workspace, workspace_bytes,
                  stream=None, check=True) -> int:
-    """``fgemm_sgemm_staged``: the GEMM after copying the k-contiguous operands k-major
-    into a caller workspace (stage = STAGE_AUTO: when the model finds it faster)."""
+    """``fgemm_sgemm_staged``: the GEMM after copying operands into a caller workspace
+    (transposed k-major, or re-pitched when unaligned; stage = STAGE_AUTO: the copies the
+    model finds faster among those that fit)."""
     st = library().fgemm_sgemm_staged(
         int(transa), int(transb), M, N, K, alpha, _ptr(A), lda, strideA, _ptr(B), ldb, strideB,
         beta, _ptr(C), ldc, strideC, batch, _ptr(bias), 1 if apply_relu else 0, int(stage),

@@ -273,32 +273,13 @@ TcProblem tc_problem(const Problem &p)
     return q;
 }
 
-// Staged calls: the operands stored with k contiguous (A for op N, B for op T) are
-// first copied k-major into the caller's workspace, and the GEMM then runs in the
-// layout that leaves (op(A) = T, op(B) = N for both staged), whose tiles move both
-// operands with 16-byte copies.  Workspace layout: A's copy (K x ld4(M) floats a
-// problem) at offset 0, B's copy (K x ld4(N)) at the next multiple of 256 bytes.
+// Staged calls: operands are first copied into the caller's workspace -- one stored
+// with k contiguous (A for op N, B for op T) transposed k-major, one already k-major but
+// not 16-byte aligned re-pitched into aligned rows -- and the GEMM then runs on the
+// copies (op(A) = T and op(B) = N for a copied operand), whose tiles move them with
+// 16-byte copies.  Workspace layout: the chosen copies packed, A's (K x ld4(M) floats a
+// problem) first, B's (K x ld4(N)) at the next multiple of 256 bytes (stage_bytes).
 long long ld4(long long x) { return (x + 3) / 4 * 4; }
-
-struct StageLayout {
-    long long lda, sa, ldb, sb;  // leading dimensions and problem strides of the copies
-    size_t off_b, bytes;         // byte offset of B's copy; bytes in all
-};
-
-StageLayout stage_layout(int ta, int tb, long long M, long long N, long long K,
-                         long long problems_a, long long problems_b)
-{
-    StageLayout L{};
-    L.lda = ld4(M);
-    L.sa = K * L.lda;
-    L.ldb = ld4(N);
-    L.sb = K * L.ldb;
-    const size_t a_bytes = ta == 0 ? (size_t)problems_a * (size_t)L.sa * sizeof(float) : 0;
-    const size_t b_bytes = tb == 1 ? (size_t)problems_b * (size_t)L.sb * sizeof(float) : 0;
-    L.off_b = (a_bytes + 255) / 256 * 256;
-    L.bytes = b_bytes > 0 ? L.off_b + b_bytes : a_bytes;
-    return L;
-}
 
 fgemm_status run_staged(const Problem &p, int stage, void *workspace, size_t workspace_bytes)
 {
@@ -306,21 +287,16 @@ fgemm_status run_staged(const Problem &p, int stage, void *workspace, size_t wor
     fgemm_status st = validate(p, &noop);
     if (st != FGEMM_OK) return st;
     if (stage < -1 || stage > 3) return FGEMM_ERR_INVALID_VALUE;
+    if (workspace != nullptr && reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+        return FGEMM_ERR_INVALID_VALUE;
     if (noop) return FGEMM_OK;
     const bool products = p.K > 0 && p.alpha != 0.0f;
     if (!products) return run(-1, p);
-    const int needed = (p.ta == 0 ? 1 : 0) | (p.tb == 1 ? 2 : 0);
-    // The workspace is checked whenever the stage argument allows a copy (the model's
-    // choice or a mask naming an operand that has to be copied), whatever is chosen.
-    const StageLayout full = stage_layout(p.ta, p.tb, p.M, p.N, p.K, p.batch, p.batch);
-    if ((stage < 0 || (stage & needed) != 0) && full.bytes > 0 &&
-        (workspace == nullptr || workspace_bytes < full.bytes ||
-         reinterpret_cast<uintptr_t>(workspace) % 16 != 0))
-        return FGEMM_ERR_INVALID_VALUE;
     // An operand a batch shares (stride 0) is copied once.
     const long long problems_a = p.batch > 1 && p.sA != 0 ? p.batch : 1;
     const long long problems_b = p.batch > 1 && p.sB != 0 ? p.batch : 1;
-    int mask = stage & needed;
+    const size_t avail = workspace != nullptr ? workspace_bytes : 0;
+    int mask = stage;
     if (stage < 0) {
         int sms = 0;
         if (device_sm_count(&sms) != 0) {
@@ -329,31 +305,41 @@ fgemm_status run_staged(const Problem &p, int stage, void *workspace, size_t wor
         }
         mask = staging_choice(p.ta, p.tb, p.M, p.N, p.K, p.batch, problems_a, problems_b,
                               aligned16(p.A, p.lda, p.sA, p.batch),
-                              aligned16(p.B, p.ldb, p.sB, p.batch), sms);
+                              aligned16(p.B, p.ldb, p.sB, p.batch), avail, sms);
+    } else if (stage_bytes(mask, p.M, p.N, p.K, problems_a, problems_b) > avail) {
+        return FGEMM_ERR_INVALID_VALUE;  // the copies asked for do not fit
     }
     if (mask == 0) return run(-1, p);
-    const StageLayout L = stage_layout(p.ta, p.tb, p.M, p.N, p.K, problems_a, problems_b);
     char *const ws = static_cast<char *>(workspace);
     Problem q = p;
     if (mask & 1) {
-        float *const At = reinterpret_cast<float *>(ws);
-        st = launch_stage_transpose(p.A, p.lda, problems_a > 1 ? p.sA : 0, p.M, p.K,
-                                    (int)problems_a, At, L.lda, L.sa, p.stream);
+        float *const Ac = reinterpret_cast<float *>(ws);
+        const long long ld = ld4(p.M), s = p.K * ld;
+        const long long sx = problems_a > 1 ? p.sA : 0;
+        st = p.ta == 0 ? launch_stage_transpose(p.A, p.lda, sx, p.M, p.K, (int)problems_a, Ac, ld,
+                                                s, p.stream)
+                       : launch_stage_repitch(p.A, p.lda, sx, p.K, p.M, (int)problems_a, Ac, ld, s,
+                                              p.stream);
         if (st != FGEMM_OK) return st;
         q.ta = 1;
-        q.A = At;
-        q.lda = L.lda;
-        q.sA = problems_a > 1 ? L.sa : 0;
+        q.A = Ac;
+        q.lda = ld;
+        q.sA = problems_a > 1 ? s : 0;
     }
     if (mask & 2) {
-        float *const Bt = reinterpret_cast<float *>(ws + L.off_b);
-        st = launch_stage_transpose(p.B, p.ldb, problems_b > 1 ? p.sB : 0, p.N, p.K,
-                                    (int)problems_b, Bt, L.ldb, L.sb, p.stream);
+        const size_t off = (mask & 1) ? stage_bytes(1, p.M, p.N, p.K, problems_a, problems_b) : 0;
+        float *const Bc = reinterpret_cast<float *>(ws + (off + 255) / 256 * 256);
+        const long long ld = ld4(p.N), s = p.K * ld;
+        const long long sx = problems_b > 1 ? p.sB : 0;
+        st = p.tb == 1 ? launch_stage_transpose(p.B, p.ldb, sx, p.N, p.K, (int)problems_b, Bc, ld,
+                                                s, p.stream)
+                       : launch_stage_repitch(p.B, p.ldb, sx, p.K, p.N, (int)problems_b, Bc, ld, s,
+                                              p.stream);
         if (st != FGEMM_OK) return st;
         q.tb = 0;
-        q.B = Bt;
-        q.ldb = L.ldb;
-        q.sB = problems_b > 1 ? L.sb : 0;
+        q.B = Bc;
+        q.ldb = ld;
+        q.sB = problems_b > 1 ? s : 0;
     }
     return run(-1, q);
 }
@@ -497,11 +483,12 @@ size_t fgemm_staged_workspace_size(fgemm_op transa, fgemm_op transb, int M, int 
         (transb != FGEMM_OP_N && transb != FGEMM_OP_T) || M <= 0 || N <= 0 || K <= 0 ||
         batch <= 0)
         return 0;
-    return fgemm::stage_layout((int)transa, (int)transb, M, N, K, batch, batch).bytes;
+    return fgemm::stage_bytes(3, M, N, K, batch, batch);
 }
 
 int fgemm_staged_choice(fgemm_op transa, fgemm_op transb, int M, int N, int K, int batch,
-                        int shared_a, int shared_b, int aligned_a, int aligned_b, int num_sms)
+                        int shared_a, int shared_b, int aligned_a, int aligned_b,
+                        size_t workspace_bytes, int num_sms)
 {
     if ((transa != FGEMM_OP_N && transa != FGEMM_OP_T) ||
         (transb != FGEMM_OP_N && transb != FGEMM_OP_T) || M < 0 || N < 0 || K < 0 ||
@@ -510,7 +497,8 @@ int fgemm_staged_choice(fgemm_op transa, fgemm_op transb, int M, int N, int K, i
     const long long problems_a = batch > 1 && !shared_a ? batch : 1;
     const long long problems_b = batch > 1 && !shared_b ? batch : 1;
     return fgemm::staging_choice((int)transa, (int)transb, M, N, K, batch, problems_a,
-                                 problems_b, aligned_a != 0, aligned_b != 0, num_sms);
+                                 problems_b, aligned_a != 0, aligned_b != 0, workspace_bytes,
+                                 num_sms);
 }
 
 fgemm_status fgemm_sgemm_staged(fgemm_op transa, fgemm_op transb, int M, int N, int K,

@@ -4,6 +4,8 @@
 
 #include <cuda_runtime.h>
 
+#include <cstddef>
+
 #include "fgemm.h"
 
 namespace fgemm {
@@ -52,20 +54,34 @@ int kchain_slices(int ta, int tb, long long r, long long K, int num_sms);
 int select_config(int ta, int tb, long long M, long long N, long long K, long long batch,
                   bool aligned, int num_sms);
 
-// Which k-contiguous operands a staged call copies k-major first (bit 0: A stored M x K,
-// bit 1: B stored N x K; 0: none), by the launch-time model: the copies' modelled time
-// plus the GEMM in the layout they leave, against the GEMM as stored.  problems_a/_b:
-// how many distinct problems each operand holds (1 when a batch shares it); aligned_a/_b:
-// whether the operand as stored allows the 16-byte copies.  Host-only.
+// Bytes of the workspace copies a staged call makes with `mask` (bit 0: A, bit 1: B): each
+// copy is K x ld4(rows) floats a problem (ld4: rounded up to a multiple of 4), B's starting
+// at the next multiple of 256 bytes after A's.  problems_a/_b: the problems each operand
+// holds (1 when a batch shares it).
+size_t stage_bytes(int mask, long long M, long long N, long long K, long long problems_a,
+                   long long problems_b);
+
+// Which operands a staged call copies into the workspace first (bit 0: A, bit 1: B; 0:
+// none), by the launch-time model: an operand stored with k contiguous is transposed
+// k-major, a k-major one that is not 16-byte aligned gets aligned rows; the copies' modelled
+// time plus the GEMM in the layout they leave, against the GEMM as stored, among the copies
+// that fit in `workspace_bytes`.  aligned_a/_b: whether the operand as stored allows the
+// 16-byte copies.  Host-only.
 int staging_choice(int ta, int tb, long long M, long long N, long long K, long long batch,
                    long long problems_a, long long problems_b, bool aligned_a, bool aligned_b,
-                   int num_sms);
+                   size_t workspace_bytes, int num_sms);
 
 // Y = X^T for each of `batch` problems (stage.cu): X is R x Cc (leading dimension ldx,
 // problems sx elements apart), Y is Cc x R (ldy, sy).  Asynchronous on `stream`.
 fgemm_status launch_stage_transpose(const float *X, long long ldx, long long sx, int R, int Cc,
                                     int batch, float *Y, long long ldy, long long sy,
                                     cudaStream_t stream);
+
+// Y = X (R x Cc) into rows of leading dimension ldy for each of `batch` problems: the
+// copy of a k-major operand whose rows are not 16-byte aligned (stage.cu).
+fgemm_status launch_stage_repitch(const float *X, long long ldx, long long sx, int R, int Cc,
+                                  int batch, float *Y, long long ldy, long long sy,
+                                  cudaStream_t stream);
 
 // A validated problem for the tensor-core path (tc_gemm.cu).
 struct TcProblem {

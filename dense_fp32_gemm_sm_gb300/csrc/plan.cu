@@ -104,8 +104,8 @@ double model_us(const LaunchModel &m, double ctas, double K, int num_sms)
 constexpr double kKchainUsPerSlice = 8.0;
 constexpr double kKchainCreditUs = 16.0;
 
-// The k-major copy of one operand (stage.cu): a launch plus its bytes read and written
-// at the copy's measured rate (CUDA events, L2 flushed, on 152 SMs: 64 MB of A at 4096^3
+// The copy of one operand into the workspace (stage.cu; a transpose or a re-pitch): a
+// launch plus its bytes read and written at the copy's measured rate (CUDA events, L2 flushed, on 152 SMs: 64 MB of A at 4096^3
 // in 24.6 us, 128 MB in 47.1 us, 16 MB in 9.2 us, 4 MB in 6.1 us).
 constexpr double kStageLaunchUs = 4.0;
 constexpr double kStageBytesPerUs = 6.2e6;
@@ -216,42 +216,51 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
     return config;
 }
 
-double stage_transpose_us(long long R, long long Cc, long long problems)
+double stage_copy_us(long long R, long long Cc, long long problems)
 {
     const double bytes = 8.0 * (double)R * (double)Cc * (double)problems;  // read + write
     return kStageLaunchUs + bytes / kStageBytesPerUs;
 }
 
+size_t stage_bytes(int mask, long long M, long long N, long long K, long long problems_a,
+                   long long problems_b)
+{
+    const size_t a = (mask & 1) ? (size_t)problems_a * (size_t)K * (size_t)((M + 3) / 4 * 4) * 4 : 0;
+    const size_t b = (mask & 2) ? (size_t)problems_b * (size_t)K * (size_t)((N + 3) / 4 * 4) * 4 : 0;
+    return b == 0 ? a : (a + 255) / 256 * 256 + b;
+}
+
 int staging_choice(int ta, int tb, long long M, long long N, long long K, long long batch,
                    long long problems_a, long long problems_b, bool aligned_a, bool aligned_b,
-                   int num_sms)
+                   size_t workspace_bytes, int num_sms)
 {
-    const int needed = (ta == 0 ? 1 : 0) | (tb == 1 ? 2 : 0);
-    if (needed == 0 || M <= 0 || N <= 0 || K <= 0 || batch <= 0) return 0;
+    if (M <= 0 || N <= 0 || K <= 0 || batch <= 0) return 0;
+    // A copy can help an operand stored with k contiguous (it is transposed) or one that
+    // is k-major but not 16-byte aligned (it gets aligned rows); others stay as stored.
+    const int useful = ((ta == 0 || !aligned_a) ? 1 : 0) | ((tb == 1 || !aligned_b) ? 2 : 0);
+    if (useful == 0) return 0;
     // Every candidate from one estimate: the GEMM with both operands k-major (op(A) = T,
-    // op(B) = N) scaled by the layout's measured cost relative to it.
+    // op(B) = N) scaled by the layout's measured cost relative to it; with an unaligned
+    // operand left as stored, the 64 x 64 element-wise kernel (measured within 4 % of the
+    // vector 64 x 64 tile from 64^3 to 4096^3, so that tile's model with a 4 % allowance).
     int unused = 0;
     const double base = select_config_us(1, 0, M, N, K, batch, true, num_sms, &unused);
-    const auto layout_us = [&](int a, int b) { return base * kLayoutFactor[(a ? 2 : 0) + (b ? 1 : 0)]; };
-    // As stored: the selected kernel with 16-byte aligned operands, else the 64 x 64
-    // element-wise kernel (measured within 4 % of the vector 64 x 64 tile from 64^3 to
-    // 4096^3, so that tile's model with a 4 % allowance).
-    double best_us = layout_us(ta, tb);
-    if (!(aligned_a && aligned_b)) {
-        const LaunchModel &m64 = kModel[(ta ? 2 : 0) + (tb ? 1 : 0)][M_64x64];
-        best_us = 1.04 * model_us(m64, tiles_of(M, N, 64, 64, batch), (double)K, num_sms);
-    }
+    const auto gemm_us = [&](int a, int b, bool aligned) {
+        if (aligned) return base * kLayoutFactor[(a ? 2 : 0) + (b ? 1 : 0)];
+        const LaunchModel &m64 = kModel[(a ? 2 : 0) + (b ? 1 : 0)][M_64x64];
+        return 1.04 * model_us(m64, tiles_of(M, N, 64, 64, batch), (double)K, num_sms);
+    };
+    double best_us = gemm_us(ta, tb, aligned_a && aligned_b);
     int best = 0;
     for (int mask = 1; mask <= 3; ++mask) {
-        if ((mask & needed) != mask) continue;
+        if ((mask & useful) != mask) continue;
+        if (stage_bytes(mask, M, N, K, problems_a, problems_b) > workspace_bytes) continue;
         const bool sa = (mask & 1) != 0, sb = (mask & 2) != 0;
-        if (!((sa || aligned_a) && (sb || aligned_b))) continue;
-        double us = layout_us(sa ? 1 : ta, sb ? 0 : tb);
-        if (sa) us += stage_transpose_us(M, K, problems_a);
-        if (sb) us += stage_transpose_us(N, K, problems_b);
+        double us = gemm_us(sa ? 1 : ta, sb ? 0 : tb, (sa || aligned_a) && (sb || aligned_b));
+        if (sa) us += stage_copy_us(M, K, problems_a);
+        if (sb) us += stage_copy_us(N, K, problems_b);
         // Stage only for a clear gain (1 % and 1 us over the best so far).
-        const double margin = 0.01 * best_us + 1.0;
-        if (us + margin < best_us) {
+        if (us + 0.01 * best_us + 1.0 < best_us) {
             best_us = us;
             best = mask;
         }

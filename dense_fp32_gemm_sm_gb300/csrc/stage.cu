@@ -15,6 +15,10 @@
 // X: R x Cc, row-major with leading dimension ldx, problems sx elements apart.
 // Y: Cc x R, row-major with leading dimension ldy, problems sy elements apart.
 //
+// An operand that is already k-major but not 16-byte aligned (an odd leading dimension
+// or pointer) is copied row by row into aligned rows instead (stage_repitch_kernel),
+// so that the GEMM after the copies can use its 16-byte kernels.
+//
 // Each CTA moves a 64 x 64 block through shared memory.  Interior blocks of a
 // 16-byte-aligned X (the common case) go by 16-byte loads and stores: a thread reads
 // four 4-float chunks of X's rows and writes four 4-float chunks of Y's rows, with its
@@ -112,7 +116,52 @@ __global__ void __launch_bounds__(kThreads) stage_transpose_kernel(
     }
 }
 
+// Y = X row by row into rows of leading dimension ldy (a multiple of 4): an operand
+// that is already k-major but whose rows do not start on 16 bytes gets aligned rows.
+// Thread (x, y) copies column blockIdx.x * 256 + threadIdx.x of a group of kRepitchRows
+// rows, all loads in flight before the stores; warps read and write 128 contiguous bytes.
+constexpr int kRepitchRows = 8;
+
+__global__ void __launch_bounds__(kThreads) stage_repitch_kernel(
+    const float *__restrict__ X, long long ldx, long long sx, int R, int Cc,
+    float *__restrict__ Y, long long ldy, long long sy, int batch0)
+{
+    const long long b = (long long)batch0 + blockIdx.z;
+    const float *const x = X + b * sx;
+    float *const y = Y + b * sy;
+    const long long c = (long long)blockIdx.x * kThreads + threadIdx.x;
+    if (c >= Cc) return;
+    for (long long r0 = (long long)blockIdx.y * kRepitchRows; r0 < R;
+         r0 += (long long)gridDim.y * kRepitchRows) {
+        float v[kRepitchRows];
+#pragma unroll
+        for (int i = 0; i < kRepitchRows; ++i)
+            v[i] = r0 + i < R ? __ldcs(x + (r0 + i) * ldx + c) : 0.0f;
+#pragma unroll
+        for (int i = 0; i < kRepitchRows; ++i)
+            if (r0 + i < R) y[(r0 + i) * ldy + c] = v[i];
+    }
+}
+
 }  // namespace
+
+fgemm_status launch_stage_repitch(const float *X, long long ldx, long long sx, int R, int Cc,
+                                  int batch, float *Y, long long ldy, long long sy,
+                                  cudaStream_t stream)
+{
+    if (R <= 0 || Cc <= 0 || batch <= 0) return FGEMM_OK;
+    const long long gx = ((long long)Cc + kThreads - 1) / kThreads;
+    const long long groups = ((long long)R + kRepitchRows - 1) / kRepitchRows;
+    if (gx > 0x7FFFFFFFLL) return FGEMM_ERR_NOT_SUPPORTED;
+    const unsigned gy = (unsigned)(groups < 65535 ? groups : 65535);
+    for (int b0 = 0; b0 < batch; b0 += 65535) {
+        const int nb = batch - b0 < 65535 ? batch - b0 : 65535;
+        stage_repitch_kernel<<<dim3((unsigned)gx, gy, (unsigned)nb), kThreads, 0, stream>>>(
+            X, ldx, sx, R, Cc, Y, ldy, sy, b0);
+        if (cudaGetLastError() != cudaSuccess) return FGEMM_ERR_LAUNCH;
+    }
+    return FGEMM_OK;
+}
 
 fgemm_status launch_stage_transpose(const float *X, long long ldx, long long sx, int R, int Cc,
                                     int batch, float *Y, long long ldy, long long sy,

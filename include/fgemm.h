@@ -173,30 +173,30 @@ fgemm_status fgemm_sgemm_splitk_noalloc(fgemm_op transa, fgemm_op transb, int M,
  * its stored rows: transpose it or change its layout.  The CUDA-core kernels keep
  * op(A) and op(B) k-major in shared memory, so an operand stored with k contiguous
  * (A for transa == N, B for transb == T) is transposed on its way in, by 4-byte
- * copies in every tile that reads it.  This call can instead copy such an operand
- * once, k-major, into `workspace` (a transpose at HBM speed: 8 bytes moved per
- * element), then run the GEMM on the copy with 16-byte copies only.  On a 152-SM
- * GB300 this pays for large products (4096^3 NN, the 8192 x 4096 x 11008 FC layer,
- * batched Q x K^T) and not for small ones, so by default the launch-time model
- * decides per call.
+ * copies in every tile that reads it, and an operand whose rows do not start on 16
+ * bytes (an odd leading dimension, batch stride or pointer) makes the call take the
+ * element-wise kernel.  This call can instead copy an operand once into `workspace`:
+ * transposed k-major when it is stored with k contiguous, row by row into aligned rows
+ * when it is already k-major (8 bytes moved per element at HBM speed).  The GEMM then
+ * runs on the copies with 16-byte copies only.  On a 152-SM GB300 this pays for large
+ * products (4096^3 NN, the 8192 x 4096 x 11008 FC layer, batched Q x K^T; any unaligned
+ * problem beyond a few hundred per side) and not for small ones, so by default the
+ * launch-time model decides per call.
  *
  * Result: that of fgemm_gemm_explicit with config -1 and the same arguments (strided
  * batch, bias (may be NULL), ReLU), within the same error bound; the sum order can
  * differ from the unstaged call, so the last bits may too.
- *   stage: -1 lets the model choose; otherwise a mask -- bit 0 copies A (only when
- *     transa == N), bit 1 copies B (only when transb == T); bits for an operand that
- *     is already k-major are ignored, and 0 runs the plain kernels.  Anything outside
- *     [-1, 3] returns FGEMM_ERR_INVALID_VALUE.
- *   workspace: caller-owned device memory, 16-byte aligned, at least
- *     fgemm_staged_workspace_size(transa, transb, M, N, K, batch) bytes, not
- *     overlapping A, B, C or bias; its contents are overwritten.  Required whenever
- *     that size is nonzero, the call forms products (K > 0, alpha != 0) and `stage`
- *     allows a copy (-1, or a mask naming an operand stored with k contiguous),
- *     whatever the model then chooses; a missing, misaligned or too small workspace
- *     returns FGEMM_ERR_INVALID_VALUE before anything is launched.  With nothing to
- *     copy it may be NULL.  An operand a batch shares (stride 0) is copied once.
- *   Any alignment of A and B is accepted: the copies are always 16-byte aligned, so
- *   staging also lets unaligned operands use the vector kernels.
+ *   stage: -1 lets the model choose among the copies that fit in the workspace (none
+ *     when workspace is NULL or too small for any); otherwise a mask of the copies to
+ *     make -- bit 0 copies A, bit 1 copies B, 0 runs the plain kernels -- whose bytes
+ *     must fit (else FGEMM_ERR_INVALID_VALUE).  Anything outside [-1, 3] returns
+ *     FGEMM_ERR_INVALID_VALUE.
+ *   workspace: caller-owned device memory, 16-byte aligned (else
+ *     FGEMM_ERR_INVALID_VALUE), not overlapping A, B, C or bias; `workspace_bytes` of it
+ *     may be overwritten.  fgemm_staged_workspace_size(transa, transb, M, N, K, batch)
+ *     bytes hold every copy the call could make (both operands); less limits the
+ *     model's choice.  An operand a batch shares (stride 0) is copied once.
+ *   Checks happen before anything is launched.
  * A staged call launches on `stream` one copy kernel per copied operand (and per 65535
  * problems of a batch), then the GEMM's launches (fgemm_launch_count of the layout the
  * copies leave); it may be captured in a CUDA graph.  Other rules as for
@@ -213,15 +213,16 @@ fgemm_status fgemm_sgemm_staged(fgemm_op transa, fgemm_op transb, int M, int N, 
                                 size_t workspace_bytes, cudaStream_t stream);
 
 /*
- * The mask fgemm_sgemm_staged(stage = -1) would use on a GPU with `num_sms` SMs:
- * bit 0 set when it copies A, bit 1 when it copies B, 0 when it runs the plain
- * kernels.  shared_a / shared_b: nonzero when the batch shares the operand (its stride
- * is 0); aligned_a / aligned_b: nonzero when the operand as stored is 16-byte aligned
- * (pointer, leading dimension and batch stride).  -1 for arguments out of range.
- * Host-only: no CUDA call is made.
+ * The mask fgemm_sgemm_staged(stage = -1) would use on a GPU with `num_sms` SMs and a
+ * workspace of `workspace_bytes`: bit 0 set when it copies A, bit 1 when it copies B, 0
+ * when it runs the plain kernels.  shared_a / shared_b: nonzero when the batch shares the
+ * operand (its stride is 0); aligned_a / aligned_b: nonzero when the operand as stored
+ * is 16-byte aligned (pointer, leading dimension and batch stride).  -1 for arguments
+ * out of range.  Host-only: no CUDA call is made.
  */
 int fgemm_staged_choice(fgemm_op transa, fgemm_op transb, int M, int N, int K, int batch,
-                        int shared_a, int shared_b, int aligned_a, int aligned_b, int num_sms);
+                        int shared_a, int shared_b, int aligned_a, int aligned_b,
+                        size_t workspace_bytes, int num_sms);
 
 /*
  * Arithmetic of the contraction (GEMM 优化详解, "进一步优化方向": tensor cores are the

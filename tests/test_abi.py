@@ -237,19 +237,20 @@ def test_noalloc_checks_arguments_before_the_scratch_size():
 
 def test_staged_workspace_size():
     sz = fg.staged_workspace_size
-    # A's k-major copy: K rows of ld4(M) floats a problem; B's after it at 256 bytes
-    assert sz(0, 0, 4096, 4096, 4096, 1) == 4096 * 4096 * 4
-    assert sz(0, 0, 5, 7, 3, 2) == 2 * 3 * 8 * 4  # ld4(5) = 8
-    a = 2 * 3 * 8 * 4
-    assert sz(0, 1, 5, 7, 3, 2) == (a + 255) // 256 * 256 + 2 * 3 * 8 * 4  # ld4(7) = 8
-    assert sz(1, 1, 5, 7, 3, 2) == 2 * 3 * 8 * 4  # B only
-    assert sz(1, 0, 4096, 4096, 4096, 1) == 0  # both operands already k-major
+    # room for a copy of each operand: K rows of ld4(M) (A) and of ld4(N) (B) floats a
+    # problem, B's at the next multiple of 256 bytes
+    assert sz(0, 0, 4096, 4096, 4096, 1) == 2 * 4096 * 4096 * 4
+    a = 2 * 3 * 8 * 4  # ld4(5) = 8, two problems, K = 3
+    b = 2 * 3 * 8 * 4  # ld4(7) = 8
+    for ta in (0, 1):
+        for tb in (0, 1):
+            assert sz(ta, tb, 5, 7, 3, 2) == (a + 255) // 256 * 256 + b
     for bad in ((0, 0, -1, 4, 4, 1), (0, 0, 4, 4, 0, 1), (0, 0, 4, 4, 4, 0), (2, 0, 4, 4, 4, 1)):
         assert sz(*bad) == 0
 
 
 def test_staged_choice_host_query():
-    ch = fg.staged_choice
+    ch = fg.staged_choice  # the last argument, when given, is the workspace size
     # the model on 152 SMs: copy where the 16-byte-copy layout repays the copy
     assert ch(0, 0, 4096, 4096, 4096, 1, 0, 0, 1, 1, 152) == 1
     assert ch(0, 1, 4096, 4096, 4096, 1, 0, 0, 1, 1, 152) == 3
@@ -258,26 +259,32 @@ def test_staged_choice_host_query():
     assert ch(0, 1, 2048, 2048, 128, 128, 0, 0, 1, 1, 152) == 3
     assert ch(0, 0, 2048, 128, 2048, 128, 0, 0, 1, 1, 152) == 0
     assert ch(0, 0, 1024, 1024, 1024, 1, 0, 0, 1, 1, 152) == 0
-    # unaligned A: copying it is the way to the 16-byte kernels for all but small
-    # problems; up to 256^3 the element-wise kernel is as fast as the copy plus the vector
-    # kernel (measured 15.0 against about 14 us at 256^3, 8.9 against 11 at 64^3)
+    # unaligned operands: copying them (a transpose, or aligned rows for a k-major one)
+    # is the way to the 16-byte kernels for all but small problems; up to 256^3 the
+    # element-wise kernel is as fast (measured 15.0 against about 14 us at 256^3)
     assert ch(0, 0, 1024, 1024, 1024, 1, 0, 0, 0, 1, 152) == 1
-    assert ch(0, 0, 4096, 4096, 4096, 1, 0, 0, 0, 1, 152) == 1
+    assert ch(0, 0, 4096, 4096, 4096, 1, 0, 0, 0, 0, 152) == 3
+    assert ch(1, 0, 4096, 4096, 4096, 1, 0, 0, 0, 1, 152) == 1  # A re-pitched
+    assert ch(1, 0, 4096, 4096, 4096, 1, 0, 0, 1, 0, 152) == 2  # B re-pitched
     assert ch(0, 0, 256, 256, 256, 1, 0, 0, 0, 1, 152) == 0
-    assert ch(0, 0, 64, 64, 64, 1, 0, 0, 0, 1, 152) == 0
-    # ... but not when the other operand (not copied in this layout) is unaligned too
-    assert ch(1, 1, 4096, 4096, 4096, 1, 0, 0, 0, 1, 152) == 0
+    assert ch(0, 0, 64, 64, 64, 1, 0, 0, 0, 0, 152) == 0
     # a batch-shared operand is copied once: cheaper, so copied at least as readily
     assert ch(0, 0, 2048, 128, 2048, 128, 1, 0, 1, 1, 152) == 1
+    # the workspace bounds the choice: 64 MiB holds the copy of A at 4096^3, not the
+    # 128 MiB copies of Q or K of the QK^T batch
+    assert ch(0, 0, 4096, 4096, 4096, 1, 0, 0, 1, 1, 152, 64 << 20) == 1
+    assert ch(0, 0, 4096, 4096, 4096, 1, 0, 0, 1, 1, 152, (64 << 20) - 4) == 0
+    assert ch(0, 1, 2048, 2048, 128, 128, 0, 0, 1, 1, 152, 64 << 20) == 0
+    assert ch(0, 0, 4096, 4096, 4096, 1, 0, 0, 0, 0, 152, 0) == 0
     assert ch(0, 0, 0, 4, 4, 1, 0, 0, 1, 1, 152) == 0
-    assert ch(0, 0, -1, 4, 4, 1, 0, 0, 1, 1, 152) == -1
-    assert ch(0, 0, 4, 4, 4, 1, 0, 0, 1, 1, 0) == -1
+    assert ch(0, 0, -1, 4, 4, 1, 0, 0, 1, 1, 152, 0) == -1
+    assert ch(0, 0, 4, 4, 4, 1, 0, 0, 1, 1, 0, 1 << 20) == -1
 
 
 @pytest.mark.parametrize("kw", [dict(stage=4), dict(stage=-2), dict(M=-1), dict(lda=1),
-                                dict(workspace=0), dict(workspace_bytes=16),
-                                dict(workspace=FAKE + 4), dict(workspace=0, stage=1),
-                                dict(workspace=0, stage=3), dict(workspace_bytes=16, stage=2)])
+                                dict(workspace=FAKE + 4), dict(workspace=FAKE + 8, stage=0),
+                                dict(workspace=0, stage=1), dict(workspace=0, stage=3),
+                                dict(workspace_bytes=16, stage=2)])
 def test_staged_validates_before_launch(kw):
     args = dict(ta=0, tb=1, M=64, N=64, K=64, lda=64, workspace=FAKE, stage=fg.STAGE_AUTO)
     args.update(kw)

@@ -63,6 +63,7 @@ def test_plain_batch_beyond_one_grid_dimension(operands, config):
 
 
 def test_staged_batch_beyond_one_grid_dimension(operands):
+    """Both operands transposed by the copy kernel in chunks of 65535 problems."""
     A, Bt, want = operands
     dA, dB = A.cuda(), Bt.cuda()
     C = torch.full((BATCH, M, N), float("nan"), device="cuda")
@@ -73,3 +74,19 @@ def test_staged_batch_beyond_one_grid_dimension(operands):
                     None, False, 3, ws, need)
     torch.cuda.synchronize()
     _check(C, A, Bt, want, -0.5)
+
+
+def test_repitched_batch_beyond_one_grid_dimension(operands):
+    """Both operands already k-major (op(A) = T, op(B) = N) and copied row by row into
+    aligned rows, in chunks of 65535 problems."""
+    A, Bt, want = operands
+    At = A.transpose(1, 2).contiguous()  # K x M: op(A) = T
+    Bk = Bt.transpose(1, 2).contiguous()  # K x N: op(B) = N
+    dA, dB = At.cuda(), Bk.cuda()
+    C = torch.full((BATCH, M, N), float("nan"), device="cuda")
+    need = fg.staged_workspace_size(1, 0, M, N, K, BATCH)
+    ws = torch.full((need // 4,), float("nan"), device="cuda")
+    fg.sgemm_staged(1, 0, M, N, K, 1.0, dA, M, M * K, dB, N, N * K, 0.0, C, N, M * N, BATCH,
+                    None, False, 3, ws, need)
+    torch.cuda.synchronize()
+    _check(C, A, Bt, want, 1.0)

@@ -1,13 +1,14 @@
 """fgemm_sgemm_staged against the FP64 oracle.
 
-The call copies the operands stored with k contiguous (A for op N, B for op T) into a
-caller workspace in k-major order and runs the GEMM on the copies (GEMM 优化详解,
-"Level 1: Naive 实现": re-store an operand that is read across its rows).  Checked
-here, through the C ABI: every transpose layout with every staging mask and the
-model's own choice, ragged sizes over several tiles, strided batches with and without
-a shared operand, unaligned operands (the copies are aligned, so the vector kernels
-run), alpha = 0 and K = 0 (no copies, no workspace read), beta = 0 over a NaN C,
-replay in a CUDA graph, and the argument checks.  Integer data must come back
+The call copies operands into a caller workspace -- transposed k-major when stored with
+k contiguous (A for op N, B for op T), row by row into aligned rows when already
+k-major -- and runs the GEMM on the copies (GEMM 优化详解, "Level 1: Naive 实现":
+re-store an operand that is read across its rows).  Checked here, through the C ABI:
+every transpose layout with every copy mask and the model's own choice, ragged sizes
+over several tiles, strided batches with and without a shared operand, unaligned
+operands (the copies are aligned, so the vector kernels run), alpha = 0 and K = 0 (no
+copies, no workspace read), beta = 0 over a NaN C, replay in a CUDA graph, a workspace
+that bounds the model's choice, and the argument checks.  Integer data must come back
 bit-exact, uniform data within 1e-5 * mag; the harness fills the workspace with NaN,
 so any element the GEMM read before the copy wrote it would show.
 """
@@ -128,38 +129,42 @@ def test_argument_checks_launch_nothing():
     A = torch.ones(M, K, device="cuda")
     B = torch.ones(K, N, device="cuda")
     C = torch.full((M, N), 7.0, device="cuda")
-    need = fg.staged_workspace_size(0, 0, M, N, K, 1)
-    assert need == K * M * 4
-    ws = torch.empty(need // 4 + 4, device="cuda")
+    need_a = K * M * 4  # the copy of A alone
+    ws = torch.empty(need_a // 4 + 4, device="cuda")
     bad = [
-        dict(workspace=None, workspace_bytes=need),
-        dict(workspace=ws, workspace_bytes=need - 4),
-        dict(workspace=ws.data_ptr() + 4, workspace_bytes=need),
-        dict(workspace=ws, workspace_bytes=need, stage=4),
-        dict(workspace=ws, workspace_bytes=need, stage=-2),
+        dict(workspace=None, workspace_bytes=0, stage=1),  # forced copies need room
+        dict(workspace=ws, workspace_bytes=need_a - 4, stage=1),
+        dict(workspace=ws, workspace_bytes=need_a, stage=3),  # A fits, B does not
+        dict(workspace=ws.data_ptr() + 4, workspace_bytes=need_a, stage=-1),  # misaligned
+        dict(workspace=ws, workspace_bytes=need_a, stage=4),
+        dict(workspace=ws, workspace_bytes=need_a, stage=-2),
     ]
     for kw in bad:
-        args = dict(stage=fg.STAGE_AUTO)
-        args.update(kw)
         st = fg.sgemm_staged(0, 0, M, N, K, 1.0, A, K, 0, B, N, 0, 0.0, C, N, 0, 1, None, False,
-                             args["stage"], args["workspace"], args["workspace_bytes"],
-                             check=False)
+                             kw["stage"], kw["workspace"], kw["workspace_bytes"], check=False)
         assert st == fg.ERR_INVALID_VALUE, kw
     torch.cuda.synchronize()
     assert bool((C == 7.0).all())
-    # stage = 0, or a mask naming only operands already k-major: no copy, no workspace
-    for stage, ta in ((0, 0), (2, 0)):
+    # the model's choice within whatever workspace there is: none at all, or one that
+    # holds only the copy of A; stage = 0 runs the plain kernels without a workspace
+    for stage, w, wb in ((-1, None, 0), (-1, ws, need_a), (1, ws, need_a), (0, None, 0)):
         C.fill_(7.0)
-        fg.sgemm_staged(ta, 0, M, N, K, 1.0, A, K, 0, B, N, 0, 0.0, C, N, 0, 1, None, False,
-                        stage, None, 0)
+        fg.sgemm_staged(0, 0, M, N, K, 1.0, A, K, 0, B, N, 0, 0.0, C, N, 0, 1, None, False,
+                        stage, w, wb)
         torch.cuda.synchronize()
-        assert bool((C == float(K)).all())
-    # op(A) = T, op(B) = N needs no copy and no workspace
-    assert fg.staged_workspace_size(1, 0, M, N, K, 1) == 0
-    fg.sgemm_staged(1, 0, M, N, K, 1.0, A, M, 0, B, N, 0, 0.0, C, N, 0, 1, None, False,
-                    fg.STAGE_AUTO, None, 0)
-    torch.cuda.synchronize()
-    assert bool((C == float(K)).all())
+        assert bool((C == float(K)).all()), (stage, wb)
+
+
+@pytest.mark.parametrize("ta,tb", COMBOS)
+def test_unaligned_operands_copied_by_the_model(ta, tb):
+    # 1200^3 with odd leading dimensions: the model copies both operands (transposing the
+    # k-contiguous ones, re-pitching the k-major ones into aligned rows)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms == 152:
+        assert fg.staged_choice(ta, tb, 1200, 1200, 1200, 1, False, False, False, False,
+                                sms) == 3
+    check(Case(ta=ta, tb=tb, M=1200, N=1200, K=1200, alpha=1.0, beta=0.5, bias=True,
+               align_ld=False, pad=(1, 1, 0), stage=fg.STAGE_AUTO, seed=170 + 2 * ta + tb))
 
 
 def test_model_choice_on_this_gpu():
