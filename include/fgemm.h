@@ -195,7 +195,9 @@ fgemm_status fgemm_sgemm_splitk_noalloc(fgemm_op transa, fgemm_op transb, int M,
  *     FGEMM_ERR_INVALID_VALUE), not overlapping A, B, C or bias; `workspace_bytes` of it
  *     may be overwritten.  fgemm_staged_workspace_size(transa, transb, M, N, K, batch)
  *     bytes hold every copy the call could make (both operands); less limits the
- *     model's choice.  An operand a batch shares (stride 0) is copied once.
+ *     model's choice.  An operand a batch shares (stride 0) is copied once.  Staged calls
+ *     whose kernels may overlap on the GPU (other streams, other host threads) need
+ *     workspaces of their own; calls on one stream may share one.
  *   Checks happen before anything is launched.
  * A staged call launches on `stream` one copy kernel per copied operand (and per 65535
  * problems of a batch), then the GEMM's launches (fgemm_launch_count of the layout the
