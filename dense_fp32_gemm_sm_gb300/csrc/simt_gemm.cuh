@@ -524,7 +524,9 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
     }
     const float *const A = p.A + bz * p.strideA + a_koff;
     const float *const B = p.B + bz * p.strideB + b_koff;
-    float *const C = p.C + bz * p.strideC;
+    // The quarter tiles form their C pointer after the main loop (measured: it frees
+    // the 24 B of spill space the TN instance needed); the other maps here.
+    float *const C_early = MAP == TILE_QUARTER ? nullptr : p.C + bz * p.strideC;
 
     float2 acc[TM][TN / 2];  // acc[i][j] = (c[i][2j], c[i][2j+1])
 #pragma unroll
@@ -602,6 +604,8 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
         }
         cp_async_wait<0>();
     }
+
+    float *const C = MAP == TILE_QUARTER ? p.C + bz * p.strideC : C_early;
 
     // ---- K-groups: groups 1.. hand their sums to group 0 through shared memory
     // (the stage buffers are free once every warp has passed the barrier), in

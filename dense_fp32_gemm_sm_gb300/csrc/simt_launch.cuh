@@ -57,12 +57,13 @@ struct ConfigOf<CFG_32x32_K4, TA, TB> {
 // The quarter tiles of the last-wave split: 64 x 64 with four k-groups of two
 // warps (8 x 8 per thread), so a quarter tile has the CTA size, register budget and
 // per-thread tile of a 128 x 128 tile and a quarter of its serial k-steps.  64-deep
-// stages give each k-group 16 k per stage; when both operands are transposed on
-// copy, 32-deep stages keep the element copies per thread at 16.
+// stages give each k-group 16 k per stage; when B is transposed on copy (NT, TT),
+// 32-deep stages keep its element copies per thread at 16 (at 64 deep the TT instance
+// needed 8 B of spill space).
 template <int TA, int TB>
 struct SplitTailOf {
-    static constexpr bool BOTH_T = (TA == 0 && TB == 1);
-    using type = SimtCfg<64, 64, BOTH_T ? 32 : 64, 64, 32, 8, 8, BOTH_T ? 4 : 3, 2, TA, TB, true, 4>;
+    static constexpr bool B_T = TB == 1;
+    using type = SimtCfg<64, 64, B_T ? 32 : 64, 64, 32, 8, 8, B_T ? 4 : 3, 2, TA, TB, true, 4>;
 };
 
 // Opt a kernel in to its dynamic shared memory once per context (attributes belong to
@@ -93,6 +94,15 @@ static cudaError_t prepare_kernel()
     return prepare_kernel_fn<Cfg>(simt_gemm_kernel<Cfg>, Cfg::SMEM_BYTES);
 }
 
+// Whole 128 x 128 tiles of TT problems always run in the one-dimensional linear tile
+// order (the same grouped order within each problem as TILE_GRID): with TILE_GRID's
+// index arithmetic that instance needs 12 B of spill space at its 128-register budget,
+// with TILE_LINEAR's none (ptxas; register allocation at the budget moves with small
+// code changes).
+template <class Cfg>
+constexpr bool kLinearWhole = Cfg::TA == 1 && Cfg::TB == 1 && Cfg::BM == 128 &&
+                              Cfg::BN == 128 && Cfg::KS == 1;
+
 template <class Cfg>
 static fgemm_status launch_simt(const GemmParams &p0, int batch, cudaStream_t stream)
 {
@@ -101,24 +111,38 @@ static fgemm_status launch_simt(const GemmParams &p0, int batch, cudaStream_t st
     p.tiles_n = (p.N + Cfg::BN - 1) / Cfg::BN;
     const long long tiles = (long long)p.tiles_m * p.tiles_n;
     if (tiles > INT_MAX) return FGEMM_ERR_NOT_SUPPORTED;
-    if (prepare_kernel<Cfg>() != cudaSuccess) {
-        (void)cudaGetLastError();
-        return FGEMM_ERR_LAUNCH;
-    }
-    const int kMaxZ = 65535;
-    for (int b0 = 0; b0 < batch; b0 += kMaxZ) {
-        const int nb = batch - b0 < kMaxZ ? batch - b0 : kMaxZ;
-        GemmParams q = p;
-        if (b0) {
-            if (q.A) q.A += (long long)b0 * q.strideA;
-            if (q.B) q.B += (long long)b0 * q.strideB;
-            q.C += (long long)b0 * q.strideC;
+    if constexpr (kLinearWhole<Cfg>) {
+        struct LinearTag {};
+        const long long units = tiles * batch;
+        if (units > INT_MAX) return FGEMM_ERR_NOT_SUPPORTED;
+        if (prepare_kernel_fn<LinearTag>(simt_gemm_kernel<Cfg, TILE_LINEAR>, Cfg::SMEM_BYTES) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();
+            return FGEMM_ERR_LAUNCH;
         }
-        simt_gemm_kernel<Cfg><<<dim3((unsigned)tiles, 1, (unsigned)nb), Cfg::THREADS,
-                                Cfg::SMEM_BYTES, stream>>>(q);
-        if (cudaGetLastError() != cudaSuccess) return FGEMM_ERR_LAUNCH;
+        simt_gemm_kernel<Cfg, TILE_LINEAR><<<(unsigned)units, Cfg::THREADS, Cfg::SMEM_BYTES,
+                                             stream>>>(p);
+        return cudaGetLastError() == cudaSuccess ? FGEMM_OK : FGEMM_ERR_LAUNCH;
+    } else {
+        if (prepare_kernel<Cfg>() != cudaSuccess) {
+            (void)cudaGetLastError();
+            return FGEMM_ERR_LAUNCH;
+        }
+        const int kMaxZ = 65535;
+        for (int b0 = 0; b0 < batch; b0 += kMaxZ) {
+            const int nb = batch - b0 < kMaxZ ? batch - b0 : kMaxZ;
+            GemmParams q = p;
+            if (b0) {
+                if (q.A) q.A += (long long)b0 * q.strideA;
+                if (q.B) q.B += (long long)b0 * q.strideB;
+                q.C += (long long)b0 * q.strideC;
+            }
+            simt_gemm_kernel<Cfg><<<dim3((unsigned)tiles, 1, (unsigned)nb), Cfg::THREADS,
+                                    Cfg::SMEM_BYTES, stream>>>(q);
+            if (cudaGetLastError() != cudaSuccess) return FGEMM_ERR_LAUNCH;
+        }
+        return FGEMM_OK;
     }
-    return FGEMM_OK;
 }
 
 // Plan of a last-wave split over Main-sized tiles: tile counts, the whole tiles of
@@ -149,19 +173,27 @@ template <class Main>
 static fgemm_status launch_whole_tiles(const GemmParams &p, int batch, cudaStream_t stream)
 {
     struct LinearTag {};
-    if (prepare_kernel<Main>() != cudaSuccess ||
-        prepare_kernel_fn<LinearTag>(simt_gemm_kernel<Main, TILE_LINEAR>, Main::SMEM_BYTES) !=
-            cudaSuccess) {
+    if constexpr (!kLinearWhole<Main>) {
+        if (prepare_kernel<Main>() != cudaSuccess) {
+            (void)cudaGetLastError();
+            return FGEMM_ERR_LAUNCH;
+        }
+    }
+    if (prepare_kernel_fn<LinearTag>(simt_gemm_kernel<Main, TILE_LINEAR>, Main::SMEM_BYTES) !=
+        cudaSuccess) {
         (void)cudaGetLastError();
         return FGEMM_ERR_LAUNCH;
     }
     if (p.full_units <= 0) return FGEMM_OK;
-    if (batch == 1)
-        simt_gemm_kernel<Main><<<(unsigned)p.full_units, Main::THREADS, Main::SMEM_BYTES,
-                                 stream>>>(p);
-    else
-        simt_gemm_kernel<Main, TILE_LINEAR><<<(unsigned)p.full_units, Main::THREADS,
-                                             Main::SMEM_BYTES, stream>>>(p);
+    if constexpr (!kLinearWhole<Main>) {
+        if (batch == 1) {
+            simt_gemm_kernel<Main><<<(unsigned)p.full_units, Main::THREADS, Main::SMEM_BYTES,
+                                     stream>>>(p);
+            return cudaGetLastError() == cudaSuccess ? FGEMM_OK : FGEMM_ERR_LAUNCH;
+        }
+    }
+    simt_gemm_kernel<Main, TILE_LINEAR><<<(unsigned)p.full_units, Main::THREADS,
+                                         Main::SMEM_BYTES, stream>>>(p);
     return cudaGetLastError() == cudaSuccess ? FGEMM_OK : FGEMM_ERR_LAUNCH;
 }
 
