@@ -75,7 +75,7 @@ def parse_args(argv=None):
                          "plain entry points")
     ap.add_argument("--config", type=int, default=-1,
                     help="explicit kernel configuration id (default: the library's choice)")
-    ap.add_argument("--e2e-steps", type=int, default=50,
+    ap.add_argument("--e2e-steps", type=int, default=100,
                     help="pipelined end-to-end steps timed (the first inputs and the last "
                          "result are not overlapped; more steps amortise them)")
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
