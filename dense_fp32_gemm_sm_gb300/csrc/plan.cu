@@ -9,6 +9,7 @@
 
 #include <atomic>
 #include <cmath>
+#include <cstdint>
 
 #include "fgemm_internal.h"
 
@@ -222,12 +223,21 @@ double stage_copy_us(long long R, long long Cc, long long problems)
     return kStageLaunchUs + bytes / kStageBytesPerUs;
 }
 
+// Saturating products and sums: sizes no allocation could hold come out as SIZE_MAX,
+// so they never pass a workspace check by wrapping around.
+static size_t sat_mul(size_t a, size_t b) { return (b != 0 && a > SIZE_MAX / b) ? SIZE_MAX : a * b; }
+static size_t sat_add(size_t a, size_t b) { return a > SIZE_MAX - b ? SIZE_MAX : a + b; }
+
 size_t stage_bytes(int mask, long long M, long long N, long long K, long long problems_a,
                    long long problems_b)
 {
-    const size_t a = (mask & 1) ? (size_t)problems_a * (size_t)K * (size_t)((M + 3) / 4 * 4) * 4 : 0;
-    const size_t b = (mask & 2) ? (size_t)problems_b * (size_t)K * (size_t)((N + 3) / 4 * 4) * 4 : 0;
-    return b == 0 ? a : (a + 255) / 256 * 256 + b;
+    const auto copy = [&](long long rows, long long problems) {
+        return sat_mul(sat_mul(sat_mul((size_t)problems, (size_t)K), (size_t)((rows + 3) / 4 * 4)),
+                       sizeof(float));
+    };
+    const size_t a = (mask & 1) ? copy(M, problems_a) : 0;
+    const size_t b = (mask & 2) ? copy(N, problems_b) : 0;
+    return b == 0 ? a : sat_add(sat_add(a, 255) / 256 * 256, b);
 }
 
 int staging_choice(int ta, int tb, long long M, long long N, long long K, long long batch,

@@ -247,6 +247,9 @@ def test_staged_workspace_size():
             assert sz(ta, tb, 5, 7, 3, 2) == (a + 255) // 256 * 256 + b
     for bad in ((0, 0, -1, 4, 4, 1), (0, 0, 4, 4, 0, 1), (0, 0, 4, 4, 4, 0), (2, 0, 4, 4, 4, 1)):
         assert sz(*bad) == 0
+    # sizes no allocation could hold saturate instead of wrapping around
+    big = 2**31 - 1
+    assert sz(0, 0, big, big, big, big) == 2**64 - 1
 
 
 def test_staged_choice_host_query():
