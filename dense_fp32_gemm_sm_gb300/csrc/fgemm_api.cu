@@ -211,7 +211,7 @@ fgemm_status run_splitk(const Problem &p, int splits, float *W, size_t ws_bytes)
     const long long Ks = splitk_slice(p.K, splits);
     const int S = (int)((p.K + Ks - 1) / Ks);  // slices actually used
     const long long slice = (long long)p.M * p.N;
-    if (W == nullptr || ws_bytes < (size_t)S * (size_t)slice * sizeof(float))
+    if (W == nullptr || ws_bytes < sat_mul(sat_mul((size_t)S, (size_t)slice), sizeof(float)))
         return FGEMM_ERR_INVALID_VALUE;
     // Offsets of one K slice in A and B.
     const long long dA = p.ta ? Ks * p.lda : Ks;
@@ -373,7 +373,7 @@ fgemm_status splitk_plan(int ta, int tb, int M, int N, int K, float alpha, const
     if (splits == 1 || !products) return FGEMM_OK;
     const long long Ks = splitk_slice(p.K, splits);
     const long long S = (p.K + Ks - 1) / Ks;
-    *workspace_bytes = (size_t)S * (size_t)p.M * (size_t)p.N * sizeof(float);
+    *workspace_bytes = sat_mul(sat_mul(sat_mul((size_t)S, (size_t)p.M), (size_t)p.N), sizeof(float));
     return FGEMM_OK;
 }
 
@@ -463,7 +463,8 @@ size_t fgemm_splitk_workspace_size(int M, int N, int K, int splits)
     if (K == 0) return 0;
     const long long Ks = fgemm::splitk_slice(K, splits);
     const long long S = (K + Ks - 1) / Ks;
-    return (size_t)S * (size_t)M * (size_t)N * sizeof(float);
+    return fgemm::sat_mul(fgemm::sat_mul(fgemm::sat_mul((size_t)S, (size_t)M), (size_t)N),
+                          sizeof(float));
 }
 
 fgemm_status fgemm_sgemm_splitk(fgemm_op transa, fgemm_op transb, int M, int N, int K, float alpha,

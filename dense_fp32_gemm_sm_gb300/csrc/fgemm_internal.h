@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cstddef>
+#include <cstdint>
 
 #include "fgemm.h"
 
@@ -53,6 +54,11 @@ int kchain_slices(int ta, int tb, long long r, long long K, int num_sms);
 // The configuration for a problem (host-only; see fgemm_select_config).
 int select_config(int ta, int tb, long long M, long long N, long long K, long long batch,
                   bool aligned, int num_sms);
+
+// Saturating size arithmetic: sizes no allocation could hold come out as SIZE_MAX, so
+// they never pass a workspace check by wrapping around.
+inline size_t sat_mul(size_t a, size_t b) { return (b != 0 && a > SIZE_MAX / b) ? SIZE_MAX : a * b; }
+inline size_t sat_add(size_t a, size_t b) { return a > SIZE_MAX - b ? SIZE_MAX : a + b; }
 
 // Bytes of the workspace copies a staged call makes with `mask` (bit 0: A, bit 1: B): each
 // copy is K x ld4(rows) floats a problem (ld4: rounded up to a multiple of 4), B's starting

@@ -223,11 +223,6 @@ double stage_copy_us(long long R, long long Cc, long long problems)
     return kStageLaunchUs + bytes / kStageBytesPerUs;
 }
 
-// Saturating products and sums: sizes no allocation could hold come out as SIZE_MAX,
-// so they never pass a workspace check by wrapping around.
-static size_t sat_mul(size_t a, size_t b) { return (b != 0 && a > SIZE_MAX / b) ? SIZE_MAX : a * b; }
-static size_t sat_add(size_t a, size_t b) { return a > SIZE_MAX - b ? SIZE_MAX : a + b; }
-
 size_t stage_bytes(int mask, long long M, long long N, long long K, long long problems_a,
                    long long problems_b)
 {

@@ -167,6 +167,8 @@ def test_splitk_workspace_size():
     assert fg.splitk_workspace_size(-1, 8, 64, 4) == 0
     assert fg.splitk_workspace_size(4, 8, 64, 0) == 0
     assert fg.splitk_workspace_size(4, 8, 64, 65) == 0
+    # sizes no allocation could hold saturate instead of wrapping around
+    assert fg.splitk_workspace_size(2**31 - 1, 2**31 - 1, 2**31 - 1, 64) == 2**64 - 1
 
 
 def test_splitk_rejects_missing_workspace_before_launch():
