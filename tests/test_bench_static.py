@@ -51,6 +51,9 @@ def test_launch_count():
     # the per-problem grid splits a batch into chunks of 65535 problems
     assert lc(cfg["simt_32x32x16_t4x4_s4"], 0, 0, 64, 64, 64, 65535, True, 152) == 1
     assert lc(cfg["simt_32x32x16_t4x4_s4"], 0, 0, 64, 64, 64, 65536, True, 152) == 2
+    assert lc(cfg["simt_128x128_t8x8"], 0, 0, 64, 64, 64, 65536, True, 152) == 2
+    # TT whole tiles: one launch in the linear tile order, whatever the batch
+    assert lc(cfg["simt_128x128_t8x8"], 1, 1, 64, 64, 64, 65536, True, 152) == 1
     # selection, empty problems and bad arguments
     assert lc(-1, 0, 0, 4096, 4096, 4096, 1, True, 152) == 5
     assert lc(-1, 0, 0, 0, 4096, 4096, 1, True, 152) == 0
