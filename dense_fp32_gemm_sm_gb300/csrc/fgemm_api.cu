@@ -562,9 +562,13 @@ int fgemm_launch_count(int config, fgemm_op transa, fgemm_op transb, int M, int 
                              : 1;
         return (total - r > 0 ? 1 : 0) + (r > 0 ? tail : 0);
     }
-    // TT whole 128 x 128 tiles run in one linear-order launch; the other configurations
-    // in one launch per 65535 problems
-    if (config == fgemm::CFG_128x128 && transa == FGEMM_OP_T && transb == FGEMM_OP_T) return 1;
+    // TT whole 128 x 128 tiles run in linear-order launches of up to INT_MAX CTAs; the
+    // other configurations in one launch per 65535 problems
+    if (config == fgemm::CFG_128x128 && transa == FGEMM_OP_T && transb == FGEMM_OP_T) {
+        const long long tiles = (long long)((M + 127) / 128) * ((N + 127) / 128);
+        const long long per_launch = INT_MAX / tiles;
+        return (int)((batch + per_launch - 1) / per_launch);
+    }
     return (batch + 65534) / 65535;
 }
 

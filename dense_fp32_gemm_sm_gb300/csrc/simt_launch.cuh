@@ -113,16 +113,26 @@ static fgemm_status launch_simt(const GemmParams &p0, int batch, cudaStream_t st
     if (tiles > INT_MAX) return FGEMM_ERR_NOT_SUPPORTED;
     if constexpr (kLinearWhole<Cfg>) {
         struct LinearTag {};
-        const long long units = tiles * batch;
-        if (units > INT_MAX) return FGEMM_ERR_NOT_SUPPORTED;
         if (prepare_kernel_fn<LinearTag>(simt_gemm_kernel<Cfg, TILE_LINEAR>, Cfg::SMEM_BYTES) !=
             cudaSuccess) {
             (void)cudaGetLastError();
             return FGEMM_ERR_LAUNCH;
         }
-        simt_gemm_kernel<Cfg, TILE_LINEAR><<<(unsigned)units, Cfg::THREADS, Cfg::SMEM_BYTES,
-                                             stream>>>(p);
-        return cudaGetLastError() == cudaSuccess ? FGEMM_OK : FGEMM_ERR_LAUNCH;
+        // One launch of tiles x batch CTAs, in chunks of problems when that exceeds a grid.
+        const long long per_launch = INT_MAX / tiles;
+        for (long long b0 = 0; b0 < batch; b0 += per_launch) {
+            const long long nb = batch - b0 < per_launch ? batch - b0 : per_launch;
+            GemmParams q = p;
+            if (b0) {
+                if (q.A) q.A += b0 * q.strideA;
+                if (q.B) q.B += b0 * q.strideB;
+                q.C += b0 * q.strideC;
+            }
+            simt_gemm_kernel<Cfg, TILE_LINEAR><<<(unsigned)(tiles * nb), Cfg::THREADS,
+                                                 Cfg::SMEM_BYTES, stream>>>(q);
+            if (cudaGetLastError() != cudaSuccess) return FGEMM_ERR_LAUNCH;
+        }
+        return FGEMM_OK;
     } else {
         if (prepare_kernel<Cfg>() != cudaSuccess) {
             (void)cudaGetLastError();

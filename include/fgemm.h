@@ -336,7 +336,7 @@ int fgemm_select_config(fgemm_op transa, fgemm_op transb, int M, int N, int K, i
 /*
  * Kernel launches one call with this configuration (config < 0: the one the plain entry
  * points would select) makes on a GPU with `num_sms` SMs: 1 for most configurations (1
- * per 65535 problems of a batch; TT whole 128 x 128 tiles 1 for any batch), and for the
+ * per 65535 problems of a batch; TT whole 128 x 128 tiles 1 per 2^31 - 1 tiles), and for the
  * last-wave configurations one for the
  * whole tiles (if any) plus one for the last (tiles mod SMs) tiles -- or, for
  * "..._kchain", one per k-slice (2 to 8, chosen from the remainder and K).  K is the

@@ -52,8 +52,9 @@ def test_launch_count():
     assert lc(cfg["simt_32x32x16_t4x4_s4"], 0, 0, 64, 64, 64, 65535, True, 152) == 1
     assert lc(cfg["simt_32x32x16_t4x4_s4"], 0, 0, 64, 64, 64, 65536, True, 152) == 2
     assert lc(cfg["simt_128x128_t8x8"], 0, 0, 64, 64, 64, 65536, True, 152) == 2
-    # TT whole tiles: one launch in the linear tile order, whatever the batch
+    # TT whole tiles: linear-order launches of up to 2^31 - 1 CTAs
     assert lc(cfg["simt_128x128_t8x8"], 1, 1, 64, 64, 64, 65536, True, 152) == 1
+    assert lc(cfg["simt_128x128_t8x8"], 1, 1, 256, 256, 64, 2**29, True, 152) == 2  # 4 tiles a problem
     # selection, empty problems and bad arguments
     assert lc(-1, 0, 0, 4096, 4096, 4096, 1, True, 152) == 5
     assert lc(-1, 0, 0, 0, 4096, 4096, 1, True, 152) == 0
