@@ -246,14 +246,16 @@ int staging_choice(int ta, int tb, long long M, long long N, long long K, long l
     if (useful == 0) return 0;
     // Every candidate from one estimate: the GEMM with both operands k-major (op(A) = T,
     // op(B) = N) scaled by the layout's measured cost relative to it; with an unaligned
-    // operand left as stored, the 64 x 64 element-wise kernel (measured within 4 % of the
-    // vector 64 x 64 tile from 64^3 to 4096^3, so that tile's model with a 4 % allowance).
+    // operand left as stored, the 64 x 64 element-wise kernel, in any layout (measured
+    // within 4 % of the vector 64 x 64 NN tile from 64^3 to 4096^3; its copies move single
+    // elements whichever way the operands run, so a copy that leaves one operand
+    // unaligned buys nothing).
     int unused = 0;
     const double base = select_config_us(1, 0, M, N, K, batch, true, num_sms, &unused);
+    const double scalar_us =
+        1.04 * model_us(kModel[0][M_64x64], tiles_of(M, N, 64, 64, batch), (double)K, num_sms);
     const auto gemm_us = [&](int a, int b, bool aligned) {
-        if (aligned) return base * kLayoutFactor[(a ? 2 : 0) + (b ? 1 : 0)];
-        const LaunchModel &m64 = kModel[(a ? 2 : 0) + (b ? 1 : 0)][M_64x64];
-        return 1.04 * model_us(m64, tiles_of(M, N, 64, 64, batch), (double)K, num_sms);
+        return aligned ? base * kLayoutFactor[(a ? 2 : 0) + (b ? 1 : 0)] : scalar_us;
     };
     double best_us = gemm_us(ta, tb, aligned_a && aligned_b);
     int best = 0;
