@@ -27,6 +27,7 @@ const ConfigInfo kConfigs[NUM_CONFIGS] = {
     {"simt_128x128_t8x8_split", 128, 128, true},
     {"simt_128x128_t8x8_ksplit", 128, 128, true},
     {"simt_128x128_t8x8_kchain", 128, 128, true},
+    {"simt_128x128_t8x8_scalar", 128, 128, false},
 };
 
 namespace {
@@ -564,7 +565,8 @@ int fgemm_launch_count(int config, fgemm_op transa, fgemm_op transb, int M, int 
     }
     // TT whole 128 x 128 tiles run in linear-order launches of up to INT_MAX CTAs; the
     // other configurations in one launch per 65535 problems
-    if (config == fgemm::CFG_128x128 && transa == FGEMM_OP_T && transb == FGEMM_OP_T) {
+    if ((config == fgemm::CFG_128x128 || config == fgemm::CFG_128x128_SCALAR) &&
+        transa == FGEMM_OP_T && transb == FGEMM_OP_T) {
         const long long tiles = (long long)((M + 127) / 128) * ((N + 127) / 128);
         const long long per_launch = INT_MAX / tiles;
         return (int)((batch + per_launch - 1) / per_launch);

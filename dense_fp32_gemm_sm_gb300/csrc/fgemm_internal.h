@@ -32,7 +32,8 @@ enum ConfigId {
     CFG_128x128_KCHAIN = 8, // CFG_128x128 for all but the last (tiles mod SMs) tiles, which
                             // then run as 2..8 k-slices of whole tiles, one launch each,
                             // added into C in slice order (programmatic dependent launches)
-    NUM_CONFIGS = 9,
+    CFG_128x128_SCALAR = 9, // CFG_128x128 with element-wise copies: any alignment
+    NUM_CONFIGS = 10,
 };
 
 struct ConfigInfo {

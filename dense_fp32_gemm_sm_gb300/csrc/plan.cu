@@ -119,6 +119,10 @@ constexpr double kStageBytesPerUs = 6.2e6;
 // above, from grids of at most a few CTAs per SM, puts the layouts closer together; the
 // staging decision compares layouts, so it uses these.
 constexpr double kLayoutFactor[4] = {1.046, 1.129, 1.000, 1.046};
+
+// The element-wise configurations against the vector model of their tile.
+constexpr double kScalar128 = 1.07;
+constexpr double kScalar64 = 1.04;
 constexpr double kTailOverlapUs = 35.0;
 
 long long ksplit_clusters_per_round(int num_sms)
@@ -150,11 +154,22 @@ int kchain_slices(int ta, int tb, long long r, long long K, int num_sms)
 double select_config_us(int ta, int tb, long long M, long long N, long long K, long long batch,
                         bool aligned, int num_sms, int *config)
 {
-    if (!aligned) {
-        *config = CFG_64x64_SCALAR;
-        return 1e300;  // element-wise copies: not modelled
-    }
     if (num_sms < 1) num_sms = 1;
+    if (!aligned) {
+        // Element-wise copies: the 128 x 128 tile (whole tiles only) at 1.07x its vector
+        // model, or the 64 x 64 tile at 1.04x (measured on 152 SMs, every layout, 256^3 to
+        // 4096^3 and the FC, QK^T and PV shapes: the 128 x 128 tile from about 2048^3 up,
+        // 1.37x at 4096^3 NN).
+        const LaunchModel *const mm = kModel[(ta ? 2 : 0) + (tb ? 1 : 0)];
+        const long long b = batch > 0 ? batch : 1;
+        const long long k = K > 0 ? K : 0;
+        const double s128 = kScalar128 * model_us(mm[M_128x128], tiles_of(M, N, 128, 128, b),
+                                                  (double)k, num_sms);
+        const double s64 = kScalar64 * model_us(mm[M_64x64], tiles_of(M, N, 64, 64, b),
+                                                (double)k, num_sms);
+        *config = s128 < s64 ? CFG_128x128_SCALAR : CFG_64x64_SCALAR;
+        return s128 < s64 ? s128 : s64;
+    }
     const long long b = batch > 0 ? batch : 1;
     const long long k = K > 0 ? K : 0;
     const double tiles128 = tiles_of(M, N, 128, 128, b);
@@ -246,14 +261,13 @@ int staging_choice(int ta, int tb, long long M, long long N, long long K, long l
     if (useful == 0) return 0;
     // Every candidate from one estimate: the GEMM with both operands k-major (op(A) = T,
     // op(B) = N) scaled by the layout's measured cost relative to it; with an unaligned
-    // operand left as stored, the 64 x 64 element-wise kernel, in any layout (measured
-    // within 4 % of the vector 64 x 64 NN tile from 64^3 to 4096^3; its copies move single
-    // elements whichever way the operands run, so a copy that leaves one operand
-    // unaligned buys nothing).
+    // operand left as stored, the element-wise kernels, estimated the same in any layout
+    // (their copies move single elements whichever way the operands run: the 128 x 128
+    // one measured within 2 % across the four layouts at 4096^3), so a copy that leaves
+    // one operand unaligned buys nothing.
     int unused = 0;
     const double base = select_config_us(1, 0, M, N, K, batch, true, num_sms, &unused);
-    const double scalar_us =
-        1.04 * model_us(kModel[0][M_64x64], tiles_of(M, N, 64, 64, batch), (double)K, num_sms);
+    const double scalar_us = select_config_us(0, 0, M, N, K, batch, false, num_sms, &unused);
     const auto gemm_us = [&](int a, int b, bool aligned) {
         return aligned ? base * kLayoutFactor[(a ? 2 : 0) + (b ? 1 : 0)] : scalar_us;
     };

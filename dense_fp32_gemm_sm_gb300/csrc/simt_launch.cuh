@@ -33,6 +33,14 @@ template <int TA, int TB>
 struct ConfigOf<CFG_64x64, TA, TB> {  // 256 threads, 4 x 4 per thread
     using type = SimtCfg<64, 64, 16, 32, 16, 4, 4, 4, 2, TA, TB, true>;
 };
+// The 128 x 128 tile with element-wise copies: any alignment.  A k-contiguous operand
+// is copied element by element in every configuration (transposed on the way), so this
+// differs from CFG_128x128 only for operands that config moves in 16-byte vectors.
+template <int TA, int TB>
+struct ConfigOf<CFG_128x128_SCALAR, TA, TB> {
+    using type = SimtCfg<128, 128, 32, 64, 32, 8, 8, 3, 2, TA, TB, false>;
+};
+
 template <int TA, int TB>
 struct ConfigOf<CFG_64x64_SCALAR, TA, TB> {  // element-wise copies: any alignment
     using type = SimtCfg<64, 64, 16, 32, 16, 4, 4, 4, 2, TA, TB, false>;
@@ -357,7 +365,8 @@ static fgemm_status launch_simt_kchain(const GemmParams &p0, int batch, cudaStre
                            SplitTailOf<TA, TB>::type>,                     \
         &launch_simt_ksplit<ConfigOf<CFG_128x128, TA, TB>::type>,          \
         &launch_simt_kchain<ConfigOf<CFG_128x128, TA, TB>::type>,          \
+        &launch_simt<ConfigOf<CFG_128x128_SCALAR, TA, TB>::type>,          \
     };                                                                     \
-    static_assert(NUM_CONFIGS == 9, "one launcher per configuration");
+    static_assert(NUM_CONFIGS == 10, "one launcher per configuration");
 
 }  // namespace fgemm

@@ -315,6 +315,10 @@ const char *fgemm_status_string(fgemm_status status);
  * last-wave launch is a programmatic dependent of the launch before it: it may start
  * while that one runs and waits for it only before writing C.  All allocate nothing and
  * give the same result on every run.
+ *
+ * Calls whose A or B is not 16-byte aligned take one of the two "..._scalar"
+ * configurations, which move single elements: the 128 x 128 tile for large problems,
+ * the 64 x 64 tile for small ones (by the same model).
  * ------------------------------------------------------------------------- */
 
 /* Number of kernel configurations; valid ids are 0 .. fgemm_num_configs()-1. */

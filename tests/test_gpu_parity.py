@@ -20,7 +20,8 @@ pytestmark = pytest.mark.gpu
 
 COMBOS = list(itertools.product((0, 1), (0, 1)))
 VEC_CONFIGS = [0, 1, 2, 4, 5, 6, 7, 8]
-SCALAR_CONFIG = 3
+SCALAR_CONFIG = 3       # 64 x 64, element-wise copies
+SCALAR_CONFIGS = [3, 9]  # and the 128 x 128 tile with element-wise copies
 SHAPES = [(300, 200, 130), (1, 1, 1), (129, 65, 17), (64, 128, 3), (7, 333, 64), (257, 31, 515)]
 
 
@@ -32,11 +33,12 @@ def _cuda():
 
 
 def test_config_names_match_ids():
-    assert fg.config_name(SCALAR_CONFIG).endswith("_scalar")
+    assert all(fg.config_name(c).endswith("_scalar") for c in SCALAR_CONFIGS)
     assert all(not fg.config_name(c).endswith("_scalar") for c in VEC_CONFIGS)
+    assert sorted(VEC_CONFIGS + SCALAR_CONFIGS) == list(range(fg.num_configs()))
 
 
-@pytest.mark.parametrize("config", VEC_CONFIGS + [SCALAR_CONFIG])
+@pytest.mark.parametrize("config", VEC_CONFIGS + SCALAR_CONFIGS)
 @pytest.mark.parametrize("ta,tb", COMBOS)
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_integer_exact(config, ta, tb, shape):
@@ -45,14 +47,14 @@ def test_integer_exact(config, ta, tb, shape):
                pad=(4, 8, 4), seed=M + N + K))
 
 
-@pytest.mark.parametrize("config", VEC_CONFIGS + [SCALAR_CONFIG])
+@pytest.mark.parametrize("config", VEC_CONFIGS + SCALAR_CONFIGS)
 @pytest.mark.parametrize("ta,tb", COMBOS)
 def test_uniform_floats(config, ta, tb):
     check(Case(ta=ta, tb=tb, M=515, N=387, K=1029, alpha=1.5, beta=0.5, ints=False,
                config=config, seed=3))
 
 
-@pytest.mark.parametrize("config", VEC_CONFIGS + [SCALAR_CONFIG])
+@pytest.mark.parametrize("config", VEC_CONFIGS + SCALAR_CONFIGS)
 @pytest.mark.parametrize("bias,relu", [(False, False), (True, False), (False, True), (True, True)])
 def test_bias_relu_combinations(config, bias, relu):
     for ta, tb in COMBOS:
@@ -64,8 +66,21 @@ def test_unaligned_pointers_and_ld_use_scalar_path(ta, tb):
     for offset, pad in (((1, 0, 0), (0, 0, 0)), ((0, 3, 0), (1, 0, 0)), ((2, 1, 3), (1, 3, 1))):
         check(Case(ta=ta, tb=tb, M=150, N=90, K=77, alpha=1.0, beta=1.0, offset=offset, pad=pad,
                    config=-1, seed=11, align_ld=False))
-        check(Case(ta=ta, tb=tb, M=150, N=90, K=77, ints=False, offset=offset, pad=pad,
-                   config=SCALAR_CONFIG, seed=12, align_ld=False))
+        for config in SCALAR_CONFIGS:
+            check(Case(ta=ta, tb=tb, M=150, N=90, K=77, ints=False, offset=offset, pad=pad,
+                       config=config, seed=12, align_ld=False))
+
+
+@pytest.mark.parametrize("ta,tb", COMBOS)
+def test_unaligned_large_problem_takes_the_128_tile(ta, tb):
+    # Odd leading dimensions at 2600 x 2400 x 900: the selector picks the 128 x 128 tile
+    # with element-wise copies (whole and ragged tiles), bit-exact on integers
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if sms == 152:
+        assert fg.select_config(ta, tb, 2600, 2400, 900, 1, False, sms) == 9
+    check(Case(ta=ta, tb=tb, M=2600, N=2400, K=900, alpha=2.0, beta=-1.0, bias=True, relu=True,
+               offset=(1, 2, 3), pad=(1, 1, 1), config=-1, seed=13 + 2 * ta + tb,
+               align_ld=False))
 
 
 @pytest.mark.parametrize("config", [-1] + VEC_CONFIGS)
@@ -75,18 +90,18 @@ def test_unaligned_c_only(config):
                align_ld=False))
 
 
-@pytest.mark.parametrize("config", VEC_CONFIGS + [SCALAR_CONFIG])
+@pytest.mark.parametrize("config", VEC_CONFIGS + SCALAR_CONFIGS)
 def test_k_zero_and_alpha_zero(config):
     check(Case(M=70, N=90, K=0, alpha=3.0, beta=-2.0, bias=True, relu=True, config=config))
     check(Case(M=70, N=90, K=33, alpha=0.0, beta=0.5, a_nan=True, config=config))
 
 
-@pytest.mark.parametrize("config", VEC_CONFIGS + [SCALAR_CONFIG])
+@pytest.mark.parametrize("config", VEC_CONFIGS + SCALAR_CONFIGS)
 def test_beta_zero_never_reads_c(config):
     check(Case(M=96, N=80, K=24, beta=0.0, c_nan=True, bias=True, config=config))
 
 
-@pytest.mark.parametrize("config", VEC_CONFIGS + [SCALAR_CONFIG])
+@pytest.mark.parametrize("config", VEC_CONFIGS + SCALAR_CONFIGS)
 @pytest.mark.parametrize("ta,tb", COMBOS)
 def test_strided_batched(config, ta, tb):
     check(Case(ta=ta, tb=tb, M=70, N=130, K=45, alpha=0.5, beta=1.0, batch=3, config=config,
