@@ -114,8 +114,11 @@ fgemm_status run(int config, const Problem &p)
     if (config >= NUM_CONFIGS) return FGEMM_ERR_INVALID_VALUE;
 
     const bool products = p.K > 0 && p.alpha != 0.0f;
-    const bool aligned = !products || (aligned16(p.A, p.lda, p.sA, p.batch) &&
-                                       aligned16(p.B, p.ldb, p.sB, p.batch));
+    // Only operands moved by 16-byte copies need alignment: the k-major ones (A for op T,
+    // B for op N).  An operand stored with k contiguous is copied element by element
+    // (transposed on the way) in every configuration.
+    const bool aligned = !products || ((p.ta == 0 || aligned16(p.A, p.lda, p.sA, p.batch)) &&
+                                       (p.tb == 1 || aligned16(p.B, p.ldb, p.sB, p.batch)));
     if (config < 0) {
         int sms = 0;
         if (device_sm_count(&sms) != 0) {

@@ -271,13 +271,19 @@ int staging_choice(int ta, int tb, long long M, long long N, long long K, long l
     const auto gemm_us = [&](int a, int b, bool aligned) {
         return aligned ? base * kLayoutFactor[(a ? 2 : 0) + (b ? 1 : 0)] : scalar_us;
     };
-    double best_us = gemm_us(ta, tb, aligned_a && aligned_b);
+    // The vector kernels need only the k-major operands aligned (A for op T, B for op N;
+    // the others are copied element by element anyway); a copied operand always is.
+    const auto vec_ok = [&](int a, int b, bool sa, bool sb) {
+        return (sa || a == 0 || aligned_a) && (sb || b == 1 || aligned_b);
+    };
+    double best_us = gemm_us(ta, tb, vec_ok(ta, tb, false, false));
     int best = 0;
     for (int mask = 1; mask <= 3; ++mask) {
         if ((mask & useful) != mask) continue;
         if (stage_bytes(mask, M, N, K, problems_a, problems_b) > workspace_bytes) continue;
         const bool sa = (mask & 1) != 0, sb = (mask & 2) != 0;
-        double us = gemm_us(sa ? 1 : ta, sb ? 0 : tb, (sa || aligned_a) && (sb || aligned_b));
+        const int a2 = sa ? 1 : ta, b2 = sb ? 0 : tb;
+        double us = gemm_us(a2, b2, vec_ok(a2, b2, sa, sb));
         if (sa) us += stage_copy_us(M, K, problems_a);
         if (sb) us += stage_copy_us(N, K, problems_b);
         // Stage only for a clear gain (1 % and 1 us over the best so far).

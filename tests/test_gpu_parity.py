@@ -83,6 +83,22 @@ def test_unaligned_large_problem_takes_the_128_tile(ta, tb):
                align_ld=False))
 
 
+@pytest.mark.parametrize("config", [-1, 0, 1, 7, 8])
+@pytest.mark.parametrize("ta,tb", [(0, 0), (0, 1), (1, 1)])
+def test_unaligned_k_contiguous_operand_keeps_the_vector_kernels(config, ta, tb):
+    # Operands stored with k contiguous (A for op N, B for op T) are copied element by
+    # element in every configuration, so their alignment does not matter: odd leading
+    # dimensions and shifted pointers on them run the 16-byte-vector configurations.
+    off_a, pad_a = (1, 1) if ta == 0 else (0, 0)
+    off_b, pad_b = (2, 3) if tb == 1 else (0, 0)
+    if config < 0 and torch.cuda.get_device_properties(0).multi_processor_count == 152:
+        assert not fg.config_name(fg.select_config(ta, tb, 1500, 1400, 300, 1, True,
+                                                   152)).endswith("_scalar")
+    check(Case(ta=ta, tb=tb, M=1500, N=1400, K=300, alpha=1.5, beta=0.5, bias=True,
+               offset=(off_a, off_b, 0), pad=(pad_a, pad_b, 0), align_ld=False, config=config,
+               seed=21 + 2 * ta + tb))
+
+
 @pytest.mark.parametrize("config", [-1] + VEC_CONFIGS)
 def test_unaligned_c_only(config):
     # A and B aligned, C shifted by one element: vector configs fall back to scalar stores.
