@@ -161,8 +161,16 @@ def test_entry_points_agree_with_explicit():
 
 
 def test_rejects_vector_config_on_unaligned_device_pointer():
-    A = torch.zeros(65, device="cuda")
-    st = fg.gemm_explicit(0, 0, 0, 4, 4, 4, 1.0, A.data_ptr() + 4, 4, 0, A, 4, 0, 0.0, A, 4, 0, 1,
+    # A vector configuration refuses an unaligned k-major operand (B for op N, which it
+    # moves in 16-byte copies) and accepts an unaligned k-contiguous one (A for op N,
+    # copied element by element).
+    X = torch.zeros(65, device="cuda")
+    C = torch.full((4, 4), 7.0, device="cuda")
+    st = fg.gemm_explicit(0, 0, 0, 4, 4, 4, 1.0, X, 4, 0, X.data_ptr() + 4, 4, 0, 0.0, C, 4, 0, 1,
                           check=False)
     assert st == fg.ERR_NOT_SUPPORTED
+    st = fg.gemm_explicit(0, 0, 0, 4, 4, 4, 1.0, X.data_ptr() + 4, 4, 0, X, 4, 0, 0.0, C, 4, 0, 1,
+                          check=False)
+    torch.cuda.synchronize()
+    assert st == fg.OK and bool((C == 0.0).all())
 
