@@ -27,9 +27,12 @@
  *   - Invalid arguments return FGEMM_ERR_INVALID_VALUE before anything is
  *     launched; C is left untouched.  A failed launch returns FGEMM_ERR_LAUNCH.
  *     Nothing aborts or exits the process.
- *   - Any alignment is accepted.  When a pointer, leading dimension or batch
- *     stride is not a multiple of 16 bytes the call runs a slower kernel that
- *     moves single elements instead of 16-byte vectors.
+ *   - Any alignment is accepted.  When the pointer, leading dimension or batch
+ *     stride of a k-major operand (A for transa == T, B for transb == N) is not a
+ *     multiple of 16 bytes, the call runs a kernel that moves single elements
+ *     instead of 16-byte vectors (an operand stored with k contiguous is moved
+ *     element by element in any case, so its alignment does not matter); C's
+ *     alignment only decides between vector and element stores.
  *   - Arithmetic is IEEE FP32 fused multiply-add on the CUDA cores, summing k
  *     in an order that differs from the plain loop; results agree with an FP64
  *     evaluation to within 1e-5 * (|alpha| sum_k |a_ik||b_kj| + |beta||c_ij| + |bias_j|).
@@ -316,9 +319,10 @@ const char *fgemm_status_string(fgemm_status status);
  * while that one runs and waits for it only before writing C.  All allocate nothing and
  * give the same result on every run.
  *
- * Calls whose A or B is not 16-byte aligned take one of the two "..._scalar"
- * configurations, which move single elements: the 128 x 128 tile for large problems,
- * the 64 x 64 tile for small ones (by the same model).
+ * Calls with an unaligned k-major operand (see the alignment rule above) take one of
+ * the two "..._scalar" configurations, which move single elements: the 128 x 128 tile
+ * for large problems, the 64 x 64 tile for small ones (by the same model).  The
+ * `aligned` argument of the queries below means the vector configurations may run.
  * ------------------------------------------------------------------------- */
 
 /* Number of kernel configurations; valid ids are 0 .. fgemm_num_configs()-1. */
