@@ -30,6 +30,7 @@ from ._binding import (  # noqa: F401
     sgemm,
     sgemm_bias_relu,
     sgemm_row_bias_relu,
+    MAX_DIM,
     NOALLOC_SCRATCH_BYTES,
     STAGE_AUTO,
     sgemm_splitk,

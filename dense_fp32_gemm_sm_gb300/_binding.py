@@ -259,6 +259,11 @@ def sgemm_splitk(transa, transb, M, N, K, alpha, A, lda, B, ldb, beta, C, ldc, b
     return st
 
 
+# FGEMM_MAX_DIM of include/fgemm.h: the largest M, N or K a call takes (2^31 - 256);
+# larger sizes return FGEMM_ERR_NOT_SUPPORTED.
+MAX_DIM = 2**31 - 256
+
+
 # FGEMM_NOALLOC_SCRATCH_BYTES of include/fgemm.h: the fixed scratch array behind
 # fgemm_sgemm_splitk_noalloc.
 NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024

@@ -95,6 +95,8 @@ fgemm_status validate(const Problem &p, bool *noop)
     if (products && (p.A == nullptr || p.B == nullptr)) return FGEMM_ERR_INVALID_VALUE;
     if (p.C == nullptr) return FGEMM_ERR_INVALID_VALUE;
     if (c_batches_overlap(p.M, p.N, p.ldc, p.sC, p.batch)) return FGEMM_ERR_INVALID_VALUE;
+    // A valid call with a size the 32-bit tile and k positions cannot reach.
+    if (!dims_supported(p.M, p.N, p.K)) return FGEMM_ERR_NOT_SUPPORTED;
     return FGEMM_OK;
 }
 
@@ -456,6 +458,7 @@ int fgemm_math_supported(fgemm_math math, fgemm_op transa, fgemm_op transb, int 
 {
     if (math == FGEMM_MATH_FP32) return 1;
     if (math != FGEMM_MATH_TF32 && math != FGEMM_MATH_3XTF32) return -1;
+    if (!fgemm::dims_supported(M, N, K)) return 0;  // the call runs nothing
     const fgemm::Problem p = make_problem(transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb,
                                           strideB, 0.0f, nullptr, 1, 0, batch, nullptr, 0, nullptr);
     return fgemm::tc_supported(fgemm::tc_problem(p)) ? 1 : 0;
@@ -554,23 +557,30 @@ int fgemm_launch_count(int config, fgemm_op transa, fgemm_op transb, int M, int 
         config >= fgemm::NUM_CONFIGS || num_sms < 1)
         return -1;
     if (M == 0 || N == 0 || batch == 0) return 0;
+    // Calls the library refuses (FGEMM_ERR_NOT_SUPPORTED) launch nothing: a size above
+    // FGEMM_MAX_DIM, or a tile grid larger than one launch takes.
+    if (!fgemm::dims_supported(M, N, K)) return 0;
     if (config < 0)
         config = fgemm::select_config((int)transa, (int)transb, M, N, K, batch, aligned != 0,
                                       num_sms);
+    const long long bm = fgemm::kConfigs[config].bm, bn = fgemm::kConfigs[config].bn;
+    const long long tiles = ((long long)M + bm - 1) / bm * (((long long)N + bn - 1) / bn);
     if (config == fgemm::CFG_128x128_SPLIT || config == fgemm::CFG_128x128_KSPLIT ||
         config == fgemm::CFG_128x128_KCHAIN) {
-        const long long total = (long long)((M + 127) / 128) * ((N + 127) / 128) * batch;
+        const long long total = tiles * batch;
         const long long r = total % num_sms;
+        const long long tail_ctas = config == fgemm::CFG_128x128_KCHAIN ? 1 : 4;
+        if (total - r > INT_MAX || tail_ctas * r > INT_MAX) return 0;
         const int tail = config == fgemm::CFG_128x128_KCHAIN
                              ? fgemm::kchain_slices((int)transa, (int)transb, r, K, num_sms)
                              : 1;
         return (total - r > 0 ? 1 : 0) + (r > 0 ? tail : 0);
     }
+    if (tiles > INT_MAX) return 0;
     // TT whole 128 x 128 tiles run in linear-order launches of up to INT_MAX CTAs; the
     // other configurations in one launch per 65535 problems
     if ((config == fgemm::CFG_128x128 || config == fgemm::CFG_128x128_SCALAR) &&
         transa == FGEMM_OP_T && transb == FGEMM_OP_T) {
-        const long long tiles = (long long)((M + 127) / 128) * ((N + 127) / 128);
         const long long per_launch = INT_MAX / tiles;
         return (int)((batch + per_launch - 1) / per_launch);
     }

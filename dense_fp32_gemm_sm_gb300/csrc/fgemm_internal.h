@@ -61,6 +61,14 @@ int select_config(int ta, int tb, long long M, long long N, long long K, long lo
 inline size_t sat_mul(size_t a, size_t b) { return (b != 0 && a > SIZE_MAX / b) ? SIZE_MAX : a * b; }
 inline size_t sat_add(size_t a, size_t b) { return a > SIZE_MAX - b ? SIZE_MAX : a + b; }
 
+// Sizes the kernels can index: their 32-bit tile, row, column and k positions run up to
+// 255 past the last row, column or k (a 256-row tensor-core tile, a 32-deep k-block), so
+// M, N and K stay at or below 2^31 - 256.
+inline bool dims_supported(long long M, long long N, long long K)
+{
+    return M <= FGEMM_MAX_DIM && N <= FGEMM_MAX_DIM && K <= FGEMM_MAX_DIM;
+}
+
 // Bytes of the workspace copies a staged call makes with `mask` (bit 0: A, bit 1: B): each
 // copy is K x ld4(rows) floats a problem (ld4: rounded up to a multiple of 4), B's starting
 // at the next multiple of 256 bytes after A's.  problems_a/_b: the problems each operand

@@ -37,6 +37,17 @@ def small_ints(g: torch.Generator, shape, lo: int = -4, hi: int = 4) -> torch.Te
     return torch.randint(lo, hi + 1, tuple(shape), generator=g).to(torch.float32)
 
 
+def pooled_ints(g: torch.Generator, count: int, pool: int, width: int, lo: int = -4,
+                hi: int = 4):
+    """Small-integer rows for a matrix too large to draw element by element: a seeded
+    ``pool x width`` block of small integers, then for each of ``count`` rows the index of
+    the pool row it repeats.  Returns ``(rows, index)``: row r of the matrix is
+    ``rows[index[r]]`` (``index`` is int64)."""
+    rows = small_ints(g, (pool, width), lo, hi)
+    index = torch.randint(0, pool, (count,), generator=g)
+    return rows, index
+
+
 @dataclass
 class Workload:
     """One GEMM problem in the library's argument convention.

@@ -27,6 +27,11 @@
  *   - Invalid arguments return FGEMM_ERR_INVALID_VALUE before anything is
  *     launched; C is left untouched.  A failed launch returns FGEMM_ERR_LAUNCH.
  *     Nothing aborts or exits the process.
+ *   - Sizes: M, N and K up to FGEMM_MAX_DIM (2^31 - 256); a valid call with a larger
+ *     one returns FGEMM_ERR_NOT_SUPPORTED before anything is launched.  Element
+ *     offsets are 64-bit, so C, A and B may each hold more than 2^31 elements; tile,
+ *     row, column and k positions are 32-bit and run up to 255 past the last row,
+ *     column or k, which the limit keeps below 2^31.
  *   - Any alignment is accepted.  When the pointer, leading dimension or batch
  *     stride of a k-major operand (A for transa == T, B for transb == N) is not a
  *     multiple of 16 bytes, the call runs a kernel that moves single elements
@@ -58,11 +63,15 @@ typedef enum fgemm_status {
     FGEMM_OK = 0,
     FGEMM_ERR_INVALID_VALUE = 1, /* an argument breaks the rules above; nothing launched */
     FGEMM_ERR_LAUNCH = 2,        /* the CUDA launch (or a CUDA query before it) failed */
-    FGEMM_ERR_NOT_SUPPORTED = 3, /* e.g. no sm_103a device, or a config that cannot run the call */
+    FGEMM_ERR_NOT_SUPPORTED = 3, /* e.g. no sm_103a device, a config that cannot run the call,
+                                    or a size above FGEMM_MAX_DIM */
     FGEMM_ERR_TIMEOUT = 4,       /* a tensor-core kernel gave up waiting (fgemm_device_status) */
 } fgemm_status;
 
 typedef enum fgemm_op { FGEMM_OP_N = 0, FGEMM_OP_T = 1 } fgemm_op;
+
+/* Largest M, N or K a call takes (see "Sizes" above). */
+#define FGEMM_MAX_DIM 2147483392
 
 /*
  * Plain GEMM: C = alpha*op(A)*op(B) + beta*C.
@@ -275,7 +284,8 @@ fgemm_status fgemm_device_status(int clear);
  * it runs the requested one (always for FGEMM_MATH_FP32; for the tensor-core modes
  * when the layout, alignment and sizes suit the tcgen05 kernel), 0 when it would run
  * the FP32 CUDA-core kernel instead (unaligned operands, K == 0, alpha == 0, an empty
- * problem, or no driver), -1 when `math` is not an fgemm_math value.  The arguments
+ * problem, or no driver) or nothing at all (a size above FGEMM_MAX_DIM), -1 when
+ * `math` is not an fgemm_math value.  The arguments
  * mean what they mean for fgemm_gemm_math; the pointers are only tested for 16-byte
  * alignment, never dereferenced, and nothing else is validated.  Host-only: no
  * kernel runs and no device memory is touched (the first call looks up the driver's
@@ -348,8 +358,10 @@ int fgemm_select_config(fgemm_op transa, fgemm_op transb, int M, int N, int K, i
  * last-wave configurations one for the
  * whole tiles (if any) plus one for the last (tiles mod SMs) tiles -- or, for
  * "..._kchain", one per k-slice (2 to 8, chosen from the remainder and K).  K is the
- * depth the kernels see: 0 when alpha == 0.  0 for an empty problem, -1 for arguments
- * the entry points would reject.  Host-only: no CUDA call is made.
+ * depth the kernels see: 0 when alpha == 0.  0 for an empty problem and for calls the
+ * entry points refuse as FGEMM_ERR_NOT_SUPPORTED (a size above FGEMM_MAX_DIM, or more
+ * tiles than one launch takes), -1 for arguments they reject as invalid.  Host-only: no
+ * CUDA call is made.
  */
 int fgemm_launch_count(int config, fgemm_op transa, fgemm_op transb, int M, int N, int K,
                        int batch, int aligned, int num_sms);

@@ -313,3 +313,77 @@ def test_staged_validates_before_launch(kw):
                          args["lda"], 0, FAKE, 64, 0, 0.0, FAKE, 64, 0, 1, None, False,
                          args["stage"], args["workspace"], wsb, check=False)
     assert st == fg.ERR_INVALID_VALUE
+
+
+def test_max_dim_matches_the_header():
+    text = open(HEADER, encoding="utf-8").read()
+    m = re.search(r"#define\s+FGEMM_MAX_DIM\s+(\d+)", text)
+    assert m and int(m.group(1)) == fg.MAX_DIM == 2**31 - 256
+
+
+@pytest.mark.parametrize("dim", ["M", "N", "K"])
+def test_sizes_above_the_limit_are_not_supported_before_launch(dim):
+    # A valid call with one size past FGEMM_MAX_DIM is refused as not supported by every
+    # entry point, before any CUDA call (the pointers are never dereferenced); at the
+    # limit itself the size checks pass (the same calls then fail only on the missing
+    # GPU or on the fake pointers, never with NOT_SUPPORTED from the size).  Invalid
+    # arguments still come first, and an empty problem is still a no-op.
+    over = fg.MAX_DIM + 1
+    big = 2**31 - 1  # leading dimensions that cover any size
+    base = dict(transa=0, transb=0, M=8, N=8, K=8, alpha=1.0, A=FAKE, lda=big, B=FAKE, ldb=big,
+                beta=0.0, C=FAKE, ldc=big)
+    kw = dict(base, **{dim: over})
+    assert fg.sgemm(**kw, check=False) == fg.ERR_NOT_SUPPORTED
+    assert fg.sgemm_bias_relu(**kw, bias=None, apply_relu=True, check=False) == fg.ERR_NOT_SUPPORTED
+    assert fg.sgemm_row_bias_relu(**kw, row_bias=None, apply_relu=False,
+                                  check=False) == fg.ERR_NOT_SUPPORTED
+    a = (kw["transa"], kw["transb"], kw["M"], kw["N"], kw["K"], 1.0, FAKE, big, 0, FAKE, big, 0,
+         0.0, FAKE, big, 0, 1)
+    assert fg.sgemm_strided_batched(*a, check=False) == fg.ERR_NOT_SUPPORTED
+    for config in (-1, 0, fg.num_configs() - 1):
+        assert fg.gemm_explicit(config, *a, check=False) == fg.ERR_NOT_SUPPORTED
+    for math in (fg.MATH_FP32, fg.MATH_TF32, fg.MATH_3XTF32):
+        assert fg.gemm_math(math, *a, check=False) == fg.ERR_NOT_SUPPORTED
+        assert fg.math_supported(math, *a[:12], 1) == (1 if math == fg.MATH_FP32 else 0)
+    assert fg.sgemm_staged(*a, None, False, fg.STAGE_AUTO, None, 0,
+                           check=False) == fg.ERR_NOT_SUPPORTED
+    assert fg.sgemm_splitk(**kw, bias=None, apply_relu=False, splits=2, workspace=FAKE,
+                           workspace_bytes=2**63, check=False) == fg.ERR_NOT_SUPPORTED
+    assert fg.sgemm_splitk_noalloc(**kw, bias=None, apply_relu=False, splits=1,
+                                   check=False) == fg.ERR_NOT_SUPPORTED
+    # invalid before unsupported; empty before both
+    assert fg.sgemm(**dict(kw, ldc=7), check=False) == fg.ERR_INVALID_VALUE
+    assert fg.sgemm(**dict(kw, C=None), check=False) == fg.ERR_INVALID_VALUE
+    empty = "N" if dim != "N" else "M"
+    assert fg.sgemm(**dict(kw, **{empty: 0}), check=False) == fg.OK
+
+
+@pytest.mark.parametrize("dim", ["M", "N", "K"])
+def test_launch_count_at_and_above_the_limit(dim):
+    # Host-only: sizes at the limit give a launch count from 64-bit tile arithmetic;
+    # above it (refused as not supported) the call launches nothing.
+    sizes = dict(M=8, N=8, K=8)
+    for config in range(-1, fg.num_configs()):
+        for ta in (0, 1):
+            for tb in (0, 1):
+                at = dict(sizes, **{dim: fg.MAX_DIM})
+                n = fg.launch_count(config, ta, tb, at["M"], at["N"], at["K"], 1, 1, 152)
+                assert 1 <= n <= 9, (config, ta, tb, n)
+                above = dict(sizes, **{dim: fg.MAX_DIM + 1})
+                assert fg.launch_count(config, ta, tb, above["M"], above["N"], above["K"], 1, 1,
+                                       152) == 0
+
+
+def test_launch_count_of_a_grid_too_large_for_one_launch():
+    # 2^48 tiles of 128 x 128 exceed one grid: the launchers refuse the call as not
+    # supported, so the query answers 0 (for TT whole tiles too, whose count divides by
+    # the tiles a launch holds).
+    side = fg.MAX_DIM
+    for config in range(fg.num_configs()):
+        assert fg.launch_count(config, 1, 1, side, side, 64, 1, 1, 152) == 0, config
+        assert fg.launch_count(config, 0, 0, side, side, 64, 1, 1, 152) == 0, config
+    # TT whole tiles: 2^31 - 256 tiles fill one launch (a batch of two takes two); one
+    # more column of tiles is more than a launch holds
+    assert fg.launch_count(0, 1, 1, fg.MAX_DIM, 128 * 128, 64, 1, 1, 152) == 1
+    assert fg.launch_count(0, 1, 1, fg.MAX_DIM, 128 * 128, 64, 2, 1, 152) == 2
+    assert fg.launch_count(0, 1, 1, fg.MAX_DIM, 128 * 128 + 1, 64, 1, 1, 152) == 0
