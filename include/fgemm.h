@@ -20,6 +20,9 @@
  *     nothing, frees nothing and keeps no workspace.
  *   - Every call is asynchronous on `stream` (NULL = the legacy default stream)
  *     and never synchronises.  Results are valid once the stream has run.
+ *   - C must not share memory with A, B or a bias vector (not checked; such a call
+ *     gives undefined results).  A, B and the bias are only read and may overlap
+ *     one another.
  *   - beta == 0: C is not read before it is written (it may hold NaN).
  *   - alpha == 0 or K == 0: no products are formed and A, B are not read
  *     (they may be NULL); the result is beta*C (then bias, ReLU).
