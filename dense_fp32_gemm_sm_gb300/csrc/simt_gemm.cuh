@@ -725,72 +725,27 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
         return;
     }
 
-    // ---- k-chain tiles: add this slice's products to C in slice order.
-    if constexpr (MAP == TILE_KCHAIN) {
-        const int slice = chain & 0xFF, slices = chain >> 8;
-        const bool first = slice == 0, last = slice + 1 == slices;
-        const bool products = KT > 0;
-        // C holds the sum of the earlier slices once the previous launch is complete;
-        // read it past L1 (.cg), which may hold lines an earlier slice replaced.  Slice 0
-        // waits too (for the whole tiles before it): its products need nothing from
-        // them, but then every launch of the call has completed when the last slice has.
-        pdl_wait_prerequisite();
-        const bool has_bias = last && p.bias != nullptr;
-        const bool has_row_bias = last && p.row_bias != nullptr;
-        const bool relu = last && p.relu;
-#pragma unroll
-        for (int i = 0; i < TM; ++i) {
-            const int gr = m0 + frag_row<Cfg>(wm0, lr, i);
-            if (gr >= p.M) continue;
-            float *const crow = C + (long long)gr * p.ldc;
-            const float rb = has_row_bias ? __ldg(p.row_bias + gr) : 0.0f;
-#pragma unroll
-            for (int g = 0; g < TN / 4; ++g) {
-                const int gc = n0 + frag_col<Cfg>(wn0, lc, 4 * g);
-                float v[4] = {acc[i][2 * g].x, acc[i][2 * g].y, acc[i][2 * g + 1].x,
-                              acc[i][2 * g + 1].y};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) v[e] = products ? p.alpha * v[e] : 0.0f;
-                float *const dst = crow + gc;
-                if (p.c_vec && gc + 3 < p.N) {
-                    if (!first || p.beta != 0.0f) {
-                        const float4 c = __ldcg(reinterpret_cast<const float4 *>(dst));
-                        const float w = first ? p.beta : 1.0f;
-                        v[0] = fmaf(w, c.x, v[0]);
-                        v[1] = fmaf(w, c.y, v[1]);
-                        v[2] = fmaf(w, c.z, v[2]);
-                        v[3] = fmaf(w, c.w, v[3]);
-                    }
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (has_bias) v[e] += __ldg(p.bias + gc + e);
-                        if (has_row_bias) v[e] += rb;
-                        if (relu) v[e] = fmaxf(v[e], 0.0f);
-                    }
-                    *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        if (gc + e >= p.N) break;
-                        float o = v[e];
-                        if (!first || p.beta != 0.0f) o = fmaf(first ? p.beta : 1.0f, __ldcg(dst + e), o);
-                        if (has_bias) o += __ldg(p.bias + gc + e);
-                        if (has_row_bias) o += rb;
-                        if (relu) o = fmaxf(o, 0.0f);
-                        dst[e] = o;
-                    }
-                }
-            }
-        }
-        return;
-    }
-
     // ---- Epilogue: alpha, beta, bias, ReLU in registers; vector stores where possible.
     // (Quarter tiles may have started while the call's whole tiles were finishing;
     // they complete only after them.)
     if constexpr (MAP == TILE_QUARTER) pdl_wait_prerequisite();
+    // k-chain slices: C holds the sum of the earlier slices once the launch before this
+    // one is complete, so every slice waits for it here (slice 0 too: its products need
+    // nothing from the whole tiles, but then every launch of the call has completed when
+    // the last slice has).  Slice 0 weighs C's old value by beta; later slices add their
+    // products to what C holds, read past L1 (.cg), which may hold lines an earlier slice
+    // replaced; only the last slice applies bias and ReLU.
+    bool last = true;
+    float cw = p.beta;
+    if constexpr (MAP == TILE_KCHAIN) {
+        const int slice = chain & 0xFF;
+        last = slice + 1 == (chain >> 8);
+        if (slice != 0) cw = 1.0f;
+        pdl_wait_prerequisite();
+    }
     const bool products = KT > 0;
-    const bool has_bias = p.bias != nullptr, has_row_bias = p.row_bias != nullptr;
+    const bool has_bias = last && p.bias != nullptr, has_row_bias = last && p.row_bias != nullptr;
+    const bool relu = last && p.relu;
     float bias_v[TN];
 #pragma unroll
     for (int j = 0; j < TN; ++j) {
@@ -811,18 +766,20 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
             for (int e = 0; e < 4; ++e) v[e] = products ? p.alpha * v[e] : 0.0f;
             float *const dst = crow + gc;
             if (p.c_vec && gc + 3 < p.N) {
-                if (p.beta != 0.0f) {
-                    const float4 c = *reinterpret_cast<const float4 *>(dst);
-                    v[0] = fmaf(p.beta, c.x, v[0]);
-                    v[1] = fmaf(p.beta, c.y, v[1]);
-                    v[2] = fmaf(p.beta, c.z, v[2]);
-                    v[3] = fmaf(p.beta, c.w, v[3]);
+                if (cw != 0.0f) {
+                    const float4 c = MAP == TILE_KCHAIN
+                                         ? __ldcg(reinterpret_cast<const float4 *>(dst))
+                                         : *reinterpret_cast<const float4 *>(dst);
+                    v[0] = fmaf(cw, c.x, v[0]);
+                    v[1] = fmaf(cw, c.y, v[1]);
+                    v[2] = fmaf(cw, c.z, v[2]);
+                    v[3] = fmaf(cw, c.w, v[3]);
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     if (has_bias) v[e] += bias_v[4 * g + e];
                     if (has_row_bias) v[e] += rb;
-                    if (p.relu) v[e] = fmaxf(v[e], 0.0f);
+                    if (relu) v[e] = fmaxf(v[e], 0.0f);
                 }
                 *reinterpret_cast<float4 *>(dst) = make_float4(v[0], v[1], v[2], v[3]);
             } else {
@@ -830,10 +787,11 @@ __global__ void __launch_bounds__(Cfg::THREADS, Cfg::MINB)
                 for (int e = 0; e < 4; ++e) {
                     if (gc + e >= p.N) break;
                     float o = v[e];
-                    if (p.beta != 0.0f) o = fmaf(p.beta, dst[e], o);
+                    if (cw != 0.0f)
+                        o = fmaf(cw, MAP == TILE_KCHAIN ? __ldcg(dst + e) : dst[e], o);
                     if (has_bias) o += bias_v[4 * g + e];
                     if (has_row_bias) o += rb;
-                    if (p.relu) o = fmaxf(o, 0.0f);
+                    if (relu) o = fmaxf(o, 0.0f);
                     dst[e] = o;
                 }
             }
