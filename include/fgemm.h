@@ -250,6 +250,11 @@ int fgemm_staged_choice(fgemm_op transa, fgemm_op transb, int M, int N, int K, i
  *   FGEMM_MATH_3XTF32  tensor cores with each operand split on chip into a TF32 high
  *                      part and a residual, three products per term (hi*hi, hi*lo,
  *                      lo*hi): near-FP32 accuracy.
+ * Special values: FP32 and TF32 give IEEE results (NaN and infinities land where the
+ * definition puts them; TF32 drops the 13 low mantissa bits, so a NaN whose payload
+ * lies only there reads as an infinity).  In 3xTF32 an infinity in an operand makes
+ * NaN of the outputs it reaches (a correction product multiplies it by the other
+ * operand's residual, often 0); outputs the definition leaves finite are unaffected.
  */
 typedef enum fgemm_math {
     FGEMM_MATH_FP32 = 0,

@@ -60,6 +60,9 @@ class Case:
     stage: object = None
     share_a: bool = False  # batch stride 0 for A (every problem reads the same A)
     share_b: bool = False
+    # (operand "A" or "B", stored row, stored column, value): entries set in every problem
+    # after the draw -- IEEE special values (NaN, +-Inf) among the small integers.
+    specials: tuple = ()
 
 
 def _draw(g, shape, ints):
@@ -110,6 +113,10 @@ def run(case: Case):
         for b in range(nb):
             for r in range(M):
                 C0[b * sC + r * ldc: b * sC + r * ldc + N] = np.nan
+    for which, r, c, v in case.specials:
+        flat, ld, stride = (A, lda, sA) if which == "A" else (B, ldb, sB)
+        for b in range(nb):
+            flat[b * stride + r * ld + c] = v
     if case.a_nan:
         A[:] = np.nan
     bias = _draw(g, (N,), True).astype(np.float32) if case.bias else None
