@@ -1,8 +1,9 @@
 """Batches of more than 65535 problems (the limit of one grid dimension).
 
 The per-problem grid runs such a batch in chunks of 65535 launches' worth of
-problems, the last-wave splits walk one linear tile order over all problems, and the
-staged call's copy kernel splits its batch the same way.  Small-integer data, so every
+problems, the last-wave splits walk one linear tile order over all problems, the
+staged call's copy kernel splits its batch the same way, and the persistent tensor-core
+kernel walks the tiles of all problems as one list of work items.  Small-integer data, so every
 result is exact: the problems on both sides of each chunk boundary, the first and the
 last are compared with the FP64 oracle element by element, and every problem is
 compared with a float64 CPU matmul of the same integers (exact as well).
@@ -90,3 +91,17 @@ def test_repitched_batch_beyond_one_grid_dimension(operands):
                     None, False, 3, ws, need)
     torch.cuda.synchronize()
     _check(C, A, Bt, want, 1.0)
+
+
+@pytest.mark.parametrize("math", [fg.MATH_TF32, fg.MATH_3XTF32], ids=["tf32", "3xtf32"])
+def test_tensor_core_batch_beyond_one_grid_dimension(operands, math):
+    """The persistent tensor-core kernel walks (problem, tile) items of all 98309 problems
+    (the batch is the tensor maps' third dimension)."""
+    A, Bt, want = operands
+    dA, dB = A.cuda(), Bt.cuda()
+    C = torch.full((BATCH, M, N), float("nan"), device="cuda")
+    assert fg.math_supported(math, 0, 1, M, N, K, 0.5, dA, K, M * K, dB, K, N * K, BATCH) == 1
+    fg.gemm_math(math, 0, 1, M, N, K, 0.5, dA, K, M * K, dB, K, N * K, 0.0, C, N, M * N, BATCH)
+    torch.cuda.synchronize()
+    assert fg.device_status() == fg.OK
+    _check(C, A, Bt, want, 0.5)
