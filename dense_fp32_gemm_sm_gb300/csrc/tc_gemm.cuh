@@ -9,7 +9,9 @@
 //   TF32   : D += A * B with each FP32 operand read as TF32 (10 explicit mantissa bits).
 //   3xTF32 : every operand x is split on chip into hi = x with the low 13 mantissa
 //            bits cleared (exactly representable in TF32) and lo = x - hi (exact in
-//            FP32), and D += A_lo*B_hi + A_hi*B_lo + A_hi*B_hi.  The dropped term
+//            FP32), and D += A_lo*B_hi + A_hi*B_lo + A_hi*B_hi.  (The MMA itself reads
+//            an FP32 operand as hi, so an operand kept in shared memory stays as loaded
+//            and only its lo is written.)  The dropped term
 //            A_lo*B_lo and the TF32 rounding of lo are about 2^-21 relative to |a||b|:
 //            close to FP32 accuracy (the split of Ootomo & Yokota, "Recovering single
 //            precision accuracy from Tensor Cores while surpassing the FP32 theoretical
@@ -27,8 +29,8 @@
 //   warps 2-5  (every layout but TF32 NT) move one operand of each stage from shared
 //              memory through registers into tensor memory, where the MMA reads it as
 //              its A operand -- transposed on the way when stored MN-major, split into
-//              hi and lo in 3xTF32 -- and split (3xTF32) or transpose (both operands
-//              MN-major) the other operand in shared memory.
+//              hi and lo in 3xTF32 -- and write the lo part of the other operand beside
+//              it (3xTF32) or transpose it (both operands MN-major) in shared memory.
 //   warps 6-9  epilogue of the previous item while the next one is being multiplied
 //              (warps 2-5 join them when there is nothing to convert): tcgen05.ld of
 //              their 32 accumulator lanes, alpha, beta*C, bias, ReLU; with beta == 0
@@ -318,9 +320,12 @@ __device__ __forceinline__ void split_tf32(float x, float &hi, float &lo)
 
 // ---- Split / transpose of one stage (warps 2-5, thread t in 0..127) --------------
 
-// K-major operand tile (already in the canonical swizzled layout): split in place,
-// element by element; lo goes to the same offsets of the lo tile.
-__device__ __forceinline__ void split_kmajor(float4 *tile, float4 *lo, int t)
+// K-major operand tile (already in the canonical swizzled layout): lo goes to the same
+// offsets of the lo tile; the tile itself stays as TMA wrote it.  The MMA reads an FP32
+// operand as TF32 by dropping its 13 low mantissa bits -- measured on GB300 for operands
+// in shared and in tensor memory: 1 + 3/4 ulp and 1 + 1/2 ulp read as 1, 2 + 7/4 ulp as
+// 2 + 1 ulp -- so the raw tile is read as exactly hi, and writing hi back is not needed.
+__device__ __forceinline__ void split_kmajor(const float4 *tile, float4 *lo, int t)
 {
 #pragma unroll 4
     for (int c = t; c < MMA_M * BK * 4 / 16; c += 128) {
@@ -330,7 +335,6 @@ __device__ __forceinline__ void split_kmajor(float4 *tile, float4 *lo, int t)
         split_tf32(v.y, h.y, l.y);
         split_tf32(v.z, h.z, l.z);
         split_tf32(v.w, h.w, l.w);
-        tile[c] = h;
         lo[c] = l;
     }
 }
