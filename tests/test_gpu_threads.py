@@ -5,7 +5,7 @@ split-K entry, whose calls share one scratch array, and the tensor-core test hoo
 test runs in a fresh Python process, so every first-use setup of the library -- kernel
 attributes, the SM count, the tensor-map encoder, the device error word -- happens while
 the threads race: eight threads wait at a barrier, then each makes a different mix of
-calls on its own stream and data, three rounds of it: plain calls in every transpose
+calls on its own stream and data, three times over: plain calls in every transpose
 layout (single and strided-batch, whole tiles and the last-wave splits), the staged call
 with its own workspace, split-K with its own workspace, the row-bias entry and both
 tensor-core modes.  Every result is compared with the FP64 oracle element by element;
@@ -21,7 +21,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 THREADS = 8
-ROUNDS = 3
+REPEATS = 3
 
 # (entry, ta, tb, M, N, K, batch, alpha, beta, bias, relu, extra)
 TEMPLATES = [
@@ -81,7 +81,7 @@ def _child():
         A, B, C, lda, ldb = d["A"], d["B"], d["C"], d["lda"], d["ldb"]
         sA, sB, sC = A[0].numel(), B[0].numel(), M * N
         al, be, bias, relu = d["alpha"], d["beta"], d["bias"], d["relu"]
-        C.copy_(d["C0"])  # on stream s: every round starts from the same C
+        C.copy_(d["C0"])  # on stream s: every repeat starts from the same C
         e = d["entry"]
         if e == "plain":
             fg.gemm_explicit(-1, ta, tb, M, N, K, al, A, lda, sA, B, ldb, sB, be, C, N, sC, b,
@@ -114,7 +114,7 @@ def _child():
             s = torch.cuda.Stream()
             with torch.cuda.stream(s):
                 barrier.wait()
-                for _ in range(ROUNDS):
+                for _ in range(REPEATS):
                     for d in dev[t]:
                         call(d, s)
             s.synchronize()
@@ -153,7 +153,7 @@ def _child():
                         got[p][tuple(bad)], want[tuple(bad)]))
                     sys.exit(1)
                 checked += 1
-    print("ok: %d threads x %d rounds, %d problems checked" % (THREADS, ROUNDS, checked))
+    print("ok: %d threads x %d repeats, %d problems checked" % (THREADS, REPEATS, checked))
 
 
 @pytest.mark.gpu
