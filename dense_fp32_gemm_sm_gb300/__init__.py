@@ -21,9 +21,12 @@ from ._binding import (  # noqa: F401
     debug_withhold_tensor_core,
     device_status,
     gemm_math,
+    gemm_math_staged,
     gemm_explicit,
     launch_count,
     library,
+    math_staged_choice,
+    math_staged_workspace_size,
     math_supported,
     num_configs,
     select_config,

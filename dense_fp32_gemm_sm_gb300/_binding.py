@@ -90,6 +90,12 @@ def library() -> ctypes.CDLL:
                                                _c_float, _c_vp, _c_int, _c_ll, _c_int, _c_vp,
                                                _c_int, _c_int, _c_vp, ctypes.c_size_t, _c_vp]
             lib.fgemm_sgemm_staged.restype = _c_int
+            lib.fgemm_math_staged_workspace_size.argtypes = [_c_int] * 7
+            lib.fgemm_math_staged_workspace_size.restype = ctypes.c_size_t
+            lib.fgemm_math_staged_choice.argtypes = [_c_int] * 11 + [ctypes.c_size_t, _c_int]
+            lib.fgemm_math_staged_choice.restype = _c_int
+            lib.fgemm_gemm_math_staged.argtypes = [_c_int] + lib.fgemm_sgemm_staged.argtypes
+            lib.fgemm_gemm_math_staged.restype = _c_int
             lib.fgemm_math_supported.argtypes = [_c_int, _c_int, _c_int, _c_int, _c_int, _c_int,
                                                  _c_float, _c_vp, _c_int, _c_ll, _c_vp, _c_int,
                                                  _c_ll, _c_int]
@@ -316,4 +322,38 @@ def sgemm_staged(transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, stride
         _ptr(workspace), int(workspace_bytes), _stream(stream, C, A, B))
     if check:
         _check(st, "fgemm_sgemm_staged")
+    return st
+
+
+def math_staged_workspace_size(math, transa, transb, M, N, K, batch) -> int:
+    """``fgemm_math_staged_workspace_size``: bytes of workspace fgemm_gemm_math_staged needs
+    for both copies."""
+    return int(library().fgemm_math_staged_workspace_size(int(math), int(transa), int(transb), M,
+                                                          N, K, batch))
+
+
+def math_staged_choice(math, transa, transb, M, N, K, batch, shared_a, shared_b, aligned_a,
+                       aligned_b, num_sms, workspace_bytes=None) -> int:
+    """``fgemm_math_staged_choice``: the copies fgemm_gemm_math_staged makes with
+    stage = STAGE_AUTO (bit 0: A, bit 1: B); host-only.  workspace_bytes=None: the full
+    fgemm_math_staged_workspace_size."""
+    if workspace_bytes is None:
+        workspace_bytes = math_staged_workspace_size(math, transa, transb, M, N, K, max(1, batch))
+    return library().fgemm_math_staged_choice(int(math), int(transa), int(transb), M, N, K, batch,
+                                              1 if shared_a else 0, 1 if shared_b else 0,
+                                              1 if aligned_a else 0, 1 if aligned_b else 0,
+                                              int(workspace_bytes), num_sms)
+
+
+def gemm_math_staged(math, transa, transb, M, N, K, alpha, A, lda, strideA, B, ldb, strideB,
+                     beta, C, ldc, strideC, batch, bias, apply_relu, stage, workspace,
+                     workspace_bytes, stream=None, check=True) -> int:
+    """``fgemm_gemm_math_staged``: fgemm_gemm_math after copying operands K-major into a
+    caller workspace (stage = STAGE_AUTO: the library's choice among the copies that fit)."""
+    st = library().fgemm_gemm_math_staged(
+        int(math), int(transa), int(transb), M, N, K, alpha, _ptr(A), lda, strideA, _ptr(B), ldb,
+        strideB, beta, _ptr(C), ldc, strideC, batch, _ptr(bias), 1 if apply_relu else 0,
+        int(stage), _ptr(workspace), int(workspace_bytes), _stream(stream, C, A, B))
+    if check:
+        _check(st, "fgemm_gemm_math_staged")
     return st

@@ -362,6 +362,110 @@ fgemm_status run_math(fgemm_math math, const Problem &p)
     return launch_tc(math == FGEMM_MATH_3XTF32 ? 3 : 1, q, p.stream);
 }
 
+// Tensor-core calls with operand staging.  The tcgen05 kernel reads an operand stored
+// K-major (A for op N, B for op T) straight from its TMA tiles; an MN-major one goes
+// through registers into tensor memory, and with both MN-major (TN) one of them is also
+// transposed in shared memory, at about half the rate of the other layouts (TF32 at
+// 4096^3: TN 335, TT 598, NN 643, NT 686 TFLOP/s).  The copies here are K-major: A as
+// M x ld4(K) floats a problem, B as N x ld4(K), B's at the next multiple of 256 bytes.
+size_t tc_stage_bytes(int mask, long long M, long long N, long long K, long long problems_a,
+                      long long problems_b)
+{
+    const auto copy = [&](long long rows, long long problems) {
+        return sat_mul(sat_mul(sat_mul((size_t)problems, (size_t)rows), (size_t)ld4(K)),
+                       sizeof(float));
+    };
+    const size_t a = (mask & 1) ? copy(M, problems_a) : 0;
+    const size_t b = (mask & 2) ? copy(N, problems_b) : 0;
+    return b == 0 ? a : sat_add(sat_add(a, 255) / 256 * 256, b);
+}
+
+// The copies a tensor-core staged call makes by default, among those that fit: every
+// operand whose alignment would keep the call off the tensor cores (then all of them or
+// none: one copy alone does not help), else in a TN call the copy of A, which turns it
+// into NN (measured at 4096^3 in TF32: 585 TFLOP/s with the copy against 335; copying
+// both, to NT, 568), or B's copy (to TT) when only that fits.
+int tc_staging_choice(int ta, int tb, long long M, long long N, long long K,
+                      long long problems_a, long long problems_b, bool aligned_a,
+                      bool aligned_b, size_t workspace_bytes)
+{
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    const auto fits = [&](int mask) {
+        return tc_stage_bytes(mask, M, N, K, problems_a, problems_b) <= workspace_bytes;
+    };
+    const int needed = (aligned_a ? 0 : 1) | (aligned_b ? 0 : 2);
+    if (needed != 0) return fits(needed) ? needed : 0;
+    if (ta == 1 && tb == 0) {
+        if (fits(1)) return 1;
+        if (fits(2)) return 2;
+    }
+    return 0;
+}
+
+fgemm_status run_math_staged(fgemm_math math, const Problem &p, int stage, void *workspace,
+                             size_t workspace_bytes)
+{
+    if (math == FGEMM_MATH_FP32) return run_staged(p, stage, workspace, workspace_bytes);
+    if (math != FGEMM_MATH_TF32 && math != FGEMM_MATH_3XTF32) return FGEMM_ERR_INVALID_VALUE;
+    bool noop = false;
+    fgemm_status st = validate(p, &noop);
+    if (st != FGEMM_OK) return st;
+    if (stage < -1 || stage > 3) return FGEMM_ERR_INVALID_VALUE;
+    if (workspace != nullptr && reinterpret_cast<uintptr_t>(workspace) % 16 != 0)
+        return FGEMM_ERR_INVALID_VALUE;
+    if (noop) return FGEMM_OK;
+    const bool products = p.K > 0 && p.alpha != 0.0f;
+    if (!products) return run_math(math, p);
+    // An operand a batch shares (stride 0) is copied once.
+    const long long problems_a = p.batch > 1 && p.sA != 0 ? p.batch : 1;
+    const long long problems_b = p.batch > 1 && p.sB != 0 ? p.batch : 1;
+    const size_t avail = workspace != nullptr ? workspace_bytes : 0;
+    int mask = stage;
+    if (stage < 0) {
+        mask = tc_staging_choice(p.ta, p.tb, p.M, p.N, p.K, problems_a, problems_b,
+                                 aligned16(p.A, p.lda, p.sA, p.batch),
+                                 aligned16(p.B, p.ldb, p.sB, p.batch), avail);
+    } else if (tc_stage_bytes(mask, p.M, p.N, p.K, problems_a, problems_b) > avail) {
+        return FGEMM_ERR_INVALID_VALUE;  // the copies asked for do not fit
+    }
+    if (mask == 0) return run_math(math, p);
+    char *const ws = static_cast<char *>(workspace);
+    const long long ld = ld4(p.K);
+    Problem q = p;
+    if (mask & 1) {
+        // A as M x K rows: transposed when stored K x M, re-pitched when already K-major.
+        float *const Ac = reinterpret_cast<float *>(ws);
+        const long long s = (long long)p.M * ld;
+        const long long sx = problems_a > 1 ? p.sA : 0;
+        st = p.ta == 1 ? launch_stage_transpose(p.A, p.lda, sx, p.K, p.M, (int)problems_a, Ac, ld,
+                                                s, p.stream)
+                       : launch_stage_repitch(p.A, p.lda, sx, p.M, p.K, (int)problems_a, Ac, ld, s,
+                                              p.stream);
+        if (st != FGEMM_OK) return st;
+        q.ta = 0;
+        q.A = Ac;
+        q.lda = ld;
+        q.sA = problems_a > 1 ? s : 0;
+    }
+    if (mask & 2) {
+        // B as N x K rows: transposed when stored K x N, re-pitched when already K-major.
+        const size_t off = (mask & 1) ? tc_stage_bytes(1, p.M, p.N, p.K, problems_a, problems_b) : 0;
+        float *const Bc = reinterpret_cast<float *>(ws + (off + 255) / 256 * 256);
+        const long long s = (long long)p.N * ld;
+        const long long sx = problems_b > 1 ? p.sB : 0;
+        st = p.tb == 0 ? launch_stage_transpose(p.B, p.ldb, sx, p.K, p.N, (int)problems_b, Bc, ld,
+                                                s, p.stream)
+                       : launch_stage_repitch(p.B, p.ldb, sx, p.N, p.K, (int)problems_b, Bc, ld, s,
+                                              p.stream);
+        if (st != FGEMM_OK) return st;
+        q.tb = 1;
+        q.B = Bc;
+        q.ldb = ld;
+        q.sB = problems_b > 1 ? s : 0;
+    }
+    return run_math(math, q);
+}
+
 }  // namespace
 
 fgemm_status splitk_plan(int ta, int tb, int M, int N, int K, float alpha, const float *A, int lda,
@@ -520,6 +624,50 @@ fgemm_status fgemm_sgemm_staged(fgemm_op transa, fgemm_op transb, int M, int N, 
                                           ldb, strideB, beta, C, ldc, strideC, batch, bias,
                                           apply_relu, stream),
                              stage, workspace, workspace_bytes);
+}
+
+size_t fgemm_math_staged_workspace_size(fgemm_math math, fgemm_op transa, fgemm_op transb, int M,
+                                        int N, int K, int batch)
+{
+    if (math == FGEMM_MATH_FP32) return fgemm_staged_workspace_size(transa, transb, M, N, K, batch);
+    if ((math != FGEMM_MATH_TF32 && math != FGEMM_MATH_3XTF32) ||
+        (transa != FGEMM_OP_N && transa != FGEMM_OP_T) ||
+        (transb != FGEMM_OP_N && transb != FGEMM_OP_T) || M <= 0 || N <= 0 || K <= 0 ||
+        batch <= 0)
+        return 0;
+    return fgemm::tc_stage_bytes(3, M, N, K, batch, batch);
+}
+
+int fgemm_math_staged_choice(fgemm_math math, fgemm_op transa, fgemm_op transb, int M, int N,
+                             int K, int batch, int shared_a, int shared_b, int aligned_a,
+                             int aligned_b, size_t workspace_bytes, int num_sms)
+{
+    if (math == FGEMM_MATH_FP32)
+        return fgemm_staged_choice(transa, transb, M, N, K, batch, shared_a, shared_b, aligned_a,
+                                   aligned_b, workspace_bytes, num_sms);
+    if ((math != FGEMM_MATH_TF32 && math != FGEMM_MATH_3XTF32) ||
+        (transa != FGEMM_OP_N && transa != FGEMM_OP_T) ||
+        (transb != FGEMM_OP_N && transb != FGEMM_OP_T) || M < 0 || N < 0 || K < 0 ||
+        batch < 0 || num_sms < 1)
+        return -1;
+    const long long problems_a = batch > 1 && !shared_a ? batch : 1;
+    const long long problems_b = batch > 1 && !shared_b ? batch : 1;
+    return fgemm::tc_staging_choice((int)transa, (int)transb, M, N, K, problems_a, problems_b,
+                                    aligned_a != 0, aligned_b != 0, workspace_bytes);
+}
+
+fgemm_status fgemm_gemm_math_staged(fgemm_math math, fgemm_op transa, fgemm_op transb, int M,
+                                    int N, int K, float alpha, const float *A, int lda,
+                                    long long strideA, const float *B, int ldb, long long strideB,
+                                    float beta, float *C, int ldc, long long strideC, int batch,
+                                    const float *bias, int apply_relu, int stage, void *workspace,
+                                    size_t workspace_bytes, cudaStream_t stream)
+{
+    return fgemm::run_math_staged(math,
+                                  make_problem(transa, transb, M, N, K, alpha, A, lda, strideA, B,
+                                               ldb, strideB, beta, C, ldc, strideC, batch, bias,
+                                               apply_relu, stream),
+                                  stage, workspace, workspace_bytes);
 }
 
 void fgemm_debug_withhold_tensor_core(int k_block, long long wait_limit_ns)

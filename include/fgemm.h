@@ -304,6 +304,48 @@ int fgemm_math_supported(fgemm_math math, fgemm_op transa, fgemm_op transb, int 
                          int ldb, long long strideB, int batch);
 
 /*
+ * fgemm_gemm_math with operand staging through a caller workspace: the tensor-core
+ * counterpart of fgemm_sgemm_staged (with FGEMM_MATH_FP32 it is fgemm_sgemm_staged).
+ * The tcgen05 kernel reads an operand stored K-major (A for transa == N, B for
+ * transb == T) straight from its TMA tiles; with both operands MN-major (transa == T,
+ * transb == N) it also transposes one of them in shared memory and runs at about half
+ * the rate of the other layouts, and an operand whose pointer, leading dimension or
+ * batch stride is not 16-byte aligned keeps the call off the tensor cores.  This call can
+ * first copy operands K-major into `workspace` -- transposed when MN-major, into aligned
+ * rows when already K-major -- and run the tensor-core kernel on the copies.
+ * Result: that of fgemm_gemm_math on the same arguments (the copies are exact), except
+ * that a call whose unaligned operands the copies make aligned runs on the tensor cores
+ * (with their error bound) instead of the CUDA cores.
+ *   stage: -1 lets the library choose among the copies that fit: every operand whose
+ *     alignment keeps the call off the tensor cores (all of them or none), else in a TN
+ *     call the copy of A (so that it runs as NN), or B's when only that fits; otherwise
+ *     a mask of the copies to make -- bit 0 copies A, bit 1 copies B -- whose bytes must
+ *     fit (else FGEMM_ERR_INVALID_VALUE).  Anything outside [-1, 3] returns
+ *     FGEMM_ERR_INVALID_VALUE.
+ *   workspace: as for fgemm_sgemm_staged; fgemm_math_staged_workspace_size(math, ...)
+ *     bytes hold both copies (A as M x K rows, B as N x K rows, each row rounded up to
+ *     a multiple of 4 floats); less limits the choice.  Concurrent calls need workspaces
+ *     of their own.  Checks happen before anything is launched.
+ * A staged call launches one copy kernel per copied operand (and per 65535 problems of
+ * a batch) on `stream`, then the GEMM; it may be captured in a CUDA graph.
+ * fgemm_math_staged_choice (host-only; arguments as for fgemm_staged_choice) gives the
+ * mask stage = -1 would use, or -1 for arguments out of range.
+ */
+size_t fgemm_math_staged_workspace_size(fgemm_math math, fgemm_op transa, fgemm_op transb, int M,
+                                        int N, int K, int batch);
+
+int fgemm_math_staged_choice(fgemm_math math, fgemm_op transa, fgemm_op transb, int M, int N,
+                             int K, int batch, int shared_a, int shared_b, int aligned_a,
+                             int aligned_b, size_t workspace_bytes, int num_sms);
+
+fgemm_status fgemm_gemm_math_staged(fgemm_math math, fgemm_op transa, fgemm_op transb, int M,
+                                    int N, int K, float alpha, const float *A, int lda,
+                                    long long strideA, const float *B, int ldb, long long strideB,
+                                    float beta, float *C, int ldc, long long strideC, int batch,
+                                    const float *bias, int apply_relu, int stage, void *workspace,
+                                    size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Testing only (failure detection without a GPU fault).  Makes later tensor-core
  * launches of this process behave as if the copy of k-block `k_block` never arrived:
  * the producer withholds it, the kernel's bounded wait runs out after

@@ -56,7 +56,8 @@ class Case:
     expect_tc: object = True
     # Not None: call fgemm_sgemm_staged with this stage argument (-1: the model's choice,
     # 0..3: the operands to copy k-major) and a NaN-filled workspace of the size
-    # fgemm_staged_workspace_size gives.
+    # fgemm_staged_workspace_size gives; with math >= 0, fgemm_gemm_math_staged and a
+    # workspace of fgemm_math_staged_workspace_size.
     stage: object = None
     share_a: bool = False  # batch stride 0 for A (every problem reads the same A)
     share_b: bool = False
@@ -133,6 +134,12 @@ def run(case: Case):
     if row_bias is not None:
         fg.sgemm_row_bias_relu(case.ta, case.tb, M, N, K, case.alpha, pA, lda, pB, ldb, case.beta,
                                pC, ldc, prow, case.relu, stream=stream)
+    elif case.math >= 0 and case.stage is not None:
+        ws_bytes = fg.math_staged_workspace_size(case.math, case.ta, case.tb, M, N, K, nb)
+        ws = torch.full((ws_bytes // 4 + 1,), float("nan"), device="cuda")
+        fg.gemm_math_staged(case.math, case.ta, case.tb, M, N, K, case.alpha, pA, lda, sA, pB,
+                            ldb, sB, case.beta, pC, ldc, sC, nb, pbias, case.relu, case.stage, ws,
+                            ws_bytes, stream=stream)
     elif case.math >= 0:
         if case.math != fg.MATH_FP32 and case.expect_tc is not None:
             path = fg.math_supported(case.math, case.ta, case.tb, M, N, K, case.alpha, pA, lda, sA,

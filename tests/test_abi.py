@@ -387,3 +387,59 @@ def test_launch_count_of_a_grid_too_large_for_one_launch():
     assert fg.launch_count(0, 1, 1, fg.MAX_DIM, 128 * 128, 64, 1, 1, 152) == 1
     assert fg.launch_count(0, 1, 1, fg.MAX_DIM, 128 * 128, 64, 2, 1, 152) == 2
     assert fg.launch_count(0, 1, 1, fg.MAX_DIM, 128 * 128 + 1, 64, 1, 1, 152) == 0
+
+
+def test_math_staged_workspace_size_and_choice():
+    sz, ch = fg.math_staged_workspace_size, fg.math_staged_choice
+    # K-major copies: A as M rows and B as N rows of ld4(K) floats a problem, B's at the
+    # next multiple of 256 bytes
+    for math in (fg.MATH_TF32, fg.MATH_3XTF32):
+        assert sz(math, 1, 0, 4096, 4096, 4096, 1) == 2 * 4096 * 4096 * 4
+        assert sz(math, 0, 0, 5, 7, 3, 2) == (2 * 5 * 4 * 4 + 255) // 256 * 256 + 2 * 7 * 4 * 4
+        assert sz(math, 0, 0, 0, 7, 3, 1) == 0 and sz(math, 2, 0, 5, 7, 3, 1) == 0
+    assert sz(fg.MATH_FP32, 0, 0, 5, 7, 3, 2) == fg.staged_workspace_size(0, 0, 5, 7, 3, 2)
+    assert sz(7, 0, 0, 5, 7, 3, 2) == 0
+    assert sz(fg.MATH_TF32, 0, 0, 2**31 - 1, 2**31 - 1, 2**31 - 1, 2**31 - 1) == 2**64 - 1
+    for math in (fg.MATH_TF32, fg.MATH_3XTF32):
+        # aligned operands: only TN is copied (A, so that it runs as NN)
+        got = {(ta, tb): ch(math, ta, tb, 4096, 4096, 4096, 1, 0, 0, 1, 1, 152)
+               for ta in (0, 1) for tb in (0, 1)}
+        assert got == {(0, 0): 0, (0, 1): 0, (1, 0): 1, (1, 1): 0}
+        # an unaligned operand is copied in any layout, two unaligned ones together
+        assert all(ch(math, ta, tb, 512, 512, 512, 1, 0, 0, 0, 1, 152) == 1
+                   for ta in (0, 1) for tb in (0, 1))
+        assert all(ch(math, ta, tb, 512, 512, 512, 1, 0, 0, 1, 0, 152) == 2
+                   for ta in (0, 1) for tb in (0, 1))
+        assert ch(math, 0, 0, 512, 512, 512, 1, 0, 0, 0, 0, 152) == 3
+        # within the workspace: TN falls back to B's copy when only it fits (N < M), two
+        # unaligned operands are copied both or not at all, nothing without a workspace
+        a_only = sz(math, 1, 0, 4096, 1024, 1024, 1) - 1024 * 1024 * 4
+        assert ch(math, 1, 0, 4096, 1024, 1024, 1, 0, 0, 1, 1, 152, 1024 * 1024 * 4) == 2
+        assert ch(math, 1, 0, 4096, 1024, 1024, 1, 0, 0, 1, 1, 152, a_only) == 1
+        assert ch(math, 0, 0, 512, 512, 512, 1, 0, 0, 0, 0, 152, 512 * 512 * 4) == 0
+        assert ch(math, 1, 0, 4096, 4096, 4096, 1, 0, 0, 1, 1, 152, 0) == 0
+        # a batch that shares A copies it once
+        one = ch(math, 1, 0, 256, 256, 256, 8, 1, 0, 1, 1, 152, 256 * 256 * 4)
+        assert one == 1 and ch(math, 1, 0, 256, 256, 256, 8, 0, 0, 1, 1, 152, 256 * 256 * 4) == 0
+    assert ch(fg.MATH_FP32, 0, 0, 4096, 4096, 4096, 1, 0, 0, 1, 1, 152) == \
+        fg.staged_choice(0, 0, 4096, 4096, 4096, 1, 0, 0, 1, 1, 152)
+    assert ch(7, 0, 0, 4, 4, 4, 1, 0, 0, 1, 1, 152) == -1
+    assert ch(fg.MATH_TF32, 0, 0, -1, 4, 4, 1, 0, 0, 1, 1, 152) == -1
+
+
+def test_math_staged_argument_checks_before_launch():
+    M = N = K = 256
+    args = (0, 0, M, N, K, 1.0, FAKE, K, 0, FAKE, N, 0, 0.0, FAKE, N, 0, 1, None, False)
+    need_a = M * K * 4
+    for math in (fg.MATH_TF32, fg.MATH_3XTF32):
+        bad = [dict(stage=1, ws=None, wb=0), dict(stage=3, ws=FAKE, wb=need_a),
+               dict(stage=-1, ws=FAKE + 4, wb=need_a), dict(stage=4, ws=FAKE, wb=need_a),
+               dict(stage=-2, ws=FAKE, wb=need_a)]
+        for kw in bad:
+            assert fg.gemm_math_staged(math, *args, kw["stage"], kw["ws"], kw["wb"],
+                                       check=False) == fg.ERR_INVALID_VALUE, kw
+        bad_ld = (0, 0, M, N, K, 1.0, FAKE, K - 1, 0, FAKE, N, 0, 0.0, FAKE, N, 0, 1, None, False)
+        assert fg.gemm_math_staged(math, *bad_ld, -1, None, 0, check=False) == fg.ERR_INVALID_VALUE
+        empty = (0, 0, 0, N, K, 1.0, None, K, 0, None, N, 0, 0.0, None, N, 0, 1, None, False)
+        assert fg.gemm_math_staged(math, *empty, -1, None, 0, check=False) == fg.OK
+    assert fg.gemm_math_staged(5, *args, -1, None, 0, check=False) == fg.ERR_INVALID_VALUE
