@@ -3,7 +3,8 @@
 Every call is asynchronous on the caller's stream and allocates nothing, so it can be
 captured.  The cases cover one launch per call (whole tiles), the two-launch last-wave
 splits (quarter tiles, and k-slice clusters launched with a cluster dimension), the
-split-K path with its reduction kernel, and the tensor-core kernel; replays must give
+split-K path with its reduction kernel, the tensor-core kernel, and the staged
+tensor-core call (a copy kernel, then the tensor-core kernel); replays must give
 the eager result bit for bit, and integer data makes both exact.
 """
 
@@ -97,3 +98,20 @@ def test_tensor_core_path_replays(math):
         lambda: fg.gemm_math(mode, 0, 0, M, N, K, 1.0, A, K, 0, B, N, 0, 0.0, C, N, 0, 1), C)
     # small integers are exact in TF32
     assert torch.equal(C, (A.double() @ B.double()).float())
+
+
+@pytest.mark.parametrize("math", ["tf32", "3xtf32"])
+def test_staged_tensor_core_call_replays(math):
+    # TN: the copy of A (K x M stored) into the workspace, then the tensor-core kernel
+    M, N, K = 640, 768, 256
+    At, B = _ints((K, M), 10), _ints((K, N), 11)
+    C = torch.empty(M, N, device="cuda")
+    mode = fg.MATH_TF32 if math == "tf32" else fg.MATH_3XTF32
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert fg.math_staged_choice(mode, 1, 0, M, N, K, 1, False, False, True, True, sms) == 1
+    need = fg.math_staged_workspace_size(mode, 1, 0, M, N, K, 1)
+    ws = torch.empty(need // 4, device="cuda")
+    _capture_and_compare(
+        lambda: fg.gemm_math_staged(mode, 1, 0, M, N, K, 1.0, At, M, 0, B, N, 0, 0.0, C, N, 0, 1,
+                                    None, False, fg.STAGE_AUTO, ws, need), C)
+    assert torch.equal(C, (At.double().t() @ B.double()).float())
